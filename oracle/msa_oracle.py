@@ -1,0 +1,278 @@
+"""fp64 CPU oracle for block-sparse paged MSA attention.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg may import this module.  The CUDA path never does, and this module
+imports nothing from it: the two share no code.  It is plain, slow and meant to
+be read against the method's description:
+
+* MiniMax-M3 sparse attention as wired by sglang ``minimax_sparse_backend.py``
+  (``MiniMaxSparseAttnBackend.__init__``: block size, init / local / top-k block
+  counts and the index score type; ``forward_decode`` / ``forward_extend``: the
+  cache write precedes attention, then index scoring, top-k block selection and
+  attention over the selected blocks) and by vLLM
+  ``minimax_m3/nvidia/sparse_attention_msa.py`` (``MiniMaxM3SparseMSAImpl.forward``:
+  per-token, per-KV-head selected block lists, GQA with ``qhead_per_kv`` query
+  heads per KV head, ``build_k2q_csr`` key-block-to-query lists for prefill).
+* The pages leave the index score formula open (only ``score_type`` is named);
+  the specification of this build fixes it: a block's score is the maximum over
+  its visible tokens of ``idx_q . idx_k``, and ties go to the lower block index.
+
+Every quantity is computed in float64 from exact copies of the inputs (bf16 and
+e4m3 values are exactly representable in float64).
+
+Notation: P = block size (= page size, 128), H_kv KV heads, G = H_q / H_kv query
+heads per KV head, D head dim, d index dim.  A query token of request r with
+n_q new tokens, the i-th of them, sits at position p = seq_len_r - n_q + i and
+sees tokens [0, p]; it has nb = floor(p / P) + 1 visible blocks.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+against brute force, hand-computed selections, closed forms or an independent
+library routine; no function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Sequence, Tuple
+
+import numpy as np
+
+__all__ = [
+    "init_blocks_from_tokens", "local_blocks_from_tokens", "e4m3_to_float",
+    "query_positions", "gather_sequence", "block_scores", "select_blocks",
+    "attention", "combine", "sparse_attention", "build_k2q_csr",
+]
+
+
+# --------------------------------------------------------------------------
+# Sparse configuration (sglang MiniMaxSparseAttnBackend.__init__)
+# --------------------------------------------------------------------------
+def init_blocks_from_tokens(init_tokens: int, block_size: int) -> int:
+    """``sparse_init_tokens`` -> init block count: ceil(tokens / block)."""
+    return -(-init_tokens // block_size)
+
+
+def local_blocks_from_tokens(local_tokens: int, block_size: int) -> int:
+    """``sparse_local_tokens`` -> local block count: ceil(tokens / block) + 1.
+
+    The extra block is the query's own, partially filled block."""
+    return -(-local_tokens // block_size) + 1
+
+
+# --------------------------------------------------------------------------
+# fp8 e4m3 ("fn": no infinities, one NaN per sign) decode, from the format's
+# definition: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0
+# is subnormal (m/8 * 2^-6); exponent 15 with mantissa 7 is NaN.  The vLLM page
+# stores fp8 KV caches as raw e4m3 with per-layer float scales
+# (MiniMaxM3SparseMSAImpl.forward, ``_k_scale`` / ``_v_scale``).
+# --------------------------------------------------------------------------
+def _e4m3_value(code: int) -> float:
+    sign = -1.0 if code & 0x80 else 1.0
+    exp = (code >> 3) & 0xF
+    man = code & 0x7
+    if exp == 0xF and man == 0x7:
+        return math.nan
+    if exp == 0:
+        return sign * (man / 8.0) * 2.0 ** -6
+    return sign * (1.0 + man / 8.0) * 2.0 ** (exp - 7)
+
+
+_E4M3_TABLE = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def e4m3_to_float(codes: np.ndarray) -> np.ndarray:
+    """Decode uint8 e4m3 codes to float64."""
+    return _E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+# --------------------------------------------------------------------------
+# Geometry of query tokens
+# --------------------------------------------------------------------------
+def query_positions(seq_lens: Sequence[int], q_lens: Sequence[int]) -> List[Tuple[int, int]]:
+    """(request, position) of every query token, token-major.
+
+    ``seq_lens[r]`` counts request r's KV tokens including its ``q_lens[r]`` new
+    ones (the fused cache write runs before attention in ``forward_decode`` and
+    ``forward_extend``), so the i-th new token is at seq_len - q_len + i."""
+    out = []
+    for r, (L, n) in enumerate(zip(seq_lens, q_lens)):
+        L, n = int(L), int(n)
+        assert 0 <= n <= L, (r, L, n)
+        for i in range(n):
+            out.append((r, L - n + i))
+    return out
+
+
+def gather_sequence(pages: np.ndarray, block_table_row: Sequence[int], n_tokens: int,
+                    block_size: int) -> np.ndarray:
+    """Dense gather through the block table: logical token t of a request lives
+    in page ``block_table_row[t // P]`` at row ``t % P``.
+
+    ``pages``: [num_pages, H, P, X] (any float dtype).  Returns [n_tokens, H, X]
+    float64 in logical token order."""
+    H, X = pages.shape[1], pages.shape[3]
+    seq = np.empty((n_tokens, H, X), dtype=np.float64)
+    for t0 in range(0, n_tokens, block_size):
+        page = int(block_table_row[t0 // block_size])
+        assert 0 <= page < pages.shape[0], f"block {t0 // block_size}: page {page}"
+        n = min(block_size, n_tokens - t0)
+        # [H, n, X] -> [n, H, X]
+        seq[t0:t0 + n] = np.transpose(pages[page, :, :n, :], (1, 0, 2))
+    return seq
+
+
+# --------------------------------------------------------------------------
+# Index score: score_j = max over visible tokens t of block j of idx_q . idx_k[t]
+# --------------------------------------------------------------------------
+def block_scores(idx_q_vec: np.ndarray, idx_k_seq: np.ndarray, position: int,
+                 block_size: int) -> np.ndarray:
+    """Scores of the visible blocks of one query token and one KV head.
+
+    ``idx_q_vec``: [d]; ``idx_k_seq``: [>= position + 1, d] (logical order).
+    Returns [nb] float64 with nb = position // P + 1; only tokens t <= position
+    take part (the last visible block may be partial)."""
+    nb = position // block_size + 1
+    dots = idx_k_seq[:position + 1].astype(np.float64) @ idx_q_vec.astype(np.float64)
+    scores = np.empty(nb, dtype=np.float64)
+    for j in range(nb):
+        scores[j] = dots[j * block_size:min((j + 1) * block_size, position + 1)].max()
+    return scores
+
+
+# --------------------------------------------------------------------------
+# Block selection: init blocks  U  local blocks  U  top-k of the rest
+# --------------------------------------------------------------------------
+def select_blocks(scores: Sequence[float], init_blocks: int, local_blocks: int,
+                  topk_blocks: int) -> List[int]:
+    """Selected blocks of one (query token, KV head), ascending.
+
+    I  = [0, min(init, nb))              mandatory init (sink) blocks
+    Lc = [max(0, nb - local), nb)        mandatory local window, incl. the
+                                         query's own block
+    C  = [0, nb) minus I minus Lc        candidates
+    Top = first min(topk, |C|) of C sorted by (score descending, index ascending)
+    Result: sorted(I | Lc | Top), of size min(nb, init + local + topk)."""
+    nb = len(scores)
+    I = set(range(0, min(init_blocks, nb)))
+    Lc = set(range(max(0, nb - local_blocks), nb))
+    C = [j for j in range(nb) if j not in I and j not in Lc]
+    ranked = sorted(C, key=lambda j: (-float(scores[j]), j))
+    top = set(ranked[:min(topk_blocks, len(C))])
+    return sorted(I | Lc | top)
+
+
+# --------------------------------------------------------------------------
+# Attention: textbook softmax over a set of key/value rows
+# --------------------------------------------------------------------------
+def attention(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray,
+              scale: float) -> Tuple[np.ndarray, np.ndarray]:
+    """out[g] = sum_t softmax_t(scale q_g . k_t) v_t; lse[g] = ln sum_t exp(scale q_g . k_t).
+
+    ``q_rows``: [G, D]; ``k``, ``v``: [n, D].  n = 0 gives out = 0, lse = -inf
+    (the idle / empty-request convention of ``forward_decode``)."""
+    q_rows = np.asarray(q_rows, dtype=np.float64)
+    G = q_rows.shape[0]
+    if k.shape[0] == 0:
+        return np.zeros((G, v.shape[1])), np.full(G, -np.inf)
+    s = scale * (q_rows @ np.asarray(k, dtype=np.float64).T)       # [G, n]
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    l = e.sum(axis=1, keepdims=True)
+    out = (e @ np.asarray(v, dtype=np.float64)) / l
+    lse = (m + np.log(l))[:, 0]
+    return out, lse
+
+
+def combine(o_parts: np.ndarray, lse_parts: np.ndarray) -> Tuple[np.ndarray, float]:
+    """Merge attention results over disjoint key sets (split-K flash decoding):
+    lse = ln sum_s exp(lse_s); out = sum_s exp(lse_s - lse) o_s.
+    Parts with lse = -inf (empty) carry no weight; all empty -> (0, -inf)."""
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    if lse_parts.size == 0 or np.all(np.isneginf(lse_parts)):
+        return np.zeros(o_parts.shape[1:]), -np.inf
+    m = lse_parts.max()
+    w = np.exp(lse_parts - m)
+    lse = m + math.log(w.sum())
+    out = np.tensordot(np.exp(lse_parts - lse), o_parts, axes=(0, 0))
+    return out, lse
+
+
+# --------------------------------------------------------------------------
+# The whole path for a batch of query tokens
+# --------------------------------------------------------------------------
+def sparse_attention(*, seq_lens, q_lens, block_table, idx_q, idx_k_pages, q,
+                     k_pages, v_pages, num_kv_heads: int, block_size: int,
+                     init_blocks: int, local_blocks: int, topk_blocks: int,
+                     softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
+                     kv_is_e4m3: bool = False, tokens=None,
+                     kv_heads=None) -> Dict[str, object]:
+    """Index score -> block selection -> attention over the selected blocks.
+
+    Arrays are numpy: ``idx_q [T, H_kv, d]``, ``idx_k_pages [pages, H_kv, P, d]``,
+    ``q [T, H_q, D]``, ``k_pages / v_pages [pages, H_kv, P, D]`` (float, or uint8
+    e4m3 codes when ``kv_is_e4m3``; dequantised value = decoded code * scale).
+    ``tokens`` / ``kv_heads`` restrict the work to a sample (default: all).
+
+    Returns dict with, per computed (t, h): ``scores[(t, h)]`` [nb],
+    ``selected[(t, h)]`` list, and arrays ``out [T, H_q, D]``, ``lse [T, H_q]``
+    (NaN where not computed)."""
+    T, H_q, D = q.shape
+    G = H_q // num_kv_heads
+    toks = query_positions(seq_lens, q_lens)
+    assert len(toks) == T
+    tokens = range(T) if tokens is None else tokens
+    kv_heads = range(num_kv_heads) if kv_heads is None else kv_heads
+    out = np.full((T, H_q, D), np.nan)
+    lse = np.full((T, H_q), np.nan)
+    scores, selected = {}, {}
+    seq_cache = {}
+    for t in tokens:
+        r, p = toks[t]
+        if r not in seq_cache:
+            L = int(seq_lens[r])
+            ik = gather_sequence(idx_k_pages, block_table[r], L, block_size)
+            kk = gather_sequence(k_pages, block_table[r], L, block_size)
+            vv = gather_sequence(v_pages, block_table[r], L, block_size)
+            if kv_is_e4m3:
+                kk = e4m3_to_float(kk.astype(np.uint8)) * k_scale
+                vv = e4m3_to_float(vv.astype(np.uint8)) * v_scale
+            seq_cache = {r: (ik, kk, vv)}
+        ik, kk, vv = seq_cache[r]
+        for h in kv_heads:
+            sc = block_scores(idx_q[t, h], ik[:, h, :], p, block_size)
+            sel = select_blocks(sc, init_blocks, local_blocks, topk_blocks)
+            scores[(t, h)] = sc
+            selected[(t, h)] = sel
+            rows = [tt for j in sel
+                    for tt in range(j * block_size, min((j + 1) * block_size, p + 1))]
+            o, ls = attention(q[t, h * G:(h + 1) * G], kk[rows, h, :], vv[rows, h, :],
+                              softmax_scale)
+            out[t, h * G:(h + 1) * G] = o
+            lse[t, h * G:(h + 1) * G] = ls
+    return {"scores": scores, "selected": selected, "out": out, "lse": lse}
+
+
+# --------------------------------------------------------------------------
+# Key-block -> query CSR for prefill (vLLM MiniMaxM3SparseMSAImpl.forward,
+# ``build_k2q_csr``).  Row (h, r, j) lists, ascending, the query tokens of
+# request r whose selection for KV head h contains key block j.  Rows are laid
+# out on the fixed grid row = (h * num_reqs + r) * max_blocks + j, so the
+# structure's shape depends only on sizes, never on data.
+# --------------------------------------------------------------------------
+def build_k2q_csr(selected: np.ndarray, token_request: Sequence[int], num_reqs: int,
+                  max_blocks: int) -> Tuple[np.ndarray, np.ndarray]:
+    """``selected``: [T, H_kv, S] int (-1 padded).  Returns (row_ptr
+    [H_kv * num_reqs * max_blocks + 1], q_indices [row_ptr[-1]])."""
+    T, H, S = selected.shape
+    rows: List[List[int]] = [[] for _ in range(H * num_reqs * max_blocks)]
+    for t in range(T):
+        r = int(token_request[t])
+        for h in range(H):
+            for j in selected[t, h]:
+                if j >= 0:
+                    rows[(h * num_reqs + r) * max_blocks + int(j)].append(t)
+    row_ptr = np.zeros(len(rows) + 1, dtype=np.int64)
+    for i, lst in enumerate(rows):
+        row_ptr[i + 1] = row_ptr[i] + len(lst)
+    q_indices = np.array([t for lst in rows for t in sorted(lst)], dtype=np.int64)
+    return row_ptr, q_indices

@@ -1,0 +1,426 @@
+"""Pins of the fp64 oracle to facts other than itself (no GPU needed).
+
+Each test checks one oracle function against brute force, a hand-computed
+fixture, a closed form, an invariant of the mathematics, or an independent
+library routine, so that a dropped term, a wrong sign, an off-by-one or a
+transposed operand anywhere in the oracle fails at least one of them.  The
+mutation tests at the bottom plant such mistakes in the oracle (on the CPU) and
+check that the pins catch them."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from block_sparse_paged_msa_gb300 import workloads as wl
+from oracle_io import oracle_local_blocks, run_oracle, to_np
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- config
+def test_block_counts_from_tokens():
+    g = _golden("config_resolution.json")
+    P = g["block_size"]
+    for tokens, blocks in g["local"]:
+        assert oracle.local_blocks_from_tokens(tokens, P) == blocks, tokens
+    for tokens, blocks in g["init"]:
+        assert oracle.init_blocks_from_tokens(tokens, P) == blocks, tokens
+
+
+# ---------------------------------------------------------------- fp8
+def test_e4m3_decode_matches_torch_and_known_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_to_float(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    known = {0x00: 0.0, 0x38: 1.0, 0xB8: -1.0, 0x7E: 448.0, 0xFE: -448.0,
+             0x01: 2.0 ** -9, 0x08: 2.0 ** -6, 0x07: 7 * 2.0 ** -9, 0x40: 2.0,
+             0x3C: 1.5, 0x30: 0.5}
+    for c, v in known.items():
+        assert ours[c] == v, hex(c)
+    assert math.isnan(ours[0x7F]) and math.isnan(ours[0xFF])
+
+
+# ---------------------------------------------------------------- geometry
+def test_query_positions_decode_verify_prefill():
+    assert oracle.query_positions([1000, 1500], [1, 1]) == [(0, 999), (1, 1499)]
+    assert oracle.query_positions([10], [4]) == [(0, 6), (0, 7), (0, 8), (0, 9)]
+    assert oracle.query_positions([5, 3], [2, 3]) == [(0, 3), (0, 4), (1, 0), (1, 1), (1, 2)]
+    assert oracle.query_positions([7], [0]) == []
+
+
+def test_gather_sequence_follows_block_table():
+    rng = np.random.default_rng(0)
+    P, H, X, pages = 4, 2, 3, 6
+    logical = rng.integers(-50, 50, size=(21, H, X)).astype(np.float64)
+    table = [4, 0, 5, 2, 1, 3]
+    pool = np.full((pages, H, P, X), np.nan)
+    for t in range(21):
+        pool[table[t // P], :, t % P, :] = logical[t]
+    got = oracle.gather_sequence(pool, table, 21, P)
+    assert np.array_equal(got, logical)
+
+
+# ---------------------------------------------------------------- scores
+def _paged(logical, P, rng, extra_pages=3):
+    """Scatter a logical [L, H, X] sequence into a shuffled pool."""
+    L, H, X = logical.shape
+    nb = -(-L // P)
+    pages = nb + extra_pages
+    perm = rng.permutation(pages)[:nb]
+    pool = rng.standard_normal((pages, H, P, X)) * 1e6  # garbage outside
+    for t in range(L):
+        pool[perm[t // P], :, t % P, :] = logical[t]
+    return pool, perm
+
+
+def test_block_scores_exact_against_integer_brute_force():
+    rng = np.random.default_rng(1)
+    P, d, L = 8, 5, 61
+    for trial in range(5):
+        ik = rng.integers(-4, 5, size=(L, 1, d))
+        iq = rng.integers(-4, 5, size=d)
+        pool, table = _paged(ik.astype(np.float64), P, rng)
+        seq = oracle.gather_sequence(pool, table, L, P)
+        for pos in (L - 1, 40, 8, 7, 0):
+            got = oracle.block_scores(iq.astype(np.float64), seq[:, 0, :], pos, P)
+            # pure-Python integer arithmetic straight on the logical sequence
+            nb = pos // P + 1
+            want = []
+            for j in range(nb):
+                best = None
+                for t in range(j * P, min(j * P + P, pos + 1)):
+                    dot = sum(int(iq[k]) * int(ik[t, 0, k]) for k in range(d))
+                    best = dot if best is None else max(best, dot)
+                want.append(best)
+            assert got.tolist() == want, (trial, pos)
+
+
+# ---------------------------------------------------------------- selection
+@pytest.mark.parametrize("case", _golden("selection_cases.json")["cases"],
+                         ids=lambda c: c["name"])
+def test_selection_hand_computed(case):
+    P, L, d = case["block_size"], case["n_tokens"], 4
+    ik = np.zeros((L, 1, d))
+    for t, val in case["planted"].items():
+        ik[int(t), 0, 0] = val
+    iq = np.zeros(d)
+    iq[0] = case["q0"]
+    rng = np.random.default_rng(7)
+    pool, table = _paged(ik, P, rng)
+    seq = oracle.gather_sequence(pool, table, L, P)
+    scores = oracle.block_scores(iq, seq[:, 0, :], case["position"], P)
+    assert scores.tolist() == case["scores"]
+    sel = oracle.select_blocks(scores, case["init"], case["local"], case["topk"])
+    assert sel == case["selected"]
+
+
+def _random_scores(rng, nb, distinct):
+    return rng.integers(-distinct, distinct + 1, size=nb).astype(np.float64)
+
+
+def test_selection_invariants_random():
+    rng = np.random.default_rng(2)
+    for _ in range(400):
+        nb = int(rng.integers(1, 70))
+        init, local, topk = (int(rng.integers(0, 4)), int(rng.integers(1, 5)),
+                             int(rng.integers(0, 20)))
+        scores = _random_scores(rng, nb, int(rng.integers(0, 6)))  # many ties
+        sel = oracle.select_blocks(scores, init, local, topk)
+        I = set(range(min(init, nb)))
+        Lc = set(range(max(0, nb - local), nb))
+        assert sel == sorted(set(sel)), "ascending, unique"
+        assert I | Lc <= set(sel), "superset of init and local"
+        assert len(sel) == min(nb, init + local + topk), "size"
+        cand_sel = [j for j in sel if j not in I | Lc]
+        cand_rest = [j for j in range(nb) if j not in I | Lc and j not in sel]
+        for a in cand_sel:
+            for b in cand_rest:
+                # every chosen candidate beats every rejected one, lower index on ties
+                assert (scores[a], -a) > (scores[b], -b)
+
+
+def test_selection_against_exhaustive_subset_search():
+    """Brute force: among all candidate subsets of the right size, the selected one
+    maximises the sorted score vector, then prefers the lexicographically smallest
+    index set."""
+    rng = np.random.default_rng(3)
+    for _ in range(60):
+        nb = int(rng.integers(4, 11))
+        init, local, topk = 1, 2, int(rng.integers(1, 4))
+        scores = _random_scores(rng, nb, 2)
+        cands = list(range(init, nb - local))
+        k = min(topk, len(cands))
+        best = None
+        for sub in itertools.combinations(cands, k):
+            key = (sorted((scores[j] for j in sub), reverse=True),
+                   [-j for j in sub])
+            if best is None or key > best[0]:
+                best = (key, sub)
+        want = sorted(set(range(init)) | set(range(nb - local, nb)) | set(best[1]))
+        assert oracle.select_blocks(scores, init, local, topk) == want
+
+
+# ---------------------------------------------------------------- attention
+def _dense_reference(q_rows, k, v, scale):
+    s = scale * (q_rows @ k.T)
+    return scipy.special.softmax(s, axis=1) @ v, scipy.special.logsumexp(s, axis=1)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((3, 16))
+    k = rng.standard_normal((9, 16))
+    # single key: out = v, lse = its logit
+    o, l = oracle.attention(q, k[:1], k[1:2], 0.3)
+    assert np.allclose(o, np.repeat(k[1:2], 3, 0), atol=0, rtol=0)
+    assert np.allclose(l, 0.3 * q @ k[0], atol=1e-15)
+    # softmax weights sum to one: v = ones -> out = 1
+    o, l = oracle.attention(q, k, np.ones((9, 5)), 0.25)
+    assert np.allclose(o, 1.0, atol=1e-15)
+    # lse bounds: max s <= lse <= max s + ln n
+    s = 0.25 * q @ k.T
+    assert np.all(l >= s.max(1) - 1e-15) and np.all(l <= s.max(1) + math.log(9) + 1e-15)
+    # shift invariance: an extra coordinate adds c/scale * 1 to every logit
+    v = rng.standard_normal((9, 4))
+    o1, l1 = oracle.attention(q, k, v, 0.5)
+    c = 1.7
+    q2 = np.concatenate([q, np.full((3, 1), c / 0.5)], 1)
+    k2 = np.concatenate([k, np.ones((9, 1))], 1)
+    o2, l2 = oracle.attention(q2, k2, v, 0.5)
+    assert np.allclose(o1, o2, atol=1e-13) and np.allclose(l2, l1 + c, atol=1e-13)
+    # empty key set: zeros and -inf
+    o, l = oracle.attention(q, k[:0], v[:0], 0.5)
+    assert np.all(o == 0) and np.all(np.isneginf(l))
+    # matches scipy's softmax / logsumexp
+    o, l = oracle.attention(q, k, v, 0.5)
+    ro, rl = _dense_reference(q, k, v, 0.5)
+    assert np.allclose(o, ro, atol=1e-13) and np.allclose(l, rl, atol=1e-13)
+    # a transposed / permuted operand is caught: q rows are not interchangeable
+    assert not np.allclose(oracle.attention(q[::-1], k, v, 0.5)[0], o)
+
+
+def test_combine_equals_unsplit():
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((4, 8))
+    k = rng.standard_normal((50, 8)) * 3
+    v = rng.standard_normal((50, 8))
+    o_all, l_all = oracle.attention(q, k, v, 0.7)
+    for cuts in ([25], [1, 2, 49], [10, 20, 30, 40], [0, 50]):
+        bounds = [0] + cuts + [50]
+        parts = [(a, b) for a, b in zip(bounds[:-1], bounds[1:])]
+        for g in range(4):
+            os_, ls_ = [], []
+            for a, b in parts:
+                o, l = oracle.attention(q[g:g + 1], k[a:b], v[a:b], 0.7)
+                os_.append(o[0])
+                ls_.append(l[0])
+            o, l = oracle.combine(np.array(os_), np.array(ls_))
+            assert np.allclose(o, o_all[g], atol=1e-12) and abs(l - l_all[g]) < 1e-12
+    o, l = oracle.combine(np.zeros((3, 8)), np.full(3, -np.inf))
+    assert np.all(o == 0) and np.isneginf(l)
+
+
+# ---------------------------------------------------------------- whole path
+def _logical_sequences(w):
+    """Per request: logical idx_k, k, v in token order, read from the pool with
+    torch indexing (independent of the oracle's gather)."""
+    out = []
+    P = w.spec.block_size
+    for r in range(w.spec.batch):
+        L = int(w.seq_lens[r])
+        nb = -(-L // P)
+        pages = w.block_table[r, :nb].long()
+        def seq(pool):
+            x = pool[pages]                               # [nb, H, P, X]
+            return x.permute(0, 2, 1, 3).reshape(nb * P, *x.shape[1:2], x.shape[3])[:L]
+        out.append((to_np(seq(w.idx_k_pages)), to_np(seq(w.k_pages)), to_np(seq(w.v_pages))))
+    return out
+
+
+def test_dense_when_topk_covers_every_block():
+    """topk >= nb - init - local: every visible token is attended, so the result
+    is plain causal attention (scipy softmax) over the logical sequence."""
+    spec = wl.small("verify", topk_blocks=64, num_kv_heads=2, num_q_heads=6)
+    w = wl.make_workload(spec)
+    res = run_oracle(w)
+    seqs = _logical_sequences(w)
+    q = to_np(w.q)
+    G = spec.group
+    for t, (r, p) in enumerate(oracle.query_positions(to_np(w.seq_lens), to_np(w.q_lens))):
+        _, k, v = seqs[r]
+        for h in range(spec.num_kv_heads):
+            ro, rl = _dense_reference(q[t, h * G:(h + 1) * G], k[:p + 1, h], v[:p + 1, h],
+                                      spec.softmax_scale)
+            assert np.allclose(res["out"][t, h * G:(h + 1) * G], ro, atol=1e-12)
+            assert np.allclose(res["lse"][t, h * G:(h + 1) * G], rl, atol=1e-12)
+            assert res["selected"][(t, h)] == list(range(p // 128 + 1))
+
+
+def test_sparse_equals_dense_over_selected_tokens():
+    """With a real top-k the output equals dense attention restricted to the
+    tokens of the selected blocks (re-derived here by masking logits)."""
+    spec = wl.small("medium_decode", num_kv_heads=2, num_q_heads=4, batch=2)
+    w = wl.make_workload(spec)
+    res = run_oracle(w)
+    seqs = _logical_sequences(w)
+    q = to_np(w.q)
+    for t, (r, p) in enumerate(oracle.query_positions(to_np(w.seq_lens), to_np(w.q_lens))):
+        _, k, v = seqs[r]
+        for h in range(2):
+            sel = res["selected"][(t, h)]
+            assert len(sel) == min(p // 128 + 1, spec.init_blocks
+                                   + oracle_local_blocks(w) + spec.topk_blocks)
+            s = spec.softmax_scale * q[t, 2 * h:2 * h + 2] @ k[:p + 1, h].T
+            mask = np.full(p + 1, -np.inf)
+            for j in sel:
+                mask[j * 128:(j + 1) * 128] = 0.0
+            s = s + mask
+            ro = scipy.special.softmax(s, axis=1) @ v[:p + 1, h]
+            assert np.allclose(res["out"][t, 2 * h:2 * h + 2], ro, atol=1e-12)
+            assert np.allclose(res["lse"][t, 2 * h:2 * h + 2],
+                               scipy.special.logsumexp(s, axis=1), atol=1e-12)
+
+
+def test_page_permutation_invariance():
+    spec = wl.small("medium_decode", batch=3, num_kv_heads=2, num_q_heads=4)
+    w = wl.make_workload(spec)
+    res = run_oracle(w)
+    rng = np.random.default_rng(8)
+    perm = torch.from_numpy(rng.permutation(spec.num_pages))     # new = perm[old]
+    inv = torch.argsort(perm)
+    w2 = wl.Workload(**{**w.__dict__})
+    w2.idx_k_pages = w.idx_k_pages[inv]
+    w2.k_pages = w.k_pages[inv]
+    w2.v_pages = w.v_pages[inv]
+    bt = w.block_table.clone()
+    valid = bt >= 0
+    bt[valid] = perm[bt[valid].long()].to(torch.int32)
+    w2.block_table = bt
+    res2 = run_oracle(w2)
+    assert res["selected"] == res2["selected"]
+    assert np.array_equal(res["out"], res2["out"]) and np.array_equal(res["lse"], res2["lse"])
+
+
+def test_fp8_path_uses_dequantised_values():
+    spec = wl.small("fp8_decode", batch=2, num_kv_heads=1, num_q_heads=4)
+    w = wl.make_workload(spec)
+    res = run_oracle(w)
+    w2 = wl.Workload(**{**w.__dict__})
+    w2.k_pages = (w.k_pages.to(torch.float64) * spec.kv_scale)
+    w2.v_pages = (w.v_pages.to(torch.float64) * spec.kv_scale)
+    w2.spec = spec.replace(kv_dtype="bf16")
+    res2 = run_oracle(w2)
+    assert res["selected"] == res2["selected"]
+    assert np.allclose(res["out"], res2["out"], atol=1e-13)
+    assert np.allclose(res["lse"], res2["lse"], atol=1e-13)
+
+
+def test_k2q_csr_round_trip():
+    rng = np.random.default_rng(9)
+    T, H, S, R, NB = 40, 3, 5, 3, 12
+    tok_req = np.sort(rng.integers(0, R, size=T))
+    sel = np.full((T, H, S), -1)
+    for t in range(T):
+        for h in range(H):
+            n = int(rng.integers(0, S + 1))
+            sel[t, h, :n] = np.sort(rng.choice(NB, size=n, replace=False))
+    row_ptr, qi = oracle.build_k2q_csr(sel, tok_req, R, NB)
+    assert row_ptr[0] == 0 and np.all(np.diff(row_ptr) >= 0)
+    assert row_ptr[-1] == (sel >= 0).sum() == len(qi)
+    back = {}
+    for h in range(H):
+        for r in range(R):
+            for j in range(NB):
+                row = (h * R + r) * NB + j
+                lst = qi[row_ptr[row]:row_ptr[row + 1]].tolist()
+                assert lst == sorted(lst)
+                for t in lst:
+                    assert tok_req[t] == r
+                    back.setdefault((t, h), []).append(j)
+    for t in range(T):
+        for h in range(H):
+            assert sorted(back.get((t, h), [])) == [j for j in sel[t, h] if j >= 0]
+
+
+# ---------------------------------------------------------------- mutations
+def _mutants():
+    """Plausible mistakes, each planted in a copy of one oracle function."""
+    real_scores, real_select = oracle.block_scores, oracle.select_blocks
+    real_attn, real_combine = oracle.attention, oracle.combine
+
+    def scores_sum(q, seq, pos, P):      # sum instead of max
+        nb = pos // P + 1
+        dots = seq[:pos + 1] @ q
+        return np.array([dots[j * P:(j + 1) * P].sum() for j in range(nb)])
+
+    def scores_no_causal(q, seq, pos, P):  # last block not masked at the position
+        nb = pos // P + 1
+        dots = seq @ q
+        return np.array([dots[j * P:(j + 1) * P].max() for j in range(nb)])
+
+    def select_high_tie(scores, i, l, k):  # ties toward the higher index
+        nb = len(scores)
+        I = set(range(min(i, nb))); L = set(range(max(0, nb - l), nb))
+        C = [j for j in range(nb) if j not in I | L]
+        top = sorted(C, key=lambda j: (-scores[j], -j))[:k]
+        return sorted(I | L | set(top))
+
+    def select_local_off_by_one(scores, i, l, k):
+        return real_select(scores, i, l - 1, k + 1)
+
+    def attn_no_scale(q, k, v, scale):
+        return real_attn(q, k, v, 1.0)
+
+    def attn_transposed_v(q, k, v, scale):
+        o, l = real_attn(q, k, v, scale)
+        return o[:, ::-1], l
+
+    def combine_lse_is_max(o, l):        # drops the log-sum term of the lse
+        out, _ = real_combine(o, l)
+        return out, float(np.max(l))
+
+    return [("block_scores", scores_sum), ("block_scores", scores_no_causal),
+            ("select_blocks", select_high_tie), ("select_blocks", select_local_off_by_one),
+            ("attention", attn_no_scale), ("attention", attn_transposed_v),
+            ("combine", combine_lse_is_max)]
+
+
+_PINS = [
+    test_block_scores_exact_against_integer_brute_force,
+    lambda: [test_selection_hand_computed(c) for c in _golden("selection_cases.json")["cases"]],
+    test_selection_invariants_random,
+    test_selection_against_exhaustive_subset_search,
+    test_attention_special_cases,
+    test_combine_equals_unsplit,
+    test_dense_when_topk_covers_every_block,
+    test_sparse_equals_dense_over_selected_tokens,
+]
+
+
+@pytest.mark.parametrize("mutant", _mutants(), ids=lambda m: f"{m[0]}:{m[1].__name__}")
+def test_pins_catch_planted_mistake(mutant, monkeypatch):
+    name, fn = mutant
+    monkeypatch.setattr(oracle, name, fn)
+    monkeypatch.setattr(oracle.msa_oracle, name, fn)
+    caught = 0
+    for pin in _PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            caught += 1
+    assert caught > 0, f"no pin caught the mutant {fn.__name__}"
