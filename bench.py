@@ -1,0 +1,416 @@
+"""Benchmark: block-sparse paged MSA decode on GB300.
+
+One step = the whole decode path for one batch (plan -> index score -> top-k
+select -> sparse decode -> combine) on the medium decode workload: batch 32,
+seq_lens uniform in [8192, 32768], 64 query / 8 KV heads, head dim 128, block
+128, init 1 + local 3 + top-16 blocks, index dim 128, 16384-page pool.  Inputs
+are resident in HBM (1.7 GB touched per step, well above the 129 MB L2, so no
+flush is needed).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload medium_decode|long_decode|fp8_decode|verify|tiny_decode]
+
+N > 1 runs N independent replicas (one per GPU, launched by torchrun); the
+path needs no exchange between GPUs.  ``--impl reference`` times the fp64 CPU
+oracle on the host cores instead (a bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# The oracle legs run single-threaded BLAS; set before numpy loads.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_sparse_paged_msa_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "sparse-decode query-tokens/s"
+UNIT = "q-tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the index-score
+# kernel, from the ncu capture summarised in profiles/ (None until captured for
+# the current kernel).
+NCU_TRAFFIC_BYTES = {}
+
+
+# ----------------------------------------------------------------- helpers
+def algorithmic_bytes(w: wl.Workload):
+    """Bytes a step must move at minimum, by kernel.
+
+    index score: every visible index key once per request and KV head
+                 (L_r * H_kv * d * 2 bytes), the index queries, and one fp32
+                 score per (token, head, visible block);
+    decode:      the visible tokens of every selected block, K and V
+                 (n_valid * D * elem * 2 per (token, KV head, block)), q, and
+                 the split partials (written, then read by combine);
+    combine:     partials read + out (bf16) + lse (fp32) written."""
+    s = w.spec
+    P, Hkv, d, D = s.block_size, s.num_kv_heads, s.index_dim, s.head_dim
+    L = w.seq_lens.long().cpu()
+    nb = (L + P - 1) // P
+    T = w.num_tokens
+    idx = int(L.sum()) * Hkv * d * 2 + T * Hkv * d * 2 + int(nb.sum()) * s.q_len * Hkv * 4
+    return {"index_score": idx, "nb": nb, "L": L}
+
+
+def decode_bytes(w: wl.Workload, selected: torch.Tensor, nsplit: int) -> dict:
+    s = w.spec
+    P, D = s.block_size, s.head_dim
+    elem = 1 if s.kv_dtype == "fp8_e4m3" else 2
+    T = w.num_tokens
+    sel = selected[:T].long()                                   # [T, Hkv, S]
+    q_lens = w.q_lens.long()
+    pos = (w.seq_lens.long().repeat_interleave(q_lens)
+           - q_lens.repeat_interleave(q_lens)
+           + torch.cat([torch.arange(int(n), device=q_lens.device) for n in q_lens.tolist()]))
+    vis = (pos[:, None, None] + 1 - sel * P).clamp(0, P)
+    vis = torch.where(sel >= 0, vis, torch.zeros_like(vis))
+    kv = int(vis.sum()) * D * elem * 2
+    partial = T * s.num_q_heads * nsplit * (D + 1) * 4
+    q = T * s.num_q_heads * D * 2
+    out = T * s.num_q_heads * (D * 2 + 4)
+    return {"decode": kv + q + partial, "combine": partial + out, "kv": kv}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------- oracle leg
+def _oracle_problems(w: wl.Workload, seed: int = 0):
+    """An endless seeded stream of (token, KV head) pairs of the workload, each
+    as a one-request, one-head host problem (that request's pages only, float32
+    copies of the bf16 values, raw codes for e4m3)."""
+    s = w.spec
+    rng = np.random.default_rng(seed)
+    G = s.group
+    cu = w.cu_seqlens_q.cpu()
+    while True:
+        t = int(rng.integers(0, w.num_tokens))
+        h = int(rng.integers(0, s.num_kv_heads))
+        r = int(torch.searchsorted(cu, torch.tensor([t], dtype=torch.int32), right=True)[0]) - 1
+        L = int(w.seq_lens[r])
+        nb = -(-L // s.block_size)
+        pages = w.block_table[r, :nb].long()
+        q0, nq = int(cu[r]), int(w.q_lens[r])
+
+        def host(x):
+            x = x[pages][:, h:h + 1].cpu()
+            return x.view(torch.uint8).numpy() if x.dtype == torch.float8_e4m3fn \
+                else x.float().numpy()
+        yield dict(
+            seq_lens=[L], q_lens=[nq], block_table=np.arange(nb)[None],
+            idx_q=w.idx_q[q0:q0 + nq, h:h + 1].float().cpu().numpy(),
+            idx_k_pages=host(w.idx_k_pages),
+            q=w.q[q0:q0 + nq, h * G:(h + 1) * G].float().cpu().numpy(),
+            k_pages=host(w.k_pages), v_pages=host(w.v_pages), token=t - q0)
+
+
+def _run_oracle_problem(oracle, s: wl.WorkloadSpec, pr):
+    return oracle.sparse_attention(
+        seq_lens=pr["seq_lens"], q_lens=pr["q_lens"], block_table=pr["block_table"],
+        idx_q=pr["idx_q"], idx_k_pages=pr["idx_k_pages"], q=pr["q"], k_pages=pr["k_pages"],
+        v_pages=pr["v_pages"], num_kv_heads=1, block_size=s.block_size,
+        init_blocks=s.init_blocks,
+        local_blocks=oracle.local_blocks_from_tokens(s.local_tokens, s.block_size),
+        topk_blocks=s.topk_blocks, softmax_scale=s.softmax_scale, k_scale=s.kv_scale,
+        v_scale=s.kv_scale, kv_is_e4m3=s.kv_dtype == "fp8_e4m3", tokens=[pr["token"]])
+
+
+def cpu_baseline(w: wl.Workload, budget_s: float = 15.0):
+    """The oracle as it stands, on the host, over a bounded sample of
+    (token, KV head) pairs drawn until about budget_s seconds of oracle time;
+    q-tokens/s = pairs / H_kv / oracle seconds (problem set-up not timed)."""
+    import oracle
+    s = w.spec
+    spent, done = 0.0, 0
+    for pr in _oracle_problems(w):
+        t0 = time.perf_counter()
+        _run_oracle_problem(oracle, s, pr)
+        spent += time.perf_counter() - t0
+        done += 1
+        if spent > budget_s:
+            break
+    return {"value": done / s.num_kv_heads / spent, "unit": UNIT,
+            "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{done} random (token, KV head) pairs of {s.name} (one request's "
+                      f"pages each), fp64 numpy, {spent:.1f} s of oracle time"}
+
+
+def _blas_threads():
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            return int(os.environ[k])
+    return 1
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import block_sparse_paged_msa_gb300 as msa
+    from block_sparse_paged_msa_gb300 import build as msa_build
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if rank == 0 or not os.path.exists(msa.ops.lib_path()):
+        msa_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    spec = wl.WORKLOADS[args.workload].replace(seed=wl.WORKLOADS[args.workload].seed + rank)
+    w = wl.make_workload(spec, device=dev)
+    cfg = msa.config_for(spec)
+    sa = msa.SparseAttention(cfg, device=dev)
+    stream = torch.cuda.current_stream()
+    args_run = (w.seq_lens, w.block_table, w.idx_q, w.idx_k_pages, w.q, w.k_pages, w.v_pages)
+    names = ["plan", "index_score", "topk_select", "sparse_decode", "combine"]
+
+    def step(evs=None):
+        c = sa.cfg
+        calls = [
+            lambda: msa.plan(c, w.seq_lens, w.block_table, sa.ws),
+            lambda: msa.index_score(c, sa.ws, w.idx_q, w.idx_k_pages, sa.block_scores),
+            lambda: msa.topk_select(c, sa.ws, sa.block_scores, sa.selected),
+            lambda: msa.sparse_decode(c, sa.ws, w.q, w.k_pages, w.v_pages, sa.selected),
+            lambda: msa.combine(c, sa.ws, sa.out, sa.lse),
+        ]
+        for i, fn in enumerate(calls):
+            if evs is not None:
+                evs[i][0].record(stream)
+            fn()
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert msa.check_device_error(sa.ws) == 0
+
+    K = args.steps
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in names] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for k in range(K):
+            step(evs[k])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+    ms = start.elapsed_time(stop)
+    per_kernel = {n: sum(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(K)) / K
+                  for i, n in enumerate(names)}
+
+    # ---- e2e: host buffers in, result out, through the public API
+    pin = {k: getattr(w, k).cpu().pin_memory() for k in ("seq_lens", "block_table", "idx_q", "q")}
+    dbuf = {k: torch.empty_like(getattr(w, k)) for k in pin}
+    out_h = torch.empty(sa.out.shape, dtype=sa.out.dtype).pin_memory()
+    lse_h = torch.empty(sa.lse.shape, dtype=sa.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def e2e_step():
+        for k, t in pin.items():
+            dbuf[k].copy_(t, non_blocking=True)
+        sa.run(dbuf["seq_lens"], dbuf["block_table"], dbuf["idx_q"], w.idx_k_pages, dbuf["q"],
+               w.k_pages, w.v_pages)
+        out_h.copy_(sa.out, non_blocking=True)
+        lse_h.copy_(sa.lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 4)):
+        e2e_step()
+    torch.cuda.synchronize()
+    Ke = max(10, K // 2)
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    # ---- accounting
+    ab = algorithmic_bytes(w)
+    db = decode_bytes(w, sa.selected, msa.num_splits(cfg))
+    T = w.num_tokens
+    t_max = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
+    ms, e2e_ms = float(t_max[0]), float(t_max[1])
+    value = T * world * K / (ms / 1e3)
+    e2e_value = T * world * Ke / (e2e_ms / 1e3)
+    peak, peak_kind = measured_peak_hbm()
+    idx_gbs = ab["index_score"] / (per_kernel["index_score"] / 1e3) / 1e9
+    step_bytes = ab["index_score"] + db["decode"] + db["combine"]
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if spec.kv_dtype == "bf16" else "fp8_e4m3",
+        "data": "synthetic (seeded; integer-valued bf16 index vectors, N(0,1) bf16 q/k/v)",
+        "config": {"workload": spec.name, "batch": spec.batch,
+                   "seq_lens": list(spec.seq_len_range or spec.seq_lens[:1]),
+                   "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads,
+                   "head_dim": spec.head_dim, "index_dim": spec.index_dim,
+                   "block": spec.block_size, "init_local_topk": [spec.init_blocks,
+                   msa.ops.local_blocks_from_tokens(spec.local_tokens), spec.topk_blocks],
+                   "pool_pages": spec.num_pages, "parallelism": f"replicas{world}",
+                   "l2": f"no flush: {step_bytes / 1e9:.2f} GB touched per step > 129 MB L2"},
+        "roofline": {"bound": "hbm", "kernel": "index_score", "achieved": idx_gbs,
+                     "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": NCU_TRAFFIC_BYTES.get((spec.name, "index_score"))},
+        "step_hbm": {"algorithmic_bytes": step_bytes,
+                     "achieved_gbs": step_bytes / (ms / K / 1e3) / 1e9,
+                     "frac": step_bytes / (ms / K / 1e3) / 1e9 / peak},
+        "kernels_ms": per_kernel,
+        "kernel_gbs": {"index_score": idx_gbs,
+                       "sparse_decode": db["decode"] / (per_kernel["sparse_decode"] / 1e3) / 1e9,
+                       "combine": db["combine"] / (per_kernel["combine"] / 1e3) / 1e9},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 5 * K,
+        "clocks": clk.summary(),
+    }
+    return result, w
+
+
+def run_reference(args):
+    """The fp64 oracle on the host cores: each step one (token, KV head) pair."""
+    import oracle
+    spec = wl.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = wl.make_workload(spec, device=dev)
+    gen = _oracle_problems(w, seed=1)
+    probs = [next(gen) for _ in range(16)]
+    for i in range(args.warmup):
+        _run_oracle_problem(oracle, spec, probs[i % len(probs)])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        _run_oracle_problem(oracle, spec, probs[i % len(probs)])
+    dt = time.perf_counter() - t0
+    value = args.steps / spec.num_kv_heads / dt
+    cores = _blas_threads()
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": spec.name},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step one (token, KV head) pair of {spec.name} "
+                                   f"(one request's pages), fp64 numpy"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="medium_decode", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    result, w = run_ours(args, rank, world, local_rank)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,213 @@
+// msa_index_score: per (query token, KV head, visible block) the maximum over
+// the block's visible tokens of idx_q . idx_k.
+//
+// sglang minimax_sparse_backend.py (MiniMaxSparseAttnBackend.__init__) reads
+// the index head dim (sparse_index_dim) and a score_type, and forward_decode
+// hands idx_q and the index-K cache to the sparse decode op; the score formula
+// itself is fixed by this library's specification: max over tokens, fp32
+// accumulation, no scale.
+//
+// Design (GB300): a pure HBM scan -- every visible index key is read once per
+// request (one 256-byte row per token and KV head at d = 128) against 128 FMAs,
+// about 0.5 FMA per byte, so CUDA cores are ample and the kernel is sized for
+// bytes in flight.  One warp owns one (block, KV head) tile of 128 rows, which
+// is contiguous in the HND page layout (32 KiB at d = 128).  Lanes own a fixed
+// 16-byte slice of the index dimension, so the index query stays in registers;
+// each lane keeps 8 16-byte streaming loads in flight, and the partial dot
+// products of 8 rows are reduced across the row's lanes with a
+// transpose-reduce butterfly (one shuffle per row instead of log2(lanes)).
+// The grid is persistent (SMs x resident CTAs) and walks the flattened
+// (request, block, head) list, so ragged sequence lengths balance by blocks,
+// not by requests.
+#include <mutex>
+
+#include "msa_internal.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 8;   // 16-byte loads in flight per lane
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float dot8(const float (&q)[8], const uint4& w) {
+  float s = q[0] * bf16lo(w.x);
+  s = fmaf(q[1], bf16hi(w.x), s);
+  s = fmaf(q[2], bf16lo(w.y), s);
+  s = fmaf(q[3], bf16hi(w.y), s);
+  s = fmaf(q[4], bf16lo(w.z), s);
+  s = fmaf(q[5], bf16hi(w.z), s);
+  s = fmaf(q[6], bf16lo(w.w), s);
+  s = fmaf(q[7], bf16hi(w.w), s);
+  return s;
+}
+
+// DIDX: index dim (64 | 128).  QL: query tokens per request scored together
+// (1 = decode, up to 4 = speculative verify); they share every key load.
+template <int DIDX, int QL>
+__global__ void __launch_bounds__(kThreads)
+index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
+                   const uint4* __restrict__ idx_q,
+                   const uint4* __restrict__ idx_k, float* __restrict__ scores) {
+  constexpr int LPR = DIDX / 8;            // lanes per key row
+  constexpr int RPI = 32 / LPR;            // rows per warp-wide load
+  constexpr int ROWS = kUnroll * RPI;      // rows per batch
+  static_assert(kBlock % ROWS == 0, "block must be a multiple of the batch");
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % LPR, rsub = lane / LPR;
+  // Row (within a batch) whose full dot product this lane holds after the
+  // transpose-reduce: the upper-half lanes keep the upper half at every step.
+  int u_lane = 0;
+  {
+    int n = kUnroll;
+#pragma unroll
+    for (int mask = LPR / 2; mask >= 1; mask >>= 1) {
+      if (n > 1) {
+        n >>= 1;
+        if (sub & mask) u_lane += n;
+      }
+    }
+  }
+  const int batch = ws.hdr->batch;
+  const int total = ws.hdr->total_blocks * Hkv;
+  const int warps = gridDim.x * (kThreads / 32);
+  for (int item = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); item < total;
+       item += warps) {
+    const int h = item % Hkv;
+    const int b = item / Hkv;
+    int lo = 0, hi = batch - 1;  // request of flat block b
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ws.req_cu_nb[mid] <= b) lo = mid; else hi = mid - 1;
+    }
+    const int r = lo;
+    const int j = b - ws.req_cu_nb[r];
+    const int page = ws.block_table[(int64_t)r * max_blocks + j];
+    const int qs = ws.req_qstart[r];
+    float* out = scores + ((int64_t)qs * Hkv + h) * max_blocks + j;
+    if (page < 0) {  // flagged by the plan; never dereferenced
+      if (lane == 0)
+        for (int i = 0; i < QL; ++i)
+          if (qs + i < max_tokens && ws.tok_req[qs + i] == r)
+            out[(int64_t)i * Hkv * max_blocks] = -INFINITY;
+      continue;
+    }
+    float q[QL][8];
+    int lim[QL];
+#pragma unroll
+    for (int i = 0; i < QL; ++i) {
+      // a request owns QL consecutive tokens; anything else is left unscored
+      const bool mine = qs + i < max_tokens && ws.tok_req[qs + i] == r;
+      const uint4 w = mine ? idx_q[(((int64_t)(qs + i) * Hkv + h) * DIDX) / 8 + sub]
+                           : make_uint4(0u, 0u, 0u, 0u);
+      q[i][0] = bf16lo(w.x); q[i][1] = bf16hi(w.x);
+      q[i][2] = bf16lo(w.y); q[i][3] = bf16hi(w.y);
+      q[i][4] = bf16lo(w.z); q[i][5] = bf16hi(w.z);
+      q[i][6] = bf16lo(w.w); q[i][7] = bf16hi(w.w);
+      lim[i] = mine ? ws.tok_pos[qs + i] - j * kBlock + 1 : 0;  // visible rows
+    }
+    const uint4* tile = idx_k + (((int64_t)page * Hkv + h) * kBlock * DIDX) / 8;
+    float best[QL];
+#pragma unroll
+    for (int i = 0; i < QL; ++i) best[i] = -INFINITY;
+#pragma unroll 1
+    for (int rb = 0; rb < kBlock; rb += ROWS) {
+      uint4 d[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) d[u] = ld_stream(tile + (rb + u * RPI + rsub) * LPR + sub);
+#pragma unroll
+      for (int i = 0; i < QL; ++i) {
+        float v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = dot8(q[i], d[u]);
+        int n = kUnroll;
+#pragma unroll
+        for (int mask = LPR / 2; mask >= 1; mask >>= 1) {
+          if (n > 1) {
+            const int half = n >> 1;
+            const bool upper = (sub & mask) != 0;
+#pragma unroll
+            for (int k = 0; k < half; ++k) {
+              const float send = upper ? v[k] : v[k + half];
+              const float keep = upper ? v[k + half] : v[k];
+              v[k] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+            }
+            n = half;
+          } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+          }
+        }
+        const int row = rb + u_lane * RPI + rsub;
+        if (row < lim[i]) best[i] = fmaxf(best[i], v[0]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < QL; ++i) {
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1)
+        best[i] = fmaxf(best[i], __shfl_xor_sync(0xffffffffu, best[i], o));
+      if (lane == 0 && lim[i] > 0) out[(int64_t)i * Hkv * max_blocks] = best[i];
+    }
+  }
+}
+
+template <int DIDX, int QL>
+msa_status launch(const msa_config& c, const WsView& v, const void* idx_q, const void* idx_k,
+                  float* scores, cudaStream_t s) {
+  static std::mutex mu;
+  static int occ[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MSA_ERR_CUDA;
+  int blocks_per_sm;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 64 && occ[dev] == 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, index_score_kernel<DIDX, QL>,
+                                                        kThreads, 0) != cudaSuccess)
+        return MSA_ERR_CUDA;
+      occ[dev] = n > 0 ? n : 1;
+    }
+    blocks_per_sm = dev < 64 ? occ[dev] : 1;
+  }
+  const int grid = sm_count() * blocks_per_sm;
+  if (grid <= 0) return MSA_ERR_CUDA;
+  index_score_kernel<DIDX, QL><<<grid, kThreads, 0, s>>>(
+      v, c.num_kv_heads, c.max_blocks_per_req, max_tokens_of(c), (const uint4*)idx_q, (const uint4*)idx_k, scores);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" msa_status msa_index_score(const msa_config* cfg, const void* ws, const void* idx_q,
+                                      const void* idx_k_pages, float* block_scores,
+                                      msa_stream_t stream) {
+  msa_status st = check_config(cfg);
+  if (st != MSA_OK) return st;
+  if (!ws || !idx_q || !idx_k_pages || !block_scores) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(idx_q) || !aligned16(idx_k_pages)) return MSA_ERR_INVALID_ARG;
+  const WsView v = view_of(*cfg, ws);
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool d128 = cfg->index_dim == 128;
+  switch (cfg->q_len) {
+    case 1: return d128 ? launch<128, 1>(*cfg, v, idx_q, idx_k_pages, block_scores, s)
+                        : launch<64, 1>(*cfg, v, idx_q, idx_k_pages, block_scores, s);
+    case 2: return d128 ? launch<128, 2>(*cfg, v, idx_q, idx_k_pages, block_scores, s)
+                        : launch<64, 2>(*cfg, v, idx_q, idx_k_pages, block_scores, s);
+    case 3: return d128 ? launch<128, 3>(*cfg, v, idx_q, idx_k_pages, block_scores, s)
+                        : launch<64, 3>(*cfg, v, idx_q, idx_k_pages, block_scores, s);
+    case 4: return d128 ? launch<128, 4>(*cfg, v, idx_q, idx_k_pages, block_scores, s)
+                        : launch<64, 4>(*cfg, v, idx_q, idx_k_pages, block_scores, s);
+    default: return MSA_ERR_UNSUPPORTED;
+  }
+}

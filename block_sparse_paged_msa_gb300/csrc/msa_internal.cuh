@@ -1,0 +1,115 @@
+// Internal definitions shared by the libmsa translation units: workspace layout,
+// argument checks and small device helpers.  Not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/msa.h"
+
+namespace msa {
+
+constexpr int kBlock = 128;      // P: sparse block = KV page
+constexpr int kHeadDim = 128;    // D
+constexpr int kMaxGroup = 16;    // query heads per KV head (one m16 MMA tile)
+constexpr int kMaxBlocksPerReq = 8192;
+constexpr int kMaxBatch = 65536;
+
+// Workspace header (first 256 bytes).
+struct WsHeader {
+  int32_t err;            // MSA_DEVERR_* bits, reset by msa_plan
+  int32_t batch;
+  int32_t num_tokens;     // T of the current plan
+  int32_t total_blocks;   // sum over requests of ceil(seq_len / P)
+};
+
+inline size_t align_up(size_t x, size_t a = 256) { return (x + a - 1) / a * a; }
+
+inline int32_t width_of(const msa_config& c) {
+  return c.init_blocks + c.local_blocks + c.topk_blocks;
+}
+
+inline int32_t max_tokens_of(const msa_config& c) {
+  return c.max_q_tokens > 0 ? c.max_q_tokens : c.max_batch * c.q_len;
+}
+
+int32_t blocks_per_split_of(const msa_config& c);  // resolves the 0 = auto case
+
+inline int32_t splits_of(const msa_config& c) {
+  int32_t S = width_of(c), b = blocks_per_split_of(c);
+  return S <= 0 ? 1 : (S + b - 1) / b;
+}
+
+// Byte offsets of every workspace region.
+struct WsLayout {
+  size_t req_seq_len, req_nb, req_cu_nb, req_qstart, tok_req, tok_pos, block_table;
+  size_t o_part, lse_part, total;
+};
+
+inline WsLayout layout_of(const msa_config& c) {
+  WsLayout L;
+  const size_t B = (size_t)c.max_batch, T = (size_t)max_tokens_of(c);
+  const size_t NS = (size_t)splits_of(c), Hq = (size_t)c.num_q_heads;
+  size_t o = 256;
+  L.req_seq_len = o; o = align_up(o + 4 * B);
+  L.req_nb = o;      o = align_up(o + 4 * B);
+  L.req_cu_nb = o;   o = align_up(o + 4 * (B + 1));
+  L.req_qstart = o;  o = align_up(o + 4 * (B + 1));
+  L.tok_req = o;     o = align_up(o + 4 * T);
+  L.tok_pos = o;     o = align_up(o + 4 * T);
+  L.block_table = o; o = align_up(o + 4 * B * (size_t)c.max_blocks_per_req);
+  L.o_part = o;      o = align_up(o + 4 * T * Hq * NS * kHeadDim);
+  L.lse_part = o;    o = align_up(o + 4 * T * Hq * NS);
+  L.total = o;
+  return L;
+}
+
+// Typed views of a workspace, passed to kernels by value.
+struct WsView {
+  WsHeader* hdr;
+  int32_t* req_seq_len;
+  int32_t* req_nb;
+  int32_t* req_cu_nb;
+  int32_t* req_qstart;
+  int32_t* tok_req;
+  int32_t* tok_pos;
+  int32_t* block_table;   // [max_batch, max_blocks_per_req], -1 = invalid
+  float* o_part;          // [T, H_q, NS, D]
+  float* lse_part;        // [T, H_q, NS]
+};
+
+inline WsView view_of(const msa_config& c, const void* ws) {
+  WsLayout L = layout_of(c);
+  char* b = (char*)ws;
+  WsView v;
+  v.hdr = (WsHeader*)b;
+  v.req_seq_len = (int32_t*)(b + L.req_seq_len);
+  v.req_nb = (int32_t*)(b + L.req_nb);
+  v.req_cu_nb = (int32_t*)(b + L.req_cu_nb);
+  v.req_qstart = (int32_t*)(b + L.req_qstart);
+  v.tok_req = (int32_t*)(b + L.tok_req);
+  v.tok_pos = (int32_t*)(b + L.tok_pos);
+  v.block_table = (int32_t*)(b + L.block_table);
+  v.o_part = (float*)(b + L.o_part);
+  v.lse_part = (float*)(b + L.lse_part);
+  return v;
+}
+
+msa_status check_config(const msa_config* c);
+int sm_count();  // SMs of the current device (cached per device)
+
+// Launch-status helper: any launch error becomes MSA_ERR_CUDA.
+inline msa_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+// ---------------------------------------------------------------- device
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void set_error(WsHeader* h, int bits) { atomicOr(&h->err, bits); }
+
+}  // namespace msa

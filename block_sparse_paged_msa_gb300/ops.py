@@ -1,0 +1,278 @@
+"""Thin Python binding of libmsa's C ABI (argument marshalling only).
+
+Every step of the path runs in the CUDA kernels of libmsa.so; this module
+checks dtypes / shapes / devices, passes ``data_ptr()`` and the current CUDA
+stream, and turns a non-OK status into an exception.  There is no fallback:
+if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsa.so")
+_lib = None
+
+MSA_KV_BF16, MSA_KV_FP8_E4M3 = 0, 1
+STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED",
+          3: "MSA_ERR_CUDA", 4: "MSA_ERR_DEVICE_FLAG"}
+DEVERR_BITS = {1: "PAGE_RANGE", 2: "SEQ_LEN", 4: "SLOT_ALIGN"}
+
+
+class MsaError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS.get(status, status)} {detail}".strip())
+
+
+class MsaConfig(ctypes.Structure):
+    """Mirror of ``msa_config`` in include/msa.h (field order matters)."""
+    _fields_ = [
+        ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+        ("init_blocks", ctypes.c_int32), ("local_blocks", ctypes.c_int32),
+        ("topk_blocks", ctypes.c_int32), ("index_dim", ctypes.c_int32),
+        ("q_len", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+        ("softmax_scale", ctypes.c_float), ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float), ("max_batch", ctypes.c_int32),
+        ("max_q_tokens", ctypes.c_int32), ("max_blocks_per_req", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32), ("blocks_per_split", ctypes.c_int32),
+    ]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+_P = ctypes.c_void_p
+_CFG = ctypes.POINTER(MsaConfig)
+_SIGNATURES = {
+    "msa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "msa_validate_config": (ctypes.c_int, [_CFG]),
+    "msa_selected_width": (ctypes.c_int32, [_CFG]),
+    "msa_num_splits": (ctypes.c_int32, [_CFG]),
+    "msa_workspace_bytes": (ctypes.c_size_t, [_CFG]),
+    "msa_plan": (ctypes.c_int, [_CFG, ctypes.c_int32, _P, _P, _P, ctypes.c_int32, _P, _P]),
+    "msa_plan_from_req_to_token": (ctypes.c_int, [_CFG, ctypes.c_int32, _P, _P, _P,
+                                                  ctypes.c_int32, _P, _P, _P]),
+    "msa_index_score": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
+    "msa_topk_select": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
+    "msa_sparse_decode": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
+    "msa_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
+    "msa_check_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+}
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """Load libmsa.so once; raise if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with block_sparse_paged_msa_gb300.build.build()")
+        L = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int, detail: str = ""):
+    if status != 0:
+        raise MsaError(fn, status, detail)
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, dim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dims, has {t.dim()}")
+
+
+# ---------------------------------------------------------------- config
+def local_blocks_from_tokens(local_tokens: int, block_size: int = 128) -> int:
+    """sglang MiniMaxSparseAttnBackend.__init__: sparse_local_tokens -> blocks,
+    ceil(tokens / block) + 1 (the query's own partial block on top)."""
+    return (local_tokens + block_size - 1) // block_size + 1
+
+
+def init_blocks_from_tokens(init_tokens: int, block_size: int = 128) -> int:
+    return (init_tokens + block_size - 1) // block_size
+
+
+def make_config(*, num_q_heads, num_kv_heads, init_blocks, local_blocks, topk_blocks,
+                index_dim, max_batch, max_blocks_per_req, num_pages, q_len=1,
+                kv_dtype="bf16", softmax_scale=None, k_scale=1.0, v_scale=1.0,
+                max_q_tokens=0, blocks_per_split=0, head_dim=128,
+                block_size=128) -> MsaConfig:
+    c = MsaConfig()
+    c.num_q_heads, c.num_kv_heads = num_q_heads, num_kv_heads
+    c.head_dim, c.block_size = head_dim, block_size
+    c.init_blocks, c.local_blocks, c.topk_blocks = init_blocks, local_blocks, topk_blocks
+    c.index_dim, c.q_len = index_dim, q_len
+    c.kv_dtype = {"bf16": MSA_KV_BF16, "fp8_e4m3": MSA_KV_FP8_E4M3}[kv_dtype]
+    c.softmax_scale = 1.0 / math.sqrt(head_dim) if softmax_scale is None else softmax_scale
+    c.k_scale, c.v_scale = k_scale, v_scale
+    c.max_batch, c.max_q_tokens = max_batch, max_q_tokens
+    c.max_blocks_per_req, c.num_pages = max_blocks_per_req, num_pages
+    c.blocks_per_split = blocks_per_split
+    return c
+
+
+def config_for(spec, **overrides) -> MsaConfig:
+    """Config of a WorkloadSpec (block counts resolved here, by the library)."""
+    kw = dict(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+              init_blocks=spec.init_blocks,
+              local_blocks=local_blocks_from_tokens(spec.local_tokens, spec.block_size),
+              topk_blocks=spec.topk_blocks, index_dim=spec.index_dim,
+              max_batch=spec.batch, max_blocks_per_req=spec.max_blocks,
+              num_pages=spec.num_pages, q_len=spec.q_len, kv_dtype=spec.kv_dtype,
+              softmax_scale=spec.softmax_scale, k_scale=spec.kv_scale,
+              v_scale=spec.kv_scale, head_dim=spec.head_dim, block_size=spec.block_size)
+    kw.update(overrides)
+    return make_config(**kw)
+
+
+def validate_config(cfg: MsaConfig) -> int:
+    return lib().msa_validate_config(ctypes.byref(cfg))
+
+
+def workspace_bytes(cfg: MsaConfig) -> int:
+    n = lib().msa_workspace_bytes(ctypes.byref(cfg))
+    if n == 0:
+        _check("msa_workspace_bytes", validate_config(cfg) or 1)
+    return n
+
+
+def selected_width(cfg: MsaConfig) -> int:
+    return lib().msa_selected_width(ctypes.byref(cfg))
+
+
+def num_splits(cfg: MsaConfig) -> int:
+    return lib().msa_num_splits(ctypes.byref(cfg))
+
+
+def status_string(status: int) -> str:
+    return lib().msa_status_string(status).decode()
+
+
+# ---------------------------------------------------------------- calls
+def plan(cfg, seq_lens, block_table, ws, cu_seqlens_q=None, stream=None):
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(ws, "ws", torch.uint8)
+    if cu_seqlens_q is not None:
+        _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    B = seq_lens.shape[0]
+    _check("msa_plan", lib().msa_plan(ctypes.byref(cfg), B, _ptr(seq_lens), _ptr(cu_seqlens_q),
+                                      _ptr(block_table), block_table.shape[1], _ptr(ws),
+                                      _stream(stream)))
+
+
+def plan_from_req_to_token(cfg, seq_lens, req_to_token, req_pool_indices, ws,
+                           cu_seqlens_q=None, stream=None):
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(req_to_token, "req_to_token", torch.int32, 2)
+    _need(req_pool_indices, "req_pool_indices", torch.int64, 1)
+    _need(ws, "ws", torch.uint8)
+    if cu_seqlens_q is not None:
+        _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _check("msa_plan_from_req_to_token", lib().msa_plan_from_req_to_token(
+        ctypes.byref(cfg), seq_lens.shape[0], _ptr(seq_lens), _ptr(cu_seqlens_q),
+        _ptr(req_to_token), req_to_token.shape[1], _ptr(req_pool_indices), _ptr(ws),
+        _stream(stream)))
+
+
+def index_score(cfg, ws, idx_q, idx_k_pages, block_scores, stream=None):
+    _need(idx_q, "idx_q", torch.bfloat16, 3)
+    _need(idx_k_pages, "idx_k_pages", torch.bfloat16, 4)
+    _need(block_scores, "block_scores", torch.float32, 3)
+    _check("msa_index_score", lib().msa_index_score(
+        ctypes.byref(cfg), _ptr(ws), _ptr(idx_q), _ptr(idx_k_pages), _ptr(block_scores),
+        _stream(stream)))
+
+
+def topk_select(cfg, ws, block_scores, selected, stream=None):
+    _need(block_scores, "block_scores", torch.float32, 3)
+    _need(selected, "selected", torch.int32, 3)
+    _check("msa_topk_select", lib().msa_topk_select(
+        ctypes.byref(cfg), _ptr(ws), _ptr(block_scores), _ptr(selected), _stream(stream)))
+
+
+def sparse_decode(cfg, ws, q, k_pages, v_pages, selected, stream=None):
+    _need(q, "q", torch.bfloat16, 3)
+    kv = (torch.bfloat16,) if cfg.kv_dtype == MSA_KV_BF16 else (torch.float8_e4m3fn, torch.uint8)
+    _need(k_pages, "k_pages", kv, 4)
+    _need(v_pages, "v_pages", kv, 4)
+    _need(selected, "selected", torch.int32, 3)
+    _check("msa_sparse_decode", lib().msa_sparse_decode(
+        ctypes.byref(cfg), _ptr(ws), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(selected),
+        _stream(stream)))
+
+
+def combine(cfg, ws, out, lse, stream=None):
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    _check("msa_combine", lib().msa_combine(ctypes.byref(cfg), _ptr(ws), _ptr(out), _ptr(lse),
+                                            _stream(stream)))
+
+
+def check_device_error(ws, stream=None) -> int:
+    """Synchronises the stream; returns the device error bits (0 = none)."""
+    flags = ctypes.c_int32(0)
+    st = lib().msa_check_device_error(_ptr(ws), ctypes.byref(flags), _stream(stream))
+    if st not in (0, 4):
+        _check("msa_check_device_error", st)
+    return flags.value
+
+
+# ---------------------------------------------------------------- the step
+class SparseAttention:
+    """Owns the buffers of one configuration and runs the whole path:
+    plan -> index score -> top-k select -> sparse decode -> combine."""
+
+    def __init__(self, cfg: MsaConfig, device="cuda"):
+        self.cfg = cfg
+        _check("msa_validate_config", validate_config(cfg))
+        T = cfg.max_q_tokens or cfg.max_batch * cfg.q_len
+        self.max_tokens = T
+        self.width = selected_width(cfg)
+        self.ws = torch.empty(workspace_bytes(cfg), dtype=torch.uint8, device=device)
+        self.block_scores = torch.empty((T, cfg.num_kv_heads, cfg.max_blocks_per_req),
+                                        dtype=torch.float32, device=device)
+        self.selected = torch.empty((T, cfg.num_kv_heads, self.width), dtype=torch.int32,
+                                    device=device)
+        self.out = torch.empty((T, cfg.num_q_heads, cfg.head_dim), dtype=torch.bfloat16,
+                               device=device)
+        self.lse = torch.empty((T, cfg.num_q_heads), dtype=torch.float32, device=device)
+
+    def run(self, seq_lens, block_table, idx_q, idx_k_pages, q, k_pages, v_pages,
+            cu_seqlens_q=None, stream=None):
+        c = self.cfg
+        plan(c, seq_lens, block_table, self.ws, cu_seqlens_q, stream)
+        index_score(c, self.ws, idx_q, idx_k_pages, self.block_scores, stream)
+        topk_select(c, self.ws, self.block_scores, self.selected, stream)
+        sparse_decode(c, self.ws, q, k_pages, v_pages, self.selected, stream)
+        combine(c, self.ws, self.out, self.lse, stream)
+        return self.out, self.lse

@@ -202,7 +202,8 @@ def make_workload(spec: WorkloadSpec, device="cpu", kv_pool=True) -> Workload:
     gen.manual_seed(spec.seed)
     B, P = spec.batch, spec.block_size
     seq_lens = _draw_seq_lens(spec, gen, device)
-    assert int(seq_lens.min()) >= spec.q_len if B else True
+    # seq_len 0 marks an idle request; any other request holds its query tokens
+    assert all(L == 0 or L >= spec.q_len for L in seq_lens.tolist())
     nb = [-(-int(s) // P) for s in seq_lens.tolist()]
     need = sum(nb)
     if need > spec.num_pages:

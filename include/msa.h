@@ -1,0 +1,227 @@
+/*
+ * msa.h -- C ABI of libmsa: block-sparse attention over a paged KV cache
+ * (MiniMax-M3 style "MSA"), hand-written CUDA for sm_103a (GB300).
+ *
+ * The method (sglang minimax_sparse_backend.py, MiniMaxSparseAttnBackend:
+ * __init__, forward_decode, forward_extend; vLLM
+ * minimax_m3/nvidia/sparse_attention_msa.py, MiniMaxM3SparseMSAImpl.forward):
+ * every query token rates each 128-token KV block of its request with a
+ * low-dimensional index query/key, keeps the init blocks, the local blocks and
+ * the topk_blocks best remaining blocks, and attends over those blocks only
+ * (GQA: the query heads of one KV head share its selection).  A decode step is
+ *
+ *     msa_plan -> msa_index_score -> msa_topk_select -> msa_sparse_decode -> msa_combine
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All pointers are DEVICE pointers unless a comment says "host".  The caller
+ *    owns every buffer; the library never allocates or frees device memory and
+ *    never synchronises, except msa_check_device_error.
+ *  - Work is enqueued on the caller's stream (NULL = legacy default stream).
+ *    Every launch has a grid fixed by the msa_config maxima, and no call reads
+ *    device data on the host, so the whole step can be captured in a CUDA graph
+ *    once and replayed with new data in the same buffers.
+ *  - Layouts (row-major, contiguous):
+ *      q            [T, H_q, D]            bf16
+ *      idx_q        [T, H_kv, d]           bf16
+ *      k_pages      [num_pages, H_kv, P, D] bf16, or fp8 e4m3 codes (kv_dtype)
+ *      v_pages      [num_pages, H_kv, P, D] same type as k_pages
+ *      idx_k_pages  [num_pages, H_kv, P, d] bf16
+ *      block_table  [batch, >= max_blocks_per_req] int32 (row stride given);
+ *                   entry j = physical page of the request's logical block j
+ *      block_scores [T, H_kv, max_blocks_per_req] float
+ *      selected     [T, H_kv, S] int32, S = init + local + topk blocks,
+ *                   ascending block indices, padded with -1
+ *      out          [T, H_q, D] bf16;  lse [T, H_q] float (natural log)
+ *    T is the number of query tokens of the step (batch * q_len for decode and
+ *    verify, cu_seqlens_q[batch] for prefill); P = block_size = page size = 128.
+ *  - seq_lens[r] counts request r's KV tokens INCLUDING its new query tokens
+ *    (the fused KV / index-K cache write precedes attention in forward_decode);
+ *    the i-th of the n new tokens of request r sits at position
+ *    seq_lens[r] - n + i and sees the tokens at positions <= its own.
+ *  - A request with seq_len 0 (or a batch of 0) produces out = 0, lse = -inf
+ *    (the idle-batch convention of forward_decode).
+ *  - Errors: argument problems found on the host return a status before any
+ *    launch.  Problems only visible on the device (a page id outside
+ *    [0, num_pages), a seq_len above max_blocks_per_req * P or below the
+ *    request's query count) never fault: the kernels skip the bad entry, set a
+ *    bit in the workspace's error word, and msa_check_device_error reports it.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* msa_stream_t;
+
+typedef enum msa_status {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad stride ...   */
+  MSA_ERR_UNSUPPORTED = 2,   /* valid, but outside what the kernels implement */
+  MSA_ERR_CUDA = 3,          /* a CUDA runtime call failed                    */
+  MSA_ERR_DEVICE_FLAG = 4    /* a kernel flagged bad data (see error bits)    */
+} msa_status;
+
+typedef enum msa_kv_dtype {
+  MSA_KV_BF16 = 0,
+  MSA_KV_FP8_E4M3 = 1        /* e4m3 "fn" codes; value = decode(code) * scale */
+} msa_kv_dtype;
+
+/* Bits of the device error word (msa_check_device_error). */
+enum {
+  MSA_DEVERR_PAGE_RANGE = 1,   /* block table / req_to_token page outside the pool */
+  MSA_DEVERR_SEQ_LEN = 2,      /* seq_len > max_blocks_per_req*P, or < query count,
+                                  or the step's tokens exceed max_q_tokens        */
+  MSA_DEVERR_SLOT_ALIGN = 4    /* req_to_token slot of a block not page-aligned   */
+};
+
+/*
+ * Static configuration of one sparse-attention layer and of the largest step
+ * the workspace must hold.  Block counts follow sglang
+ * MiniMaxSparseAttnBackend.__init__: init_blocks = ceil(sparse_init_tokens/P)
+ * (or sparse_init_block), local_blocks = ceil(sparse_local_tokens/P) + 1 (or
+ * sparse_local_block), topk_blocks = sparse_topk_blocks, index_dim =
+ * sparse_index_dim.  GQA: num_q_heads / num_kv_heads query heads per KV head
+ * (qhead_per_kv in MiniMaxM3SparseMSAImpl.forward).
+ */
+typedef struct msa_config {
+  int32_t num_q_heads;        /* H_q                                            */
+  int32_t num_kv_heads;       /* H_kv; H_q % H_kv == 0, H_q / H_kv <= 16         */
+  int32_t head_dim;           /* D; must be 128                                  */
+  int32_t block_size;         /* P = sparse block = KV page; must be 128         */
+  int32_t init_blocks;        /* >= 0                                            */
+  int32_t local_blocks;       /* >= 1 (includes the query's own block)           */
+  int32_t topk_blocks;        /* >= 0                                            */
+  int32_t index_dim;          /* d; 64 or 128                                    */
+  int32_t q_len;              /* new query tokens per request: 1 = decode,
+                                 2..4 = speculative verify                       */
+  int32_t kv_dtype;           /* msa_kv_dtype                                    */
+  float softmax_scale;        /* applied to q.k before the softmax               */
+  float k_scale;              /* fp8 only: dequantised k = e4m3(code) * k_scale  */
+  float v_scale;              /* fp8 only: dequantised v = e4m3(code) * v_scale  */
+  int32_t max_batch;          /* largest batch a plan may describe               */
+  int32_t max_q_tokens;       /* largest T; 0 = max_batch * q_len                */
+  int32_t max_blocks_per_req; /* block-table width used; seq_len <= this * P     */
+  int32_t num_pages;          /* pages in the KV / index-K pool                  */
+  int32_t blocks_per_split;   /* selected blocks per split-K work item; 0 = auto */
+} msa_config;
+
+/* Human-readable name of a status (static string). */
+const char* msa_status_string(msa_status status);
+
+/* MSA_OK if the kernels implement cfg, else INVALID_ARG / UNSUPPORTED.  Every
+ * entry point below runs this check first. */
+msa_status msa_validate_config(const msa_config* cfg);
+
+/* Width S of a selected list: init_blocks + local_blocks + topk_blocks. */
+int32_t msa_selected_width(const msa_config* cfg);
+
+/* Number of split-K partials per (token, query head) msa_sparse_decode writes. */
+int32_t msa_num_splits(const msa_config* cfg);
+
+/* Bytes of device workspace a step needs (plan metadata, a validated copy of
+ * the block table, split-K partials).  0 if cfg is not valid.  The workspace
+ * must be 256-byte aligned; its contents need no initialisation. */
+size_t msa_workspace_bytes(const msa_config* cfg);
+
+/*
+ * msa_plan -- split metadata for one step, built on the device
+ * (sglang MiniMaxSparseAttnBackend._prepare_msa_decode_meta: the decode plan is
+ * built per batch outside graph capture and refreshed in place; vLLM
+ * MiniMaxM3SparseMSAMetadataBuilder.build: block_table + seq_lens +
+ * decode_query_len).
+ *   batch        host int, 0 <= batch <= cfg->max_batch
+ *   seq_lens     [batch] int32
+ *   cu_seqlens_q [batch + 1] int32 or NULL; NULL = cfg->q_len tokens per request
+ *   block_table  [batch, bt_stride] int32; bt_stride >= cfg->max_blocks_per_req
+ *   ws           workspace of msa_workspace_bytes(cfg) bytes
+ * Writes per-request block counts and their prefix sums, per-token (request,
+ * position), and a validated copy of the block table into ws; resets the
+ * device error word.  Entries past a request's last block are not read.
+ */
+msa_status msa_plan(const msa_config* cfg, int32_t batch, const int32_t* seq_lens,
+                    const int32_t* cu_seqlens_q, const int32_t* block_table,
+                    int32_t bt_stride, void* ws, msa_stream_t stream);
+
+/*
+ * msa_plan_from_req_to_token -- as msa_plan, but the block table is derived
+ * from sglang's token-slot map (MiniMaxSparseAttnBackend._prepare_msa_decode_meta
+ * feeds req_to_token and req_pool_indices to update_msa_decode_cg_meta):
+ * page of block j of request r = req_to_token[req_pool_indices[r], j * P] / P.
+ *   req_to_token      [pool_rows, r2t_stride] int32 token slots
+ *   req_pool_indices  [batch] int64 rows of req_to_token
+ * A slot that is not a multiple of P sets MSA_DEVERR_SLOT_ALIGN.
+ */
+msa_status msa_plan_from_req_to_token(const msa_config* cfg, int32_t batch,
+                                      const int32_t* seq_lens,
+                                      const int32_t* cu_seqlens_q,
+                                      const int32_t* req_to_token, int32_t r2t_stride,
+                                      const int64_t* req_pool_indices, void* ws,
+                                      msa_stream_t stream);
+
+/*
+ * msa_index_score -- block scores from the index query/key
+ * (sglang MiniMaxSparseAttnBackend.__init__ reads the index head dim and
+ * score_type; forward_decode passes idx_q and the index-K cache to the sparse
+ * decode op).  For every token t, KV head h and visible block j:
+ *     block_scores[t, h, j] = max over tokens u of block j with
+ *                             position(u) <= position(t) of  idx_q[t,h,:] . idx_k[u,h,:]
+ * accumulated in fp32 (exact for the integer-valued index vectors used in
+ * tests).  Entries j >= the token's visible block count are not written.
+ * Bandwidth-bound: reads every visible index key once per request.
+ */
+msa_status msa_index_score(const msa_config* cfg, const void* ws, const void* idx_q,
+                           const void* idx_k_pages, float* block_scores,
+                           msa_stream_t stream);
+
+/*
+ * msa_topk_select -- per (token, KV head): blocks [0, init) U [nb - local, nb)
+ * U the topk best of the remaining blocks, ranked by score descending and block
+ * index ascending on ties; written ascending into selected[t, h, 0..S), the
+ * rest -1.  nb = position / P + 1.  (vLLM MiniMaxM3SparseMSAImpl.forward reads
+ * the per-token [H, MK] selected-block lists that this produces.)
+ */
+msa_status msa_topk_select(const msa_config* cfg, const void* ws,
+                           const float* block_scores, int32_t* selected,
+                           msa_stream_t stream);
+
+/*
+ * msa_sparse_decode -- split-K flash decoding over the selected blocks only
+ * (vLLM sparse_attention_msa.py module docstring and
+ * MiniMaxM3SparseMSAImpl.forward: split-K decode over the top-k blocks with
+ * block_table, seq_lens and decode_query_len; fp8 KV is dequantised on load).
+ * For each token t, KV head h and split s, every query head of h's group runs
+ * an online softmax over the tokens of the split's selected blocks that are at
+ * or before t's position, and the normalised partial output and its
+ * log-sum-exp are written to the workspace.  msa_combine finishes the step.
+ */
+msa_status msa_sparse_decode(const msa_config* cfg, void* ws, const void* q,
+                             const void* k_pages, const void* v_pages,
+                             const int32_t* selected, msa_stream_t stream);
+
+/*
+ * msa_combine -- log-sum-exp merge of the split-K partials in ws
+ * (FlashMLA decode in sglang flashmla_backend.py returns (o, lse) per split
+ * plan): lse = ln sum_s exp(lse_s), out = sum_s exp(lse_s - lse) o_s, out
+ * rounded to bf16.  All splits empty -> out = 0, lse = -inf.
+ */
+msa_status msa_combine(const msa_config* cfg, const void* ws, void* out, float* lse,
+                       msa_stream_t stream);
+
+/*
+ * msa_check_device_error -- synchronises `stream`, copies the workspace error
+ * word to *flags (host) and returns MSA_ERR_DEVICE_FLAG if any bit is set.
+ * Never call it inside stream capture.
+ */
+msa_status msa_check_device_error(const void* ws, int32_t* flags, msa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MSA_H_ */

@@ -92,10 +92,15 @@ def query_positions(seq_lens: Sequence[int], q_lens: Sequence[int]) -> List[Tupl
 
     ``seq_lens[r]`` counts request r's KV tokens including its ``q_lens[r]`` new
     ones (the fused cache write runs before attention in ``forward_decode`` and
-    ``forward_extend``), so the i-th new token is at seq_len - q_len + i."""
+    ``forward_extend``), so the i-th new token is at seq_len - q_len + i.
+    A request with seq_len 0 is idle (the idle-batch path of ``forward_decode``
+    returns zeros): its tokens get position -1 and see nothing."""
     out = []
     for r, (L, n) in enumerate(zip(seq_lens, q_lens)):
         L, n = int(L), int(n)
+        if L == 0:
+            out.extend((r, -1) for _ in range(n))
+            continue
         assert 0 <= n <= L, (r, L, n)
         for i in range(n):
             out.append((r, L - n + i))
@@ -238,6 +243,12 @@ def sparse_attention(*, seq_lens, q_lens, block_table, idx_q, idx_k_pages, q,
                 vv = e4m3_to_float(vv.astype(np.uint8)) * v_scale
             seq_cache = {r: (ik, kk, vv)}
         ik, kk, vv = seq_cache[r]
+        if p < 0:                              # idle request: attends to nothing
+            for h in kv_heads:
+                scores[(t, h)], selected[(t, h)] = np.zeros(0), []
+                out[t, h * G:(h + 1) * G] = 0.0
+                lse[t, h * G:(h + 1) * G] = -np.inf
+            continue
         for h in kv_heads:
             sc = block_scores(idx_q[t, h], ik[:, h, :], p, block_size)
             sel = select_blocks(sc, init_blocks, local_blocks, topk_blocks)

@@ -1,0 +1,110 @@
+"""GPU-side helpers for the parity tests: run the CUDA path, compare with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import block_sparse_paged_msa_gb300 as msa
+from block_sparse_paged_msa_gb300 import workloads as wl
+from oracle_io import oracle_local_blocks, run_oracle, selected_array, to_np
+
+# Acceptance bounds: selection bit-exact; out max |err| <= 1e-2 and mean |err|
+# <= 1e-3 against fp64 (bf16 output rounding alone is ~4e-3 relative); LSE
+# within 1e-3.
+OUT_MAX, OUT_MEAN, LSE_MAX = 1e-2, 1e-3, 1e-3
+
+
+def run_gpu(w: wl.Workload, **cfg_overrides):
+    cfg = msa.config_for(w.spec, **cfg_overrides)
+    sa = msa.SparseAttention(cfg, device=w.q.device)
+    sa.run(w.seq_lens, w.block_table, w.idx_q, w.idx_k_pages, w.q, w.k_pages, w.v_pages,
+           cu_seqlens_q=None if w.spec.q_len > 0 else w.cu_seqlens_q)
+    torch.cuda.synchronize()
+    return sa
+
+
+def compare(w: wl.Workload, sa, ref, tokens=None, kv_heads=None):
+    """Element-wise comparison of the GPU results with the oracle's over the
+    computed (token, KV head) pairs.  Returns the error statistics."""
+    spec = w.spec
+    T = w.num_tokens
+    G = spec.group
+    tokens = range(T) if tokens is None else tokens
+    kv_heads = range(spec.num_kv_heads) if kv_heads is None else kv_heads
+    sel = sa.selected[:T].cpu().numpy()
+    scores = sa.block_scores[:T].cpu().numpy()
+    out = to_np(sa.out[:T])
+    lse = sa.lse[:T].cpu().numpy().astype(np.float64)
+    errs, lerrs = [], []
+    for t in tokens:
+        for h in kv_heads:
+            want = ref["selected"][(t, h)]
+            got = [int(x) for x in sel[t, h]]
+            assert got == want + [-1] * (len(got) - len(want)), (t, h, got, want)
+            sc = ref["scores"][(t, h)]
+            assert np.array_equal(scores[t, h, :len(sc)], sc.astype(np.float32)), (t, h)
+            hs = slice(h * G, (h + 1) * G)
+            errs.append(np.abs(out[t, hs] - ref["out"][t, hs]).ravel())
+            lerrs.append(np.abs(lse[t, hs] - ref["lse"][t, hs]))
+    e = np.concatenate(errs)
+    le = np.concatenate(lerrs)
+    stats = dict(out_max=float(e.max()), out_mean=float(e.mean()), lse_max=float(le.max()))
+    assert stats["out_max"] <= OUT_MAX and stats["out_mean"] <= OUT_MEAN, stats
+    assert stats["lse_max"] <= LSE_MAX, stats
+    return stats
+
+
+def sub_problem(w: wl.Workload, t: int, h: int) -> wl.Workload:
+    """Token t and KV head h of a large workload as a stand-alone workload with
+    one request and one KV head: only that request's pages are copied, in
+    logical order (the oracle is invariant to the physical page order, which
+    its pins check)."""
+    spec = w.spec
+    r = int(torch.searchsorted(w.cu_seqlens_q, torch.tensor([t], device=w.cu_seqlens_q.device,
+                                                            dtype=torch.int32), right=True)[0]) - 1
+    L = int(w.seq_lens[r])
+    nb = -(-L // spec.block_size)
+    pages = w.block_table[r, :nb].long()
+    G = spec.group
+    q0 = int(w.cu_seqlens_q[r])
+    nq = int(w.q_lens[r])
+    sub_spec = spec.replace(batch=1, num_kv_heads=1, num_q_heads=G, num_pages=nb,
+                            seq_lens=(L,), seq_len_range=None, q_len=nq)
+    hs = slice(h, h + 1)
+    return wl.Workload(
+        spec=sub_spec,
+        seq_lens=w.seq_lens[r:r + 1].cpu(), q_lens=w.q_lens[r:r + 1].cpu(),
+        cu_seqlens_q=torch.tensor([0, nq], dtype=torch.int32),
+        block_table=torch.arange(nb, dtype=torch.int32)[None],
+        idx_q=w.idx_q[q0:q0 + nq, hs].cpu(), idx_k_pages=w.idx_k_pages[pages][:, hs].cpu(),
+        q=w.q[q0:q0 + nq, h * G:(h + 1) * G].cpu(), k_pages=w.k_pages[pages][:, hs].cpu(),
+        v_pages=w.v_pages[pages][:, hs].cpu()), r, q0
+
+
+def compare_sampled(w: wl.Workload, sa, samples):
+    """Full-size parity on sampled (token, KV head) pairs, each re-derived by the
+    oracle from a one-request copy of the inputs."""
+    spec = w.spec
+    G = spec.group
+    T = w.num_tokens
+    sel = sa.selected[:T].cpu().numpy()
+    out = to_np(sa.out[:T])
+    lse = sa.lse[:T].cpu().numpy().astype(np.float64)
+    scores = sa.block_scores[:T].cpu().numpy()
+    worst = dict(out_max=0.0, out_mean=0.0, lse_max=0.0)
+    for t, h in samples:
+        sub, r, q0 = sub_problem(w, t, h)
+        ref = run_oracle(sub, tokens=[t - q0])
+        want = ref["selected"][(t - q0, 0)]
+        got = [int(x) for x in sel[t, h]]
+        assert got == want + [-1] * (len(got) - len(want)), (t, h, got, want)
+        sc = ref["scores"][(t - q0, 0)]
+        assert np.array_equal(scores[t, h, :len(sc)], sc.astype(np.float32)), (t, h)
+        e = np.abs(out[t, h * G:(h + 1) * G] - ref["out"][t - q0])
+        le = np.abs(lse[t, h * G:(h + 1) * G] - ref["lse"][t - q0])
+        worst["out_max"] = max(worst["out_max"], float(e.max()))
+        worst["out_mean"] = max(worst["out_mean"], float(e.mean()))
+        worst["lse_max"] = max(worst["lse_max"], float(le.max()))
+    assert worst["out_max"] <= OUT_MAX and worst["out_mean"] <= OUT_MEAN, worst
+    assert worst["lse_max"] <= LSE_MAX, worst
+    return worst

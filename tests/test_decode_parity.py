@@ -1,0 +1,94 @@
+"""CUDA path vs the fp64 oracle for decode and speculative verify (GPU).
+
+Selections and block scores are compared bit-exactly (integer-valued index
+vectors make every dot product exact in fp32 and fp64); out and LSE within the
+bounds in gpu_util.  Small cases span several blocks and ragged last pages and
+are compared on every element; the full-size medium decode (batch 32, seq_lens
+8k..32k, 64/8 heads) runs in the launch configuration the bench times and is
+compared on sampled (token, KV head) pairs."""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_paged_msa_gb300 as msa
+from block_sparse_paged_msa_gb300 import workloads as wl
+from gpu_util import compare, compare_sampled, run_gpu
+from oracle_io import run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_case(spec):
+    w = wl.make_workload(spec, device="cuda")
+    sa = run_gpu(w)
+    assert msa.check_device_error(sa.ws) == 0
+    return compare(w, sa, run_oracle(w.to("cpu")))
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "medium_decode", "fp8_decode", "long_decode",
+                                  "verify"])
+def test_small_workloads_every_element(name):
+    spec = wl.WORKLOADS[name] if name == "tiny_decode" else wl.small(name)
+    print(name, _full_case(spec))
+
+
+@pytest.mark.parametrize("seed", [11, 12, 13])
+def test_random_seeds_ragged(seed):
+    spec = wl.small("medium_decode", seed=seed, batch=5, seq_len_range=(1, 2200),
+                    num_pages=120)
+    _full_case(spec)
+
+
+def test_group_16_and_index_dim_64():
+    spec = wl.small("medium_decode", num_q_heads=32, num_kv_heads=2, index_dim=64, batch=3)
+    _full_case(spec)
+
+
+def test_group_1_and_topk_0():
+    spec = wl.small("medium_decode", num_q_heads=4, num_kv_heads=4, topk_blocks=0, batch=3)
+    _full_case(spec)
+
+
+@pytest.mark.parametrize("bps", [1, 2, 7, 32])
+def test_split_sizes_agree(bps):
+    spec = wl.small("medium_decode", batch=3)
+    w = wl.make_workload(spec, device="cuda")
+    ref = run_oracle(w.to("cpu"))
+    sa = run_gpu(w, blocks_per_split=bps)
+    compare(w, sa, ref)
+
+
+def test_block_boundaries_and_short_requests():
+    # exact multiples of the block, one token, within init+local, one past a block
+    spec = wl.small("medium_decode", seq_lens=(128, 1, 384, 129, 1024, 255), seq_len_range=None,
+                    batch=6, num_pages=64)
+    _full_case(spec)
+
+
+def test_medium_decode_full_size_sampled():
+    spec = wl.WORKLOADS["medium_decode"]
+    w = wl.make_workload(spec, device="cuda")
+    sa = run_gpu(w)
+    assert msa.check_device_error(sa.ws) == 0
+    rng = np.random.default_rng(0)
+    samples = [(int(t), int(h)) for t, h in zip(rng.integers(0, spec.batch, 6),
+                                                 rng.integers(0, spec.num_kv_heads, 6))]
+    samples += [(0, 0), (spec.batch - 1, spec.num_kv_heads - 1)]
+    print(compare_sampled(w, sa, samples))
+    # properties that hold everywhere: selection sizes and bounds
+    P = 128
+    nb = (w.seq_lens.long() + P - 1) // P
+    sel = sa.selected[:spec.batch].long()
+    width = sel.shape[-1]
+    assert bool((sel[..., :width] >= -1).all())
+    assert bool(((sel >= 0).sum(-1) == torch.clamp(nb, max=width)[:, None]).all())
+    assert torch.isfinite(sa.out[:spec.batch].float()).all()
+
+
+def test_verify_full_size_sampled():
+    spec = wl.WORKLOADS["verify"]
+    w = wl.make_workload(spec, device="cuda")
+    sa = run_gpu(w)
+    assert msa.check_device_error(sa.ws) == 0
+    samples = [(0, 0), (1, 3), (2, 7), (3, 5), (255, 7), (128, 2)]
+    print(compare_sampled(w, sa, samples))

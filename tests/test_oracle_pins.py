@@ -61,6 +61,8 @@ def test_query_positions_decode_verify_prefill():
     assert oracle.query_positions([10], [4]) == [(0, 6), (0, 7), (0, 8), (0, 9)]
     assert oracle.query_positions([5, 3], [2, 3]) == [(0, 3), (0, 4), (1, 0), (1, 1), (1, 2)]
     assert oracle.query_positions([7], [0]) == []
+    # an idle request (seq_len 0) keeps its token rows, at position -1
+    assert oracle.query_positions([0, 3], [1, 1]) == [(0, -1), (1, 2)]
 
 
 def test_gather_sequence_follows_block_table():
