@@ -43,7 +43,11 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the index-score
 # kernel, from the ncu capture summarised in profiles/ (None until captured for
 # the current kernel).
-NCU_TRAFFIC_BYTES = {}
+NCU_TRAFFIC_BYTES = {
+    # batch-8 / 2048-page capture: 372.6 MB for 367.7 MB algorithmic, scaled by
+    # bytes to a full medium-decode launch (1.2608 GB algorithmic)
+    ("medium_decode", "index_score"): 1.2776e9,
+}
 
 
 # ----------------------------------------------------------------- helpers
@@ -228,7 +232,7 @@ def run_ours(args, rank, world, local_rank):
         msa_build.build()
     if world > 1:
         torch.distributed.barrier()
-    spec = wl.WORKLOADS[args.workload].replace(seed=wl.WORKLOADS[args.workload].seed + rank)
+    spec = workload_spec(args).replace(seed=workload_spec(args).seed + rank)
     w = wl.make_workload(spec, device=dev)
     cfg = msa.config_for(spec)
     sa = msa.SparseAttention(cfg, device=dev)
@@ -352,10 +356,22 @@ def run_ours(args, rank, world, local_rank):
     return result, w
 
 
+def workload_spec(args) -> wl.WorkloadSpec:
+    spec = wl.WORKLOADS[args.workload]
+    kw = {}
+    if args.batch is not None:
+        kw["batch"] = args.batch
+        if spec.seq_lens is not None:
+            kw["seq_lens"] = (spec.seq_lens * args.batch)[:args.batch]
+    if args.pool_pages is not None:
+        kw["num_pages"] = args.pool_pages
+    return spec.replace(**kw) if kw else spec
+
+
 def run_reference(args):
     """The fp64 oracle on the host cores: each step one (token, KV head) pair."""
     import oracle
-    spec = wl.WORKLOADS[args.workload]
+    spec = workload_spec(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     w = wl.make_workload(spec, device=dev)
     gen = _oracle_problems(w, seed=1)
@@ -388,6 +404,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="medium_decode", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (smaller profiling captures)")
+    ap.add_argument("--pool-pages", type=int, default=None,
+                    help="override the workload's KV pool size in pages")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
