@@ -63,7 +63,10 @@ _SIGNATURES = {
     "msa_sparse_decode": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "msa_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "msa_check_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+    "msa_sparse_decode_noalloc": (ctypes.c_int, [_CFG, ctypes.c_int32, _P, _P, ctypes.c_int32,
+                                                 _P, _P, _P, _P, _P, _P, _P]),
 }
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def lib_path() -> str:
@@ -276,3 +279,28 @@ class SparseAttention:
         sparse_decode(c, self.ws, q, k_pages, v_pages, self.selected, stream)
         combine(c, self.ws, self.out, self.lse, stream)
         return self.out, self.lse
+
+
+def sparse_decode_noalloc(cfg, seq_lens, block_table, q, k_pages, v_pages, selected, out, lse,
+                          stream=None):
+    """Plan + split-K decode + combine without a workspace or any allocation,
+    for callers that cannot allocate device memory (their allocator owns all
+    of it, or HBM is reserved for the KV cache, or the call sits on a path
+    where cudaMalloc is not acceptable).  Scratch is a fixed 16 MiB device
+    array inside libmsa; steps that need more raise MsaError (UNSUPPORTED).
+    The first call on a device must come before any stream capture; calls
+    that overlap on the GPU share that scratch and race."""
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(q, "q", torch.bfloat16, 3)
+    kv = (torch.bfloat16,) if cfg.kv_dtype == MSA_KV_BF16 else (torch.float8_e4m3fn, torch.uint8)
+    _need(k_pages, "k_pages", kv, 4)
+    _need(v_pages, "v_pages", kv, 4)
+    _need(selected, "selected", torch.int32, 3)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    _check("msa_sparse_decode_noalloc", lib().msa_sparse_decode_noalloc(
+        ctypes.byref(cfg), seq_lens.shape[0], _ptr(seq_lens), _ptr(block_table),
+        block_table.shape[1], _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(selected), _ptr(out),
+        _ptr(lse), _stream(stream)),
+        "(the step may need more than the 16 MiB scratch: see msa_workspace_bytes)")

@@ -215,6 +215,34 @@ msa_status msa_combine(const msa_config* cfg, const void* ws, void* out, float* 
                        msa_stream_t stream);
 
 /*
+ * msa_sparse_decode_noalloc -- msa_plan + msa_sparse_decode + msa_combine in
+ * one call that allocates nothing and takes no workspace.  The method's pages
+ * have no counterpart; it exists for callers that cannot allocate device
+ * memory (a host framework whose allocator owns all device memory, a serving
+ * loop that reserved nearly all HBM for its KV cache, a latency-critical path
+ * that cannot afford cudaMalloc / cudaFree).  The caller passes its inputs
+ * (seq_lens, block_table as for msa_plan with cu_seqlens_q = NULL; q, k_pages,
+ * v_pages; `selected` as msa_topk_select writes it, e.g. from its own indexer)
+ * and its outputs (out, lse, as msa_combine writes them).
+ * Scratch: a fixed device array of MSA_NOALLOC_SCRATCH_BYTES inside the
+ * library, held by every GPU that loads the library until the process exits.
+ * Returns MSA_ERR_UNSUPPORTED, before any launch, when the step needs more
+ * than that (msa_workspace_bytes(cfg) > MSA_NOALLOC_SCRATCH_BYTES).
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array: calls whose work overlaps on the
+ * GPU (other streams, other threads) race and must be serialised by the
+ * caller.  Each call rewrites every part of the scratch it reads, so earlier
+ * contents never leak into a result.
+ */
+#define MSA_NOALLOC_SCRATCH_BYTES (16u << 20)
+msa_status msa_sparse_decode_noalloc(const msa_config* cfg, int32_t batch,
+                                     const int32_t* seq_lens, const int32_t* block_table,
+                                     int32_t bt_stride, const void* q, const void* k_pages,
+                                     const void* v_pages, const int32_t* selected, void* out,
+                                     float* lse, msa_stream_t stream);
+
+/*
  * msa_check_device_error -- synchronises `stream`, copies the workspace error
  * word to *flags (host) and returns MSA_ERR_DEVICE_FLAG if any bit is set.
  * Never call it inside stream capture.

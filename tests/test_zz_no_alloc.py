@@ -1,0 +1,86 @@
+"""msa_sparse_decode_noalloc: the decode step for callers that cannot allocate
+device memory (their framework's allocator owns all of it, HBM is reserved for
+the KV cache, or cudaMalloc is not acceptable on the call's path).
+
+Called through the C ABI with no workspace, twice in a row (the second call
+runs on scratch left by the first), it must agree with the workspace-based
+entry points within the parity tolerances; steps too large for its fixed
+scratch are refused before any launch.  Collected last so that a failure here
+never hides another test's result."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_paged_msa_gb300 as msa
+from block_sparse_paged_msa_gb300 import ops
+from block_sparse_paged_msa_gb300 import workloads as wl
+from gpu_util import LSE_MAX, OUT_MAX, OUT_MEAN
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(cfg, w, selected, out, lse):
+    st = ops.lib().msa_sparse_decode_noalloc(
+        ctypes.byref(cfg), w.seq_lens.shape[0], w.seq_lens.data_ptr(), w.block_table.data_ptr(),
+        w.block_table.shape[1], w.q.data_ptr(), w.k_pages.data_ptr(), w.v_pages.data_ptr(),
+        selected.data_ptr(), out.data_ptr(), lse.data_ptr(),
+        torch.cuda.current_stream().cuda_stream)
+    assert st == 0, ops.status_string(st)
+
+
+def _close(a_out, a_lse, b_out, b_lse):
+    e = (a_out.double() - b_out.double()).abs()
+    assert float(e.max()) <= OUT_MAX and float(e.mean()) <= OUT_MEAN
+    fin = torch.isfinite(b_lse)
+    assert torch.equal(fin, torch.isfinite(a_lse))
+    assert float((a_lse[fin].double() - b_lse[fin].double()).abs().max()) <= LSE_MAX
+
+
+@pytest.mark.parametrize("first,second", [("medium_decode", "fp8_decode")])
+def test_noalloc_matches_workspace_path_two_calls(first, second):
+    for name in (first, second):
+        spec = wl.small(name, batch=4)
+        w = wl.make_workload(spec, device="cuda")
+        cfg = msa.config_for(spec)
+        assert msa.workspace_bytes(cfg) <= ops.NOALLOC_SCRATCH_BYTES
+        ref = msa.SparseAttention(cfg)
+        ref.run(w.seq_lens, w.block_table, w.idx_q, w.idx_k_pages, w.q, w.k_pages, w.v_pages)
+        T = w.num_tokens
+        for call in range(2):
+            out = torch.full_like(ref.out[:T], float("nan"))
+            lse = torch.full_like(ref.lse[:T], float("nan"))
+            _noalloc(cfg, w, ref.selected, out, lse)
+            torch.cuda.synchronize()
+            _close(out, lse, ref.out[:T], ref.lse[:T])
+
+
+def test_noalloc_full_size_medium_decode():
+    spec = wl.WORKLOADS["medium_decode"]
+    w = wl.make_workload(spec, device="cuda")
+    cfg = msa.config_for(spec)
+    ref = msa.SparseAttention(cfg)
+    ref.run(w.seq_lens, w.block_table, w.idx_q, w.idx_k_pages, w.q, w.k_pages, w.v_pages)
+    T = w.num_tokens
+    for _ in range(2):
+        out = torch.empty_like(ref.out[:T])
+        lse = torch.empty_like(ref.lse[:T])
+        msa.ops.sparse_decode_noalloc(cfg, w.seq_lens, w.block_table, w.q, w.k_pages, w.v_pages,
+                                      ref.selected, out, lse)
+        torch.cuda.synchronize()
+        _close(out, lse, ref.out[:T], ref.lse[:T])
+
+
+def test_noalloc_refuses_steps_beyond_its_scratch():
+    spec = wl.small("medium_decode", batch=4)
+    w = wl.make_workload(spec, device="cuda")
+    big = msa.config_for(spec, max_batch=4096, blocks_per_split=1)
+    assert msa.workspace_bytes(big) > ops.NOALLOC_SCRATCH_BYTES
+    out = torch.zeros((4, 64, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((4, 64), dtype=torch.float32, device="cuda")
+    sel = torch.zeros((4, 8, 20), dtype=torch.int32, device="cuda")
+    with pytest.raises(msa.MsaError, match="UNSUPPORTED"):
+        msa.ops.sparse_decode_noalloc(big, w.seq_lens, w.block_table, w.q, w.k_pages, w.v_pages,
+                                      sel, out, lse)
+    assert bool((out == 0).all())
