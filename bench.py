@@ -145,13 +145,38 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def measured_peak_hbm():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def measured_peaks():
+    """(value, "measured" | "fallback") for hbm_gbs, bf16_tflops and
+    bf16_tflops_sustained."""
+    fallback = {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1900.0,
+                "bf16_tflops_sustained": 1700.0}
     try:
-        with open(p) as f:
-            return float(json.load(f)["hbm_gbs"]), "measured"
-    except (OSError, KeyError, ValueError):
-        return FALLBACK_HBM_GBS, "fallback"
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+    except (OSError, ValueError):
+        m = {}
+    return {k: ((float(m[k]), "measured") if k in m else (v, "fallback"))
+            for k, v in fallback.items()}
+
+
+def prefill_flops(w: wl.Workload, selected: torch.Tensor) -> dict:
+    """Algorithmic FLOPs of a prefill step.
+
+    index score: 2 * d per (query token, KV head, visible key);
+    sparse prefill (selected tiles): 4 * D per (query token, query head,
+    visible key of a selected block) -- QK^T and PV."""
+    s = w.spec
+    P = s.block_size
+    T = w.num_tokens
+    q_lens = w.q_lens.long()
+    pos = (w.seq_lens.long().repeat_interleave(q_lens) - q_lens.repeat_interleave(q_lens)
+           + torch.cat([torch.arange(int(n), device=q_lens.device) for n in q_lens.tolist()]))
+    idx = int((pos + 1).sum()) * s.num_kv_heads * 2 * s.index_dim
+    sel = selected[:T].long()
+    vis = (pos[:, None, None] + 1 - sel * P).clamp(0, P)
+    vis = torch.where(sel >= 0, vis, torch.zeros_like(vis))
+    att = int(vis.sum()) * s.group * 4 * s.head_dim
+    return {"index_score": idx, "sparse_prefill": att}
 
 
 # ----------------------------------------------------------------- oracle leg
@@ -237,19 +262,31 @@ def run_ours(args, rank, world, local_rank):
     cfg = msa.config_for(spec)
     sa = msa.SparseAttention(cfg, device=dev)
     stream = torch.cuda.current_stream()
-    args_run = (w.seq_lens, w.block_table, w.idx_q, w.idx_k_pages, w.q, w.k_pages, w.v_pages)
-    names = ["plan", "index_score", "topk_select", "sparse_decode", "combine"]
+    cu = w.cu_seqlens_q if sa.prefill else None
+    c = sa.cfg
+    calls = [
+        ("plan", lambda: msa.plan(c, w.seq_lens, w.block_table, sa.ws, cu)),
+        ("index_score", lambda: msa.index_score(c, sa.ws, w.idx_q, w.idx_k_pages,
+                                                sa.block_scores)),
+        ("topk_select", lambda: msa.topk_select(c, sa.ws, sa.block_scores, sa.selected)),
+    ]
+    if sa.prefill:
+        calls += [
+            ("build_k2q_csr", lambda: msa.ops.build_k2q_csr(c, sa.ws, sa.selected, sa.row_ptr,
+                                                            sa.q_indices)),
+            ("sparse_prefill", lambda: msa.ops.sparse_prefill(
+                c, sa.ws, w.q, w.k_pages, w.v_pages, sa.selected, sa.row_ptr, sa.q_indices)),
+        ]
+    else:
+        calls += [("sparse_decode", lambda: msa.sparse_decode(c, sa.ws, w.q, w.k_pages,
+                                                              w.v_pages, sa.selected))]
+    calls += [("combine", lambda: msa.combine(c, sa.ws, sa.out, sa.lse))]
+    names = [n for n, _ in calls]
+    launches_per_step = {"plan": 1, "index_score": 1, "topk_select": 1, "build_k2q_csr": 3,
+                         "sparse_prefill": 1, "sparse_decode": 1, "combine": 1}
 
     def step(evs=None):
-        c = sa.cfg
-        calls = [
-            lambda: msa.plan(c, w.seq_lens, w.block_table, sa.ws),
-            lambda: msa.index_score(c, sa.ws, w.idx_q, w.idx_k_pages, sa.block_scores),
-            lambda: msa.topk_select(c, sa.ws, sa.block_scores, sa.selected),
-            lambda: msa.sparse_decode(c, sa.ws, w.q, w.k_pages, w.v_pages, sa.selected),
-            lambda: msa.combine(c, sa.ws, sa.out, sa.lse),
-        ]
-        for i, fn in enumerate(calls):
+        for i, (_, fn) in enumerate(calls):
             if evs is not None:
                 evs[i][0].record(stream)
             fn()
@@ -281,7 +318,9 @@ def run_ours(args, rank, world, local_rank):
                   for i, n in enumerate(names)}
 
     # ---- e2e: host buffers in, result out, through the public API
-    pin = {k: getattr(w, k).cpu().pin_memory() for k in ("seq_lens", "block_table", "idx_q", "q")}
+    step_inputs = ("seq_lens", "block_table", "idx_q", "q") + (("cu_seqlens_q",) if sa.prefill
+                                                               else ())
+    pin = {k: getattr(w, k).cpu().pin_memory() for k in step_inputs}
     dbuf = {k: torch.empty_like(getattr(w, k)) for k in pin}
     out_h = torch.empty(sa.out.shape, dtype=sa.out.dtype).pin_memory()
     lse_h = torch.empty(sa.lse.shape, dtype=sa.lse.dtype).pin_memory()
@@ -292,7 +331,7 @@ def run_ours(args, rank, world, local_rank):
         for k, t in pin.items():
             dbuf[k].copy_(t, non_blocking=True)
         sa.run(dbuf["seq_lens"], dbuf["block_table"], dbuf["idx_q"], w.idx_k_pages, dbuf["q"],
-               w.k_pages, w.v_pages)
+               w.k_pages, w.v_pages, cu_seqlens_q=dbuf.get("cu_seqlens_q"))
         out_h.copy_(sa.out, non_blocking=True)
         lse_h.copy_(sa.lse, non_blocking=True)
 
@@ -312,8 +351,6 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1)
 
     # ---- accounting
-    ab = algorithmic_bytes(w)
-    db = decode_bytes(w, sa.selected, msa.num_splits(cfg))
     T = w.num_tokens
     t_max = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -321,38 +358,59 @@ def run_ours(args, rank, world, local_rank):
     ms, e2e_ms = float(t_max[0]), float(t_max[1])
     value = T * world * K / (ms / 1e3)
     e2e_value = T * world * Ke / (e2e_ms / 1e3)
-    peak, peak_kind = measured_peak_hbm()
-    idx_gbs = ab["index_score"] / (per_kernel["index_score"] / 1e3) / 1e9
-    step_bytes = ab["index_score"] + db["decode"] + db["combine"]
+    peaks = measured_peaks()
     result = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "metric": METRIC if not sa.prefill else "sparse-prefill query-tokens/s",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if spec.kv_dtype == "bf16" else "fp8_e4m3",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if spec.kv_dtype == "bf16" else "fp8_e4m3",
         "data": "synthetic (seeded; integer-valued bf16 index vectors, N(0,1) bf16 q/k/v)",
         "config": {"workload": spec.name, "batch": spec.batch,
                    "seq_lens": list(spec.seq_len_range or spec.seq_lens[:1]),
+                   "q_per_request": spec.q_len,
                    "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads,
                    "head_dim": spec.head_dim, "index_dim": spec.index_dim,
                    "block": spec.block_size, "init_local_topk": [spec.init_blocks,
                    msa.ops.local_blocks_from_tokens(spec.local_tokens), spec.topk_blocks],
-                   "pool_pages": spec.num_pages, "parallelism": f"replicas{world}",
-                   "l2": f"no flush: {step_bytes / 1e9:.2f} GB touched per step > 129 MB L2"},
-        "roofline": {"bound": "hbm", "kernel": "index_score", "achieved": idx_gbs,
-                     "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak,
-                     "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": NCU_TRAFFIC_BYTES.get((spec.name, "index_score"))},
-        "step_hbm": {"algorithmic_bytes": step_bytes,
-                     "achieved_gbs": step_bytes / (ms / K / 1e3) / 1e9,
-                     "frac": step_bytes / (ms / K / 1e3) / 1e9 / peak},
+                   "pool_pages": spec.num_pages, "parallelism": f"replicas{world}"},
         "kernels_ms": per_kernel,
-        "kernel_gbs": {"index_score": idx_gbs,
-                       "sparse_decode": db["decode"] / (per_kernel["sparse_decode"] / 1e3) / 1e9,
-                       "combine": db["combine"] / (per_kernel["combine"] / 1e3) / 1e9},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 5 * K,
+        "gpu_launches": sum(launches_per_step[n] for n in names) * K,
         "clocks": clk.summary(),
     }
+    if sa.prefill:
+        fl = prefill_flops(w, sa.selected)
+        achieved = {n: fl[n] / (per_kernel[n] / 1e3) / 1e12 for n in ("index_score", "sparse_prefill")}
+        peak = peaks["bf16_tflops_sustained"]
+        result["roofline"] = {
+            "bound": "tensor", "kernel": "sparse_prefill", "achieved": achieved["sparse_prefill"],
+            "peak": peak[0], "unit": "TFLOP/s", "frac": achieved["sparse_prefill"] / peak[0],
+            "peak_source": f"{peak[1]} bf16_tflops_sustained",
+            "traffic": NCU_TRAFFIC_BYTES.get((spec.name, "sparse_prefill"))}
+        result["kernel_tflops"] = achieved
+        result["flops_per_step"] = {k: fl[k] for k in ("index_score", "sparse_prefill")}
+        result["config"]["l2"] = "no flush: K/V + index pools 0.9 GB and 2.7 GB of partials > L2"
+    else:
+        ab = algorithmic_bytes(w)
+        db = decode_bytes(w, sa.selected, msa.num_splits(cfg))
+        peak = peaks["hbm_gbs"]
+        idx_gbs = ab["index_score"] / (per_kernel["index_score"] / 1e3) / 1e9
+        step_bytes = ab["index_score"] + db["decode"] + db["combine"]
+        result["roofline"] = {"bound": "hbm", "kernel": "index_score", "achieved": idx_gbs,
+                              "peak": peak[0], "unit": "GB/s", "frac": idx_gbs / peak[0],
+                              "peak_source": f"{peak[1]} hbm_gbs",
+                              "traffic": NCU_TRAFFIC_BYTES.get((spec.name, "index_score"))}
+        result["step_hbm"] = {"algorithmic_bytes": step_bytes,
+                              "achieved_gbs": step_bytes / (ms / K / 1e3) / 1e9,
+                              "frac": step_bytes / (ms / K / 1e3) / 1e9 / peak[0]}
+        result["kernel_gbs"] = {
+            "index_score": idx_gbs,
+            "sparse_decode": db["decode"] / (per_kernel["sparse_decode"] / 1e3) / 1e9,
+            "combine": db["combine"] / (per_kernel["combine"] / 1e3) / 1e9}
+        result["config"]["l2"] = (f"no flush: {step_bytes / 1e9:.2f} GB touched per step "
+                                  f"> 129 MB L2")
     return result, w
 
 

@@ -27,7 +27,7 @@
 // msa_combine merges them in a fixed order (deterministic).
 #include <mutex>
 
-#include "msa_internal.cuh"
+#include "msa_device.cuh"
 
 namespace msa {
 namespace {
@@ -35,8 +35,6 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kStages = 3;
 constexpr int kTileBytes = kBlock * kHeadDim * 2;  // bf16 tile, 32 KiB
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 struct DecodeArgs {
   int Hkv, Hq, G, S, bps, nsplit, max_blocks;
@@ -47,61 +45,6 @@ struct DecodeArgs {
   const uint8_t* v;
   const int32_t* selected;
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                          uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Byte offset of 16-byte chunk `c` (0..15) of row `row` in a swizzled bf16 tile.
-__device__ __forceinline__ uint32_t swz(int row, int c) {
-  return (uint32_t)(row * 256 + ((c ^ (row & 7)) << 4));
-}
-
-// e4m3 byte pair -> bf16x2 (exact): via the hardware f16x2 conversion.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
-  uint32_t h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
-  const __half2 hh = *reinterpret_cast<const __half2*>(&h);
-  const float2 f = __half22float2(hh);
-  return pack_bf16(f.x, f.y);
-}
 
 // Issue the copy of one K or V tile (block slot i, kind 0 = K, 1 = V) into ring
 // buffer `buf`.  bf16: 2048 16-byte chunks, swizzled.  fp8: 1024 raw chunks.
@@ -357,13 +300,17 @@ decode_kernel(WsView ws, DecodeArgs a) {
     }
     const int64_t hq = (int64_t)t * a.Hq + (int64_t)h * a.G + row;
     const bool empty = !(L > 0.f);
-    ws.o_part[(hq * a.nsplit + s) * kHeadDim + col] = empty ? 0.f : o * (a.v_scale / L);
+    static_cast<float*>(ws.o_part)[(hq * a.nsplit + s) * kHeadDim + col] =
+        empty ? 0.f : o * (a.v_scale / L);
     if (col == 0)
       ws.lse_part[hq * a.nsplit + s] = empty ? -INFINITY : (M + log2f(L)) * kLn2;
   }
 }
 
-// ---- combine: one warp per (token, query head)
+// ---- combine: one warp per (token, query head), splits merged in a fixed
+// order.  PREFILL: fp16 partials, one per selected slot, of which the first
+// min(nb, S) exist (nb = the token's visible blocks).
+template <bool PREFILL>
 __global__ void __launch_bounds__(256)
 combine_kernel(WsView ws, int Hq, int nsplit, __nv_bfloat16* __restrict__ out,
                float* __restrict__ lse) {
@@ -372,24 +319,32 @@ combine_kernel(WsView ws, int Hq, int nsplit, __nv_bfloat16* __restrict__ out,
   const int t = (int)(idx / Hq);
   if (t >= ws.hdr->num_tokens) return;
   const bool active = ws.tok_req[t] >= 0;
-  float ls = -INFINITY;
-  if (active && lane < nsplit) ls = ws.lse_part[idx * nsplit + lane];
-  float M = ls;
+  int nvalid = nsplit;
+  if (PREFILL) nvalid = active ? min(nsplit, ws.tok_pos[t] / kBlock + 1) : 0;
+  const float* lp = ws.lse_part + idx * nsplit;
+  float M = -INFINITY;
+  if (active)
+    for (int s = lane; s < nvalid; s += 32) M = fmaxf(M, lp[s]);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  for (int base = 32; active && base < nsplit; base += 32) {   // nsplit > 32 (rare)
-    for (int s = base; s < nsplit; ++s) M = fmaxf(M, ws.lse_part[idx * nsplit + s]);
-    break;
-  }
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  float L = 0.f;
   if (M != -INFINITY) {
-    for (int s = 0; s < nsplit; ++s) L += exp2f((ws.lse_part[idx * nsplit + s] - M) * kLog2e);
+    float L = 0.f;
+    for (int s = 0; s < nvalid; ++s) L += exp2f((lp[s] - M) * kLog2e);
     const float lse_tot = M + logf(L);
-    for (int s = 0; s < nsplit; ++s) {
-      const float w = expf(ws.lse_part[idx * nsplit + s] - lse_tot);
-      const float4 v =
-          *reinterpret_cast<const float4*>(ws.o_part + (idx * nsplit + s) * kHeadDim + 4 * lane);
+    for (int s = 0; s < nvalid; ++s) {
+      const float w = expf(lp[s] - lse_tot);
+      float4 v;
+      if (PREFILL) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(
+            static_cast<const __half*>(ws.o_part) + (idx * nsplit + s) * kHeadDim + 4 * lane);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+        v = make_float4(a.x, a.y, b.x, b.y);
+      } else {
+        v = *reinterpret_cast<const float4*>(static_cast<const float*>(ws.o_part) +
+                                             (idx * nsplit + s) * kHeadDim + 4 * lane);
+      }
       o.x = fmaf(w, v.x, o.x); o.y = fmaf(w, v.y, o.y);
       o.z = fmaf(w, v.z, o.z); o.w = fmaf(w, v.w, o.w);
     }
@@ -435,6 +390,7 @@ extern "C" msa_status msa_sparse_decode(const msa_config* cfg, void* ws, const v
   if (st != MSA_OK) return st;
   if (!ws || !q || !k_pages || !v_pages || !selected) return MSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages)) return MSA_ERR_INVALID_ARG;
+  if (is_prefill(*cfg)) return MSA_ERR_INVALID_ARG;   // prefill uses msa_sparse_prefill
   const int S = width_of(*cfg);
   if (S > 64 * 1024) return MSA_ERR_UNSUPPORTED;
   DecodeArgs a;
@@ -478,7 +434,11 @@ extern "C" msa_status msa_combine(const msa_config* cfg, const void* ws, void* o
   if (items <= 0) return MSA_OK;
   const int64_t grid = (items + 7) / 8;
   if (grid > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
-  combine_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
-      view_of(*cfg, ws), cfg->num_q_heads, splits_of(*cfg), (__nv_bfloat16*)out, lse);
+  if (is_prefill(*cfg))
+    combine_kernel<true><<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
+        view_of(*cfg, ws), cfg->num_q_heads, splits_of(*cfg), (__nv_bfloat16*)out, lse);
+  else
+    combine_kernel<false><<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
+        view_of(*cfg, ws), cfg->num_q_heads, splits_of(*cfg), (__nv_bfloat16*)out, lse);
   return launch_status();
 }

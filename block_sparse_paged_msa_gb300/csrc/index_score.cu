@@ -52,7 +52,7 @@ __device__ __forceinline__ float dot8(const float (&q)[8], const uint4& w) {
 // DIDX: index dim (64 | 128).  QL: query tokens per request scored together
 // (1 = decode, up to 4 = speculative verify); they share every key load.
 template <int DIDX, int QL>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, QL == 1 ? 5 : 2)
 index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
                    const uint4* __restrict__ idx_q,
                    const uint4* __restrict__ idx_k, float* __restrict__ scores) {
@@ -198,6 +198,7 @@ extern "C" msa_status msa_index_score(const msa_config* cfg, const void* ws, con
   if (!aligned16(idx_q) || !aligned16(idx_k_pages)) return MSA_ERR_INVALID_ARG;
   const WsView v = view_of(*cfg, ws);
   cudaStream_t s = (cudaStream_t)stream;
+  if (is_prefill(*cfg)) return prefill_index_score(*cfg, v, idx_q, idx_k_pages, block_scores, s);
   const bool d128 = cfg->index_dim == 128;
   switch (cfg->q_len) {
     case 1: return d128 ? launch<128, 1>(*cfg, v, idx_q, idx_k_pages, block_scores, s)

@@ -36,9 +36,24 @@ inline int32_t max_tokens_of(const msa_config& c) {
 
 int32_t blocks_per_split_of(const msa_config& c);  // resolves the 0 = auto case
 
+inline bool is_prefill(const msa_config& c) { return c.mode == MSA_MODE_PREFILL; }
+
+// Partials per (token, query head): split-K splits in decode mode, one per
+// selected slot in prefill mode.
 inline int32_t splits_of(const msa_config& c) {
-  int32_t S = width_of(c), b = blocks_per_split_of(c);
+  int32_t S = width_of(c);
+  if (is_prefill(c)) return S > 0 ? S : 1;
+  int32_t b = blocks_per_split_of(c);
   return S <= 0 ? 1 : (S + b - 1) / b;
+}
+
+// Bytes of one partial-output element: fp32 (decode), fp16 (prefill, where
+// the per-slot partials dominate the traffic).
+inline size_t part_elem_bytes(const msa_config& c) { return is_prefill(c) ? 2 : 4; }
+
+// CSR rows of the key-block -> query map: (KV head, request, block) grid.
+inline int64_t csr_rows_of(const msa_config& c) {
+  return (int64_t)c.num_kv_heads * c.max_batch * c.max_blocks_per_req;
 }
 
 // Byte offsets of every workspace region.
@@ -59,7 +74,7 @@ inline WsLayout layout_of(const msa_config& c) {
   L.tok_req = o;     o = align_up(o + 4 * T);
   L.tok_pos = o;     o = align_up(o + 4 * T);
   L.block_table = o; o = align_up(o + 4 * B * (size_t)c.max_blocks_per_req);
-  L.o_part = o;      o = align_up(o + 4 * T * Hq * NS * kHeadDim);
+  L.o_part = o;      o = align_up(o + part_elem_bytes(c) * T * Hq * NS * kHeadDim);
   L.lse_part = o;    o = align_up(o + 4 * T * Hq * NS);
   L.total = o;
   return L;
@@ -75,7 +90,7 @@ struct WsView {
   int32_t* tok_req;
   int32_t* tok_pos;
   int32_t* block_table;   // [max_batch, max_blocks_per_req], -1 = invalid
-  float* o_part;          // [T, H_q, NS, D]
+  void* o_part;           // [T, H_q, NS, D] fp32 (decode) | fp16 (prefill)
   float* lse_part;        // [T, H_q, NS]
 };
 
@@ -91,12 +106,15 @@ inline WsView view_of(const msa_config& c, const void* ws) {
   v.tok_req = (int32_t*)(b + L.tok_req);
   v.tok_pos = (int32_t*)(b + L.tok_pos);
   v.block_table = (int32_t*)(b + L.block_table);
-  v.o_part = (float*)(b + L.o_part);
+  v.o_part = (void*)(b + L.o_part);
   v.lse_part = (float*)(b + L.lse_part);
   return v;
 }
 
 msa_status check_config(const msa_config* c);
+// Index scores of a prefill chunk (tensor-core tiles; prefill.cu).
+msa_status prefill_index_score(const msa_config& c, const WsView& v, const void* idx_q,
+                               const void* idx_k, float* scores, cudaStream_t s);
 int sm_count();  // SMs of the current device (cached per device)
 
 // Launch-status helper: any launch error becomes MSA_ERR_CUDA.

@@ -42,6 +42,10 @@ msa_status check_config(const msa_config* c) {
   if (c->head_dim != kHeadDim || c->block_size != kBlock) return MSA_ERR_UNSUPPORTED;
   if (c->index_dim != 64 && c->index_dim != 128) return MSA_ERR_UNSUPPORTED;
   if (c->num_q_heads / c->num_kv_heads > kMaxGroup) return MSA_ERR_UNSUPPORTED;
+  if (c->mode != MSA_MODE_DECODE && c->mode != MSA_MODE_PREFILL) return MSA_ERR_INVALID_ARG;
+  if (c->mode == MSA_MODE_PREFILL && (kMaxGroup % (c->num_q_heads / c->num_kv_heads)) != 0)
+    return MSA_ERR_UNSUPPORTED;
+  if (c->mode == MSA_MODE_PREFILL && c->max_q_tokens <= 0) return MSA_ERR_INVALID_ARG;
   if (c->max_blocks_per_req > kMaxBlocksPerReq || c->max_batch > kMaxBatch)
     return MSA_ERR_UNSUPPORTED;
   if ((int64_t)max_tokens_of(*c) * c->num_q_heads > (int64_t)1 << 30) return MSA_ERR_UNSUPPORTED;
@@ -204,6 +208,7 @@ static msa_status plan_common(const msa_config* cfg, int32_t batch, const int32_
   if (batch > 0 && bt == nullptr && (r2t == nullptr || pool_idx == nullptr))
     return MSA_ERR_INVALID_ARG;
   if (bt != nullptr && bt_stride < cfg->max_blocks_per_req) return MSA_ERR_INVALID_ARG;
+  if (cfg->mode == MSA_MODE_PREFILL && batch > 0 && cu_q == nullptr) return MSA_ERR_INVALID_ARG;
   if (r2t != nullptr && r2t_stride < cfg->max_blocks_per_req * kBlock) return MSA_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), s) != cudaSuccess) return MSA_ERR_CUDA;

@@ -18,6 +18,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsa.so"
 _lib = None
 
 MSA_KV_BF16, MSA_KV_FP8_E4M3 = 0, 1
+MSA_MODE_DECODE, MSA_MODE_PREFILL = 0, 1
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED",
           3: "MSA_ERR_CUDA", 4: "MSA_ERR_DEVICE_FLAG"}
 DEVERR_BITS = {1: "PAGE_RANGE", 2: "SEQ_LEN", 4: "SLOT_ALIGN"}
@@ -41,6 +42,7 @@ class MsaConfig(ctypes.Structure):
         ("v_scale", ctypes.c_float), ("max_batch", ctypes.c_int32),
         ("max_q_tokens", ctypes.c_int32), ("max_blocks_per_req", ctypes.c_int32),
         ("num_pages", ctypes.c_int32), ("blocks_per_split", ctypes.c_int32),
+        ("mode", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -65,6 +67,10 @@ _SIGNATURES = {
     "msa_check_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "msa_sparse_decode_noalloc": (ctypes.c_int, [_CFG, ctypes.c_int32, _P, _P, ctypes.c_int32,
                                                  _P, _P, _P, _P, _P, _P, _P]),
+    "msa_k2q_rows": (ctypes.c_int64, [_CFG]),
+    "msa_k2q_capacity": (ctypes.c_int64, [_CFG]),
+    "msa_build_k2q_csr": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
+    "msa_sparse_prefill": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -128,7 +134,7 @@ def make_config(*, num_q_heads, num_kv_heads, init_blocks, local_blocks, topk_bl
                 index_dim, max_batch, max_blocks_per_req, num_pages, q_len=1,
                 kv_dtype="bf16", softmax_scale=None, k_scale=1.0, v_scale=1.0,
                 max_q_tokens=0, blocks_per_split=0, head_dim=128,
-                block_size=128) -> MsaConfig:
+                block_size=128, mode="decode") -> MsaConfig:
     c = MsaConfig()
     c.num_q_heads, c.num_kv_heads = num_q_heads, num_kv_heads
     c.head_dim, c.block_size = head_dim, block_size
@@ -140,17 +146,22 @@ def make_config(*, num_q_heads, num_kv_heads, init_blocks, local_blocks, topk_bl
     c.max_batch, c.max_q_tokens = max_batch, max_q_tokens
     c.max_blocks_per_req, c.num_pages = max_blocks_per_req, num_pages
     c.blocks_per_split = blocks_per_split
+    c.mode = {"decode": MSA_MODE_DECODE, "prefill": MSA_MODE_PREFILL}[mode]
     return c
 
 
 def config_for(spec, **overrides) -> MsaConfig:
-    """Config of a WorkloadSpec (block counts resolved here, by the library)."""
+    """Config of a WorkloadSpec (block counts resolved here, by the library).
+    Chunks of more than 4 query tokens per request run in prefill mode."""
+    prefill = spec.q_len > 4
     kw = dict(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
               init_blocks=spec.init_blocks,
               local_blocks=local_blocks_from_tokens(spec.local_tokens, spec.block_size),
               topk_blocks=spec.topk_blocks, index_dim=spec.index_dim,
               max_batch=spec.batch, max_blocks_per_req=spec.max_blocks,
-              num_pages=spec.num_pages, q_len=spec.q_len, kv_dtype=spec.kv_dtype,
+              num_pages=spec.num_pages, q_len=1 if prefill else spec.q_len,
+              kv_dtype=spec.kv_dtype, mode="prefill" if prefill else "decode",
+              max_q_tokens=spec.batch * spec.q_len if prefill else 0,
               softmax_scale=spec.softmax_scale, k_scale=spec.kv_scale,
               v_scale=spec.kv_scale, head_dim=spec.head_dim, block_size=spec.block_size)
     kw.update(overrides)
@@ -241,6 +252,37 @@ def combine(cfg, ws, out, lse, stream=None):
                                             _stream(stream)))
 
 
+def k2q_rows(cfg) -> int:
+    return lib().msa_k2q_rows(ctypes.byref(cfg))
+
+
+def k2q_capacity(cfg) -> int:
+    return lib().msa_k2q_capacity(ctypes.byref(cfg))
+
+
+def build_k2q_csr(cfg, ws, selected, row_ptr, q_indices, stream=None):
+    _need(selected, "selected", torch.int32, 3)
+    _need(row_ptr, "row_ptr", torch.int32, 1)
+    _need(q_indices, "q_indices", torch.int32, 1)
+    if row_ptr.numel() < k2q_rows(cfg) + 1 or q_indices.numel() < k2q_capacity(cfg):
+        raise ValueError("row_ptr / q_indices smaller than msa_k2q_rows + 1 / msa_k2q_capacity")
+    _check("msa_build_k2q_csr", lib().msa_build_k2q_csr(
+        ctypes.byref(cfg), _ptr(ws), _ptr(selected), _ptr(row_ptr), _ptr(q_indices),
+        _stream(stream)))
+
+
+def sparse_prefill(cfg, ws, q, k_pages, v_pages, selected, row_ptr, q_indices, stream=None):
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(selected, "selected", torch.int32, 3)
+    _need(row_ptr, "row_ptr", torch.int32, 1)
+    _need(q_indices, "q_indices", torch.int32, 1)
+    _check("msa_sparse_prefill", lib().msa_sparse_prefill(
+        ctypes.byref(cfg), _ptr(ws), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(selected),
+        _ptr(row_ptr), _ptr(q_indices), _stream(stream)))
+
+
 def check_device_error(ws, stream=None) -> int:
     """Synchronises the stream; returns the device error bits (0 = none)."""
     flags = ctypes.c_int32(0)
@@ -269,14 +311,26 @@ class SparseAttention:
         self.out = torch.empty((T, cfg.num_q_heads, cfg.head_dim), dtype=torch.bfloat16,
                                device=device)
         self.lse = torch.empty((T, cfg.num_q_heads), dtype=torch.float32, device=device)
+        self.prefill = cfg.mode == MSA_MODE_PREFILL
+        if self.prefill:
+            self.row_ptr = torch.empty(k2q_rows(cfg) + 1, dtype=torch.int32, device=device)
+            self.q_indices = torch.empty(k2q_capacity(cfg), dtype=torch.int32, device=device)
 
     def run(self, seq_lens, block_table, idx_q, idx_k_pages, q, k_pages, v_pages,
             cu_seqlens_q=None, stream=None):
+        """Decode / verify: plan, index score, top-k, split-K decode, combine.
+        Prefill (cu_seqlens_q required): plan, index score, top-k, CSR,
+        sparse prefill tiles, combine."""
         c = self.cfg
         plan(c, seq_lens, block_table, self.ws, cu_seqlens_q, stream)
         index_score(c, self.ws, idx_q, idx_k_pages, self.block_scores, stream)
         topk_select(c, self.ws, self.block_scores, self.selected, stream)
-        sparse_decode(c, self.ws, q, k_pages, v_pages, self.selected, stream)
+        if self.prefill:
+            build_k2q_csr(c, self.ws, self.selected, self.row_ptr, self.q_indices, stream)
+            sparse_prefill(c, self.ws, q, k_pages, v_pages, self.selected, self.row_ptr,
+                           self.q_indices, stream)
+        else:
+            sparse_decode(c, self.ws, q, k_pages, v_pages, self.selected, stream)
         combine(c, self.ws, self.out, self.lse, stream)
         return self.out, self.lse
 

@@ -73,6 +73,14 @@ typedef enum msa_kv_dtype {
   MSA_KV_FP8_E4M3 = 1        /* e4m3 "fn" codes; value = decode(code) * scale */
 } msa_kv_dtype;
 
+typedef enum msa_mode {
+  MSA_MODE_DECODE = 0,       /* q_len new tokens per request (1 = decode, 2..4 =
+                                speculative verify); msa_sparse_decode          */
+  MSA_MODE_PREFILL = 1       /* a chunk of any length per request, given by
+                                cu_seqlens_q; msa_build_k2q_csr +
+                                msa_sparse_prefill; H_q / H_kv must divide 16     */
+} msa_mode;
+
 /* Bits of the device error word (msa_check_device_error). */
 enum {
   MSA_DEVERR_PAGE_RANGE = 1,   /* block table / req_to_token page outside the pool */
@@ -110,6 +118,7 @@ typedef struct msa_config {
   int32_t max_blocks_per_req; /* block-table width used; seq_len <= this * P     */
   int32_t num_pages;          /* pages in the KV / index-K pool                  */
   int32_t blocks_per_split;   /* selected blocks per split-K work item; 0 = auto */
+  int32_t mode;               /* msa_mode: decode / verify, or chunked prefill   */
 } msa_config;
 
 /* Human-readable name of a status (static string). */
@@ -174,7 +183,9 @@ msa_status msa_plan_from_req_to_token(const msa_config* cfg, int32_t batch,
  *                             position(u) <= position(t) of  idx_q[t,h,:] . idx_k[u,h,:]
  * accumulated in fp32 (exact for the integer-valued index vectors used in
  * tests).  Entries j >= the token's visible block count are not written.
- * Bandwidth-bound: reads every visible index key once per request.
+ * Decode mode: bandwidth-bound, every visible index key read once per request
+ * (q_len <= 4 queries share each load).  Prefill mode: tensor-core tiles of
+ * 64 query tokens x one 128-key block, causal.
  */
 msa_status msa_index_score(const msa_config* cfg, const void* ws, const void* idx_q,
                            const void* idx_k_pages, float* block_scores,
@@ -213,6 +224,37 @@ msa_status msa_sparse_decode(const msa_config* cfg, void* ws, const void* q,
  */
 msa_status msa_combine(const msa_config* cfg, const void* ws, void* out, float* lse,
                        msa_stream_t stream);
+
+/*
+ * Key-block -> query CSR for prefill (vLLM MiniMaxM3SparseMSAImpl.forward calls
+ * build_k2q_csr on the [H, tokens, MK] selections with qhead_per_kv).  Rows
+ * sit on the fixed grid row = (h * max_batch + r) * max_blocks_per_req + j
+ * (KV head h, request r, key block j), so every size depends on cfg alone;
+ * rows of absent requests / blocks are empty.
+ *   msa_k2q_rows(cfg)      number of rows (row_ptr holds rows + 1 int32)
+ *   msa_k2q_capacity(cfg)  an upper bound of the entries (q_indices length)
+ * msa_build_k2q_csr (prefill mode only) fills row_ptr (prefix sums, row_ptr[0]
+ * = 0) and q_indices: row (h, r, j) lists, ascending, the token indices t of
+ * request r whose selected[t, h, :] contains j.  Deterministic.
+ */
+int64_t msa_k2q_rows(const msa_config* cfg);
+int64_t msa_k2q_capacity(const msa_config* cfg);
+msa_status msa_build_k2q_csr(const msa_config* cfg, const void* ws, const int32_t* selected,
+                             int32_t* row_ptr, int32_t* q_indices, msa_stream_t stream);
+
+/*
+ * msa_sparse_prefill -- block-sparse causal attention for a prefill chunk
+ * (vLLM MiniMaxM3SparseMSAImpl.forward: sparse_atten_func with blk_kv = 128,
+ * causal = True, page_table and the CSR).  One tile per CSR row: the row's
+ * tokens x their GQA query heads against the block's 128 keys, causal inside
+ * the block that holds the token.  Writes one normalised fp16 partial and its
+ * LSE per (token, query head, selected slot) into ws; msa_combine merges them
+ * into out / lse.  Prefill mode, bf16 KV only (fp8 -> MSA_ERR_UNSUPPORTED).
+ */
+msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const void* q,
+                              const void* k_pages, const void* v_pages,
+                              const int32_t* selected, const int32_t* row_ptr,
+                              const int32_t* q_indices, msa_stream_t stream);
 
 /*
  * msa_sparse_decode_noalloc -- msa_plan + msa_sparse_decode + msa_combine in

@@ -18,7 +18,7 @@ def run_gpu(w: wl.Workload, **cfg_overrides):
     cfg = msa.config_for(w.spec, **cfg_overrides)
     sa = msa.SparseAttention(cfg, device=w.q.device)
     sa.run(w.seq_lens, w.block_table, w.idx_q, w.idx_k_pages, w.q, w.k_pages, w.v_pages,
-           cu_seqlens_q=None if w.spec.q_len > 0 else w.cu_seqlens_q)
+           cu_seqlens_q=w.cu_seqlens_q if sa.prefill else None)
     torch.cuda.synchronize()
     return sa
 

@@ -1,0 +1,117 @@
+"""Chunked prefill: CUDA path vs the fp64 oracle (GPU).
+
+Per-token block scores and selections bit-exact; the key-block -> query CSR
+identical to the oracle's (built from the same selections); out / lse within
+the parity bounds.  Small chunks are compared on every element; the full-size
+prefill (4 requests x (16384 cached + 2048 new) tokens) on sampled pairs plus
+structural CSR properties over every row."""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_paged_msa_gb300 as msa
+import oracle
+from block_sparse_paged_msa_gb300 import workloads as wl
+from gpu_util import compare, compare_sampled, run_gpu
+from oracle_io import run_oracle, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _csr_matches_oracle(w, sa):
+    spec = w.spec
+    T = w.num_tokens
+    sel = sa.selected[:T].cpu().numpy().astype(np.int64)
+    tok_req = np.repeat(np.arange(spec.batch), w.q_lens.cpu().numpy())
+    rp, qi = oracle.build_k2q_csr(sel, tok_req, spec.batch, spec.max_blocks)
+    got_rp = sa.row_ptr.cpu().numpy().astype(np.int64)
+    assert np.array_equal(got_rp, rp)
+    assert np.array_equal(sa.q_indices[:len(qi)].cpu().numpy().astype(np.int64), qi)
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(num_q_heads=32, num_kv_heads=2),
+                                dict(num_q_heads=16, num_kv_heads=4, index_dim=64),
+                                dict(seq_lens=(700, 129), q_len=129, topk_blocks=2)],
+                         ids=["g8", "g16", "g4_d64", "chunk129_topk2"])
+def test_small_prefill_every_element(kw):
+    spec = wl.small("prefill", **kw)
+    w = wl.make_workload(spec, device="cuda")
+    sa = run_gpu(w)
+    assert sa.prefill
+    assert msa.check_device_error(sa.ws) == 0
+    print(compare(w, sa, run_oracle(w.to("cpu"))))
+    _csr_matches_oracle(w, sa)
+
+
+def test_prefill_whole_sequence_is_dense_causal():
+    """A chunk that is the whole sequence with top-k covering every block is
+    plain causal attention."""
+    spec = wl.small("prefill", seq_lens=(600,), q_len=600, batch=1, topk_blocks=16,
+                    num_pages=8)
+    w = wl.make_workload(spec, device="cuda")
+    sa = run_gpu(w)
+    ref = run_oracle(w.to("cpu"))
+    compare(w, sa, ref)
+    for (t, h), s in ref["selected"].items():
+        assert s == list(range(t // 128 + 1))
+
+
+def test_prefill_full_size_sampled():
+    spec = wl.WORKLOADS["prefill"]
+    w = wl.make_workload(spec, device="cuda")
+    sa = run_gpu(w)
+    assert msa.check_device_error(sa.ws) == 0
+    samples = [(0, 0), (2047, 7), (2048, 3), (4100, 1), (6000, 5), (8191, 2)]
+    print(compare_sampled(w, sa, samples))
+    # CSR structure over every row: sizes add up to the selections, each row
+    # ascending and inside its request, every entry's selection holds the block
+    T = w.num_tokens
+    sel = sa.selected[:T]
+    rp = sa.row_ptr.long()
+    total = int(rp[-1])
+    assert total == int((sel >= 0).sum())
+    assert bool((rp[1:] >= rp[:-1]).all())
+    qi = sa.q_indices[:total].long()
+    rows = torch.repeat_interleave(torch.arange(rp.numel() - 1, device="cuda"), rp[1:] - rp[:-1])
+    NB, B = spec.max_blocks, spec.batch
+    j = rows % NB
+    r = (rows // NB) % B
+    h = rows // (NB * B)
+    assert bool((qi // spec.q_len == r).all())
+    same_row = rows[1:] == rows[:-1]
+    assert bool((qi[1:][same_row] > qi[:-1][same_row]).all())
+    assert bool((sel[qi, h] == j[:, None]).any(-1).all())
+    assert torch.isfinite(sa.out[:T].float()).all()
+
+
+def test_prefill_graph_replay_equals_eager():
+    base = wl.small("prefill")
+    w = wl.make_workload(base, device="cuda")
+    cfg = msa.config_for(base)
+    sa = msa.SparseAttention(cfg)
+    bufs = {k: v.clone() for k, v in w.__dict__.items() if isinstance(v, torch.Tensor)}
+    args = lambda: (bufs["seq_lens"], bufs["block_table"], bufs["idx_q"], bufs["idx_k_pages"],
+                    bufs["q"], bufs["k_pages"], bufs["v_pages"])
+    sa.run(*args(), cu_seqlens_q=bufs["cu_seqlens_q"])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            sa.run(*args(), cu_seqlens_q=bufs["cu_seqlens_q"])
+    torch.cuda.current_stream().wait_stream(s)
+    for seed in (201, 202):
+        w2 = wl.make_workload(base.replace(seed=seed), device="cuda")
+        for k, v in bufs.items():
+            v.copy_(getattr(w2, k))
+        graph.replay()
+        torch.cuda.synchronize()
+        g_out, g_lse, g_rp = sa.out.clone(), sa.lse.clone(), sa.row_ptr.clone()
+        eager = msa.SparseAttention(cfg)
+        eager.run(w2.seq_lens, w2.block_table, w2.idx_q, w2.idx_k_pages, w2.q, w2.k_pages,
+                  w2.v_pages, cu_seqlens_q=w2.cu_seqlens_q)
+        torch.cuda.synchronize()
+        T = w2.num_tokens
+        assert torch.equal(g_rp, eager.row_ptr)
+        assert torch.equal(g_out[:T], eager.out[:T]) and torch.equal(g_lse[:T], eager.lse[:T])
