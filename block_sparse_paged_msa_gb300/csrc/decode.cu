@@ -9,22 +9,28 @@
 // the query, the K/V cache and the per-request page table to the same op.
 //
 // Work item = (query token t, KV head h, split s); a split is a run of
-// consecutive slots of t's selected list.  One 128-thread CTA per item:
-//  * the G = H_q / H_kv query heads of h form the M side of an m16n8k16 bf16
-//    MMA (rows >= G are zero), the group shares every K/V tile it loads;
-//  * each selected block contributes a 32 KiB K tile and a 32 KiB V tile
-//    ([128 tokens][128 dims], contiguous per page and head in the HND pool),
-//    staged through a 3-deep ring of shared-memory tiles with 16-byte
-//    cp.async copies (XOR-swizzled 16-byte chunks so that ldmatrix reads are
-//    conflict-free; rows past the last visible token are zero-filled, never
-//    read);
-//  * warp w owns tokens [32w, 32w+32) of every tile and keeps its own online
-//    softmax state; the four states are merged once at the end of the item;
-//  * fp8-e4m3 tiles (16 KiB) are converted to bf16 in shared memory (e4m3 is
-//    exact in bf16); k_scale is folded into the softmax scale and v_scale into
-//    the output.
-// The partial output (normalised) and its natural-log LSE go to the workspace;
-// msa_combine merges them in a fixed order (deterministic).
+// consecutive slots of t's selected list.  Design (GB300):
+//  * a persistent grid (two 160-thread CTAs per SM) strides over the work
+//    items; in each CTA one producer warp streams, for every selected block,
+//    the block's K tile and V tile ([128 tokens][128 dims], contiguous per page
+//    and KV head in the HND pool: 32 KiB bf16, 16 KiB e4m3) with 2-D TMA loads
+//    (128-byte swizzle) into a ring of shared-memory stages guarded by
+//    mbarriers -- so the copies of the next items are already in flight while
+//    the current one is being finished;
+//  * four consumer warps share every tile: warp w owns tokens [32w, 32w+32),
+//    runs S = Q K^T and O += P V on m16n8k16 tensor-core MMAs with the G =
+//    H_q / H_kv query heads of the group as the M side (rows >= G are zero),
+//    and keeps its own online softmax (exp2 domain); the four states merge once
+//    per item and warp 0 writes the normalised partial and its LSE;
+//  * rows past the last visible token are masked in S and cleared in V before
+//    P V (whatever they hold, 0 * NaN would not vanish);
+//  * e4m3 tiles: K feeds an fp16 MMA straight from shared memory (the index
+//    dimension is permuted so a thread's four K values of a k-step are one
+//    32-bit load), V is converted to fp16 rows by its warp; e4m3 is exact in
+//    fp16, k_scale folds into the softmax scale and v_scale into the output.
+// msa_combine then merges the splits in a fixed order (deterministic).
+#include <cuda.h>
+
 #include <mutex>
 
 #include "msa_device.cuh"
@@ -32,166 +38,239 @@
 namespace msa {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kStages = 3;
+constexpr int kConsumers = 4;                      // consumer warps
+constexpr int kThreads = (kConsumers + 1) * 32;    // + one producer warp
+constexpr int kStages = 3;                         // ring depth (tiles)
 constexpr int kTileBytes = kBlock * kHeadDim * 2;  // bf16 tile, 32 KiB
+constexpr int kFp8Stages = 4;                      // fp8 tiles are 16 KiB
+constexpr int kFp8TileBytes = kBlock * kHeadDim;
+constexpr int kConvBytes = 32 * 256;               // per consumer warp: 32 rows, f16
 
 struct DecodeArgs {
-  int Hkv, Hq, G, S, bps, nsplit, max_blocks;
+  int Hkv, Hq, G, S, bps, nsplit, max_blocks, n_items;
   float scale_log2;     // softmax_scale * k_scale * log2(e)
   float v_scale;
   const __nv_bfloat16* q;
-  const uint8_t* k;     // bf16 or e4m3 pool
-  const uint8_t* v;
   const int32_t* selected;
 };
 
-// Issue the copy of one K or V tile (block slot i, kind 0 = K, 1 = V) into ring
-// buffer `buf`.  bf16: 2048 16-byte chunks, swizzled.  fp8: 1024 raw chunks.
-template <bool FP8>
-__device__ __forceinline__ void issue_tile(const DecodeArgs& a, uint8_t* ring, int buf,
-                                           int page, int h, int ntok, int kind) {
-  const uint8_t* pool = kind == 0 ? a.k : a.v;
-  constexpr int kRowBytes = FP8 ? 128 : 256;
-  constexpr int kChunksPerRow = kRowBytes / 16;
-  const uint8_t* src = pool + ((int64_t)page * a.Hkv + h) * (int64_t)kBlock * kRowBytes;
-  uint8_t* dst = ring + buf * kTileBytes;
-  const uint32_t dst_s = smem_u32(dst);
-#pragma unroll
-  for (int k = 0; k < kBlock * kChunksPerRow / kThreads; ++k) {
-    const int idx = k * kThreads + threadIdx.x;
-    const int row = idx / kChunksPerRow, c = idx % kChunksPerRow;
-    const int bytes = row < ntok ? 16 : 0;                // zero-fill past the end
-    const uint8_t* g = src + (row < ntok ? row * kRowBytes + c * 16 : 0);
-    const uint32_t off = FP8 ? (uint32_t)(row * kRowBytes + c * 16) : swz(row, c);
-    cp_async16(dst_s + off, g, bytes);
-  }
-}
+// The blocks of work item (t, h, split s), as a lane-distributed list: lane i
+// (< bps) holds slot s*bps + i; `mask` has a bit for every usable slot (a valid,
+// visible block whose page passed the plan's check).  Producer and consumers
+// derive it identically.
+struct ItemBlocks {
+  unsigned mask;
+  int page, ntok;     // this lane's slot
+};
 
-// fp8: convert the raw tile at the start of ring buffer `buf` into the bf16
-// swizzled tile `conv`.
-__device__ __forceinline__ void convert_tile(const uint8_t* raw, uint8_t* conv) {
-#pragma unroll
-  for (int k = 0; k < (kBlock * 8) / kThreads; ++k) {       // 1024 raw chunks
-    const int idx = k * kThreads + threadIdx.x;
-    const int row = idx >> 3, c = idx & 7;
-    const uint4 w = *reinterpret_cast<const uint4*>(raw + row * 128 + c * 16);
-    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
-    uint32_t o[8];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      o[2 * e] = e4m3x2_to_bf16x2((uint16_t)(in[e] & 0xffffu));
-      o[2 * e + 1] = e4m3x2_to_bf16x2((uint16_t)(in[e] >> 16));
+__device__ __forceinline__ ItemBlocks item_blocks(const WsView& ws, const DecodeArgs& a, int t,
+                                                  int h, int s, int r, int pos, int lane) {
+  ItemBlocks b;
+  const int slot0 = s * a.bps;
+  const int nslot = min(a.bps, a.S - slot0);
+  b.page = -1;
+  b.ntok = 0;
+  if (lane < nslot) {
+    const int j = a.selected[((int64_t)t * a.Hkv + h) * a.S + slot0 + lane];
+    if (j >= 0 && j * kBlock <= pos) {
+      b.page = ws.block_table[(int64_t)r * a.max_blocks + j];
+      b.ntok = min(kBlock, pos + 1 - j * kBlock);
     }
-    *reinterpret_cast<uint4*>(conv + swz(row, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<uint4*>(conv + swz(row, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
   }
+  b.mask = __ballot_sync(0xffffffffu, b.page >= 0);
+  return b;
 }
 
-template <bool FP8>
-__global__ void __launch_bounds__(kThreads)
-decode_kernel(WsView ws, DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;                                     // kStages tiles
-  uint8_t* conv = smem + kStages * kTileBytes;              // fp8: bf16 staging tile
-  __shared__ int blk_page[64], blk_ntok[64];
-  __shared__ int n_blk_s;
-  __shared__ float red_m[4][16], red_l[4][16];
+struct Item {
+  int t, h, s, r, pos;
+  bool active;
+};
 
-  const int item = blockIdx.x;
-  const int s = item % a.nsplit;
-  const int h = (item / a.nsplit) % a.Hkv;
-  const int t = item / (a.nsplit * a.Hkv);
-  if (t >= ws.hdr->num_tokens) return;
-  const int r = ws.tok_req[t];
-  if (r < 0) return;                                        // combine writes 0 / -inf
-  const int pos = ws.tok_pos[t];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, tq = lane & 3;
+__device__ __forceinline__ Item item_of(const WsView& ws, const DecodeArgs& a, int idx) {
+  Item it;
+  it.s = idx % a.nsplit;
+  it.h = (idx / a.nsplit) % a.Hkv;
+  it.t = idx / (a.nsplit * a.Hkv);
+  it.active = it.t < ws.hdr->num_tokens;
+  it.r = it.active ? ws.tok_req[it.t] : -1;
+  it.active = it.active && it.r >= 0;
+  it.pos = it.active ? ws.tok_pos[it.t] : -1;
+  return it;
+}
 
-  // ---- the split's blocks: (page, visible rows), invalid slots dropped
-  if (tid < 32) {
-    const int slot0 = s * a.bps;
-    const int nslot = min(a.bps, a.S - slot0);
-    int page = -1, ntok = 0;
-    if (lane < nslot) {
-      const int j = a.selected[((int64_t)t * a.Hkv + h) * a.S + slot0 + lane];
-      if (j >= 0 && j * kBlock <= pos) {
-        page = ws.block_table[(int64_t)r * a.max_blocks + j];
-        ntok = min(kBlock, pos + 1 - j * kBlock);
+// fp8: the warp converts its 32 rows of an e4m3 V tile (TMA 128-byte swizzle)
+// to f16 rows in its private staging area (256-byte swizzled rows), zeroing
+// rows past the last visible token.
+__device__ __forceinline__ void convert_v_rows(const uint8_t* tile, uint8_t* conv, int warp,
+                                               int ntok, int lane) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int idx = k * 32 + lane;            // 32 rows x 8 chunks of 16 e4m3
+    const int rl = idx >> 3, c = idx & 7;
+    const int row = warp * 32 + rl;
+    uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (row < ntok) {
+      const uint4 w = *reinterpret_cast<const uint4*>(tile + swz128(row, c));
+      const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        o[2 * e] = e4m3x2_to_f16x2((uint16_t)(in[e] & 0xffffu));
+        o[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(in[e] >> 16));
       }
     }
-    const bool ok = page >= 0 && lane < nslot;
-    const unsigned bal = __ballot_sync(0xffffffffu, ok);
-    if (ok) {
-      const int p = __popc(bal & ((1u << lane) - 1u));
-      blk_page[p] = page;
-      blk_ntok[p] = ntok;
-    }
-    if (lane == 0) n_blk_s = __popc(bal);
+    *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
   }
-  // ---- Q fragments (rows = query heads of the group, zero past G)
-  uint32_t qa[8][4];
-  {
-    const __nv_bfloat16* qb = a.q + ((int64_t)t * a.Hq + (int64_t)h * a.G) * kHeadDim;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int c0 = ks * 16 + 2 * tq, c1 = c0 + 8;
-      qa[ks][0] = g < a.G ? *reinterpret_cast<const uint32_t*>(qb + g * kHeadDim + c0) : 0u;
-      qa[ks][1] = g + 8 < a.G ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * kHeadDim + c0) : 0u;
-      qa[ks][2] = g < a.G ? *reinterpret_cast<const uint32_t*>(qb + g * kHeadDim + c1) : 0u;
-      qa[ks][3] = g + 8 < a.G ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * kHeadDim + c1) : 0u;
+}
+
+// Persistent split-K decode.  Warp 4 produces: for every block of every work
+// item of this CTA it waits for a free ring slot and issues the K and the V
+// tile as 2-D TMA loads.  Warps 0-3 consume: warp w owns tokens [32w, 32w+32)
+// of every tile, runs S = Q K^T and P V on m16n8k16 tensor-core MMAs with its
+// own online softmax, and the four states merge once per work item.
+template <bool FP8>
+__global__ void __launch_bounds__(kThreads, 2)
+decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
+              const __grid_constant__ CUtensorMap tmap_v) {
+  constexpr int NST = FP8 ? kFp8Stages : kStages;
+  constexpr int TB = FP8 ? kFp8TileBytes : kTileBytes;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* ring = smem;                                      // NST x TB, 1 KiB aligned
+  uint8_t* conv = smem + NST * TB;                           // fp8: 4 x 8 KiB
+  float* merge = reinterpret_cast<float*>(conv + (FP8 ? kConsumers * kConvBytes : 0));
+  __shared__ __align__(8) uint64_t full_bar[NST], empty_bar[NST];
+  __shared__ float red_m[kConsumers][16], red_l[kConsumers][16];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], kConsumers);
     }
+    fence_barrier_init();
   }
   __syncthreads();
-  const int nblk = n_blk_s;
-  const int ntiles = 2 * nblk;   // K0 V0 K1 V1 ...
 
-  float acc[16][4];
+  if (warp == kConsumers) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int idx = blockIdx.x; idx < a.n_items; idx += gridDim.x) {
+      const Item it = item_of(ws, a, idx);
+      if (!it.active) continue;
+      ItemBlocks bl = item_blocks(ws, a, it.t, it.h, it.s, it.r, it.pos, lane);
+      unsigned m = bl.mask;
+      while (m) {
+        const int L = __ffs(m) - 1;
+        m &= m - 1;
+        const int page = __shfl_sync(0xffffffffu, bl.page, L);
+        const int y = (page * a.Hkv + it.h) * kBlock;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  float m_r[2] = {-INFINITY, -INFINITY};   // running max (log2 domain), rows g, g+8
-  float l_r[2] = {0.f, 0.f};               // per-thread partial row sums
-  uint32_t pa[2][4];                        // P as bf16 A fragments (2 k-steps)
-
-  // ---- prologue
-#pragma unroll
-  for (int x = 0; x < kStages - 1; ++x) {
-    if (x < ntiles) issue_tile<FP8>(a, ring, x, blk_page[x >> 1], h, blk_ntok[x >> 1], x & 1);
-    cp_async_commit();
+        for (int kind = 0; kind < 2; ++kind) {
+          if (lane == 0) {
+            mbar_wait(&empty_bar[stage], phase ^ 1u, ws.hdr);
+            mbar_arrive_expect_tx(&full_bar[stage], TB);
+            const void* tm = kind == 0 ? (const void*)&tmap_k : (const void*)&tmap_v;
+            uint8_t* dst = ring + stage * TB;
+            if (FP8) {
+              tma_load_2d(dst, tm, 0, y, &full_bar[stage]);
+            } else {
+              tma_load_2d(dst, tm, 0, y, &full_bar[stage]);
+              tma_load_2d(dst + TB / 2, tm, 64, y, &full_bar[stage]);
+            }
+          }
+          __syncwarp();
+          if (++stage == NST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    // No drain needed: the consumers wait for every tile issued here before
+    // they finish, so no copy is in flight when the CTA retires.
+    return;
   }
-  for (int x = 0; x < ntiles; ++x) {
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, tq = lane & 3;
+  int stage = 0;
+  uint32_t phase = 0;
+  uint8_t* my_conv = conv + warp * kConvBytes;
+  for (int idx = blockIdx.x; idx < a.n_items; idx += gridDim.x) {
+    const Item it = item_of(ws, a, idx);
+    if (!it.active) continue;
+    const ItemBlocks bl = item_blocks(ws, a, it.t, it.h, it.s, it.r, it.pos, lane);
+
+    // Q fragments: rows = the group's query heads (zero past G).  fp8: f16
+    // operands with the index dim permuted so that a thread's four K values of
+    // a k-step are one 32-bit shared load (d = 16ks + 4tq + {0,1 | 2,3}).
+    uint32_t qa[8][4];
     {
-      const int y = x + kStages - 1;
-      if (y < ntiles) issue_tile<FP8>(a, ring, y % kStages, blk_page[y >> 1], h, blk_ntok[y >> 1], y & 1);
-      cp_async_commit();
+      const __nv_bfloat16* qb = a.q + ((int64_t)it.t * a.Hq + (int64_t)it.h * a.G) * kHeadDim;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int row = g + 8 * hr;
+          const __nv_bfloat16* qr = qb + row * kHeadDim;
+          if (row >= a.G) {
+            qa[ks][hr] = qa[ks][hr + 2] = 0u;
+          } else if (FP8) {
+            const uint2 w = *reinterpret_cast<const uint2*>(qr + ks * 16 + 4 * tq);
+            qa[ks][hr] = bf16x2_to_f16x2(w.x);
+            qa[ks][hr + 2] = bf16x2_to_f16x2(w.y);
+          } else {
+            qa[ks][hr] = *reinterpret_cast<const uint32_t*>(qr + ks * 16 + 2 * tq);
+            qa[ks][hr + 2] = *reinterpret_cast<const uint32_t*>(qr + ks * 16 + 8 + 2 * tq);
+          }
+        }
+      }
     }
-    cp_async_wait<kStages - 1>();
-    __syncthreads();
-    const uint8_t* tile = ring + (x % kStages) * kTileBytes;
-    if (FP8) {
-      convert_tile(tile, conv);
-      __syncthreads();
-      tile = conv;
-    }
-    const uint32_t tile_s = smem_u32(tile);
-    const int ntok = blk_ntok[x >> 1];
-    if ((x & 1) == 0) {
-      // ---- S = Q K^T for this warp's 32 tokens (4 n-tiles of 8)
+    float acc[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float m_r[2] = {-INFINITY, -INFINITY};   // running max (log2 domain), rows g, g+8
+    float l_r[2] = {0.f, 0.f};
+
+    unsigned m = bl.mask;
+    while (m) {
+      const int L = __ffs(m) - 1;
+      m &= m - 1;
+      const int ntok = __shfl_sync(0xffffffffu, bl.ntok, L);
+      // ---------------- K tile: S = Q K^T for this warp's 32 tokens
+      mbar_wait(&full_bar[stage], phase, ws.hdr);
+      const uint8_t* kt = ring + stage * TB;
       float sc[4][4];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-        const int row = warp * 32 + nt * 8 + (lane & 7);
+        if (FP8) {
+          const int row = warp * 32 + nt * 8 + g;
 #pragma unroll
-        for (int ks = 0; ks < 8; ks += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(tile_s + swz(row, 2 * ks + (lane >> 3)), b0, b1, b2, b3);
-          mma_bf16(sc[nt], qa[ks], b0, b1);
-          mma_bf16(sc[nt], qa[ks + 1], b2, b3);
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t w =
+                *reinterpret_cast<const uint32_t*>(kt + swz128(row, ks) + 4 * tq);
+            mma_f16(sc[nt], qa[ks], e4m3x2_to_f16x2((uint16_t)(w & 0xffffu)),
+                    e4m3x2_to_f16x2((uint16_t)(w >> 16)));
+          }
+        } else {
+          const int row = warp * 32 + nt * 8 + (lane & 7);
+          const uint32_t kts = smem_u32(kt);
+#pragma unroll
+          for (int ks = 0; ks < 8; ks += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kts + swz_tma(row, 2 * ks + (lane >> 3)), b0, b1, b2, b3);
+            mma_bf16(sc[nt], qa[ks], b0, b1);
+            mma_bf16(sc[nt], qa[ks + 1], b2, b3);
+          }
         }
       }
-      // ---- online softmax (log2 domain), rows g (c0,c1) and g+8 (c2,c3)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[stage]);
+      if (++stage == NST) { stage = 0; phase ^= 1u; }
+
+      // ---------------- online softmax (log2 domain)
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
@@ -219,91 +298,138 @@ decode_kernel(WsView ws, DecodeArgs a) {
         acc[nd][0] *= alpha[0]; acc[nd][1] *= alpha[0];
         acc[nd][2] *= alpha[1]; acc[nd][3] *= alpha[1];
       }
+      uint32_t pa[2][4];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p = exp2f(sc[nt][e] - mref[e >> 1]);
-          sc[nt][e] = p;
-          l_r[e >> 1] += p;
+        const float p0 = exp2f(sc[nt][0] - mref[0]), p1 = exp2f(sc[nt][1] - mref[0]);
+        const float p2 = exp2f(sc[nt][2] - mref[1]), p3 = exp2f(sc[nt][3] - mref[1]);
+        if (FP8) {
+          const __half2 h01 = __floats2half2_rn(p0, p1), h23 = __floats2half2_rn(p2, p3);
+          const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+          l_r[0] += f01.x + f01.y;
+          l_r[1] += f23.x + f23.y;
+          pa[nt >> 1][(nt & 1) * 2] = *reinterpret_cast<const uint32_t*>(&h01);
+          pa[nt >> 1][(nt & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+        } else {
+          l_r[0] += p0 + p1;
+          l_r[1] += p2 + p3;
+          pa[nt >> 1][(nt & 1) * 2] = pack_bf16(p0, p1);
+          pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(p2, p3);
         }
       }
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        pa[kk][0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-        pa[kk][1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-        pa[kk][2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-        pa[kk][3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+
+      // ---------------- V tile: O += P V
+      mbar_wait(&full_bar[stage], phase, ws.hdr);
+      uint8_t* vt = ring + stage * TB;
+      uint32_t vbase;
+      int vrow0;
+      if (FP8) {
+        convert_v_rows(vt, my_conv, warp, ntok, lane);
+        __syncwarp();
+        vbase = smem_u32(my_conv);
+        vrow0 = 0;
+      } else {
+        if (ntok < warp * 32 + 32) {
+          // rows past the last visible token may hold anything; P is 0 there,
+          // but 0 * NaN is not, so clear this warp's rows of the tile
+          for (int i = lane; i < 32 * 16; i += 32) {
+            const int row = warp * 32 + (i >> 4);
+            if (row >= ntok) *reinterpret_cast<uint4*>(vt + swz_tma(row, i & 15)) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          __syncwarp();
+        }
+        vbase = smem_u32(vt);
+        vrow0 = warp * 32;
       }
-    } else {
-      // ---- O += P V for this warp's 32 tokens (2 k-steps of 16)
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
-        const int row = warp * 32 + kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int row = vrow0 + kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
         for (int nd = 0; nd < 16; nd += 2) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(tile_s + swz(row, nd + (lane >> 4)), b0, b1, b2, b3);
-          mma_bf16(acc[nd], pa[kk], b0, b1);
-          mma_bf16(acc[nd + 1], pa[kk], b2, b3);
+          if (FP8) {
+            ldsm_x4_t(vbase + swz(row, nd + (lane >> 4)), b0, b1, b2, b3);
+            mma_f16(acc[nd], pa[kk], b0, b1);
+            mma_f16(acc[nd + 1], pa[kk], b2, b3);
+          } else {
+            ldsm_x4_t(vbase + swz_tma(row, nd + (lane >> 4)), b0, b1, b2, b3);
+            mma_bf16(acc[nd], pa[kk], b0, b1);
+            mma_bf16(acc[nd + 1], pa[kk], b2, b3);
+          }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[stage]);
+      if (++stage == NST) { stage = 0; phase ^= 1u; }
     }
-    __syncthreads();
-  }
-  cp_async_wait<0>();
 
-  // ---- merge the four warps' states
+    // ---------------- merge the four warps' states; warp 0 writes the partial
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    l_r[i] += __shfl_xor_sync(0xffffffffu, l_r[i], 1);
-    l_r[i] += __shfl_xor_sync(0xffffffffu, l_r[i], 2);
-  }
-  if (tq == 0) {
-    red_m[warp][g] = m_r[0];
-    red_m[warp][g + 8] = m_r[1];
-    red_l[warp][g] = l_r[0];
-    red_l[warp][g + 8] = l_r[1];
-  }
-  __syncthreads();
-  float* red = reinterpret_cast<float*>(smem);   // [4 warps][16 rows][128] fp32, 32 KiB
-  float fw[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int row = g + 8 * i;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, red_m[w][row]);
-    fw[i] = M == -INFINITY ? 0.f : exp2f(m_r[i] - M);
-  }
-#pragma unroll
-  for (int nd = 0; nd < 16; ++nd) {
-    const int col = nd * 8 + 2 * tq;
-    float* p0 = red + (warp * 16 + g) * kHeadDim + col;
-    float* p1 = red + (warp * 16 + g + 8) * kHeadDim + col;
-    *reinterpret_cast<float2*>(p0) = make_float2(acc[nd][0] * fw[0], acc[nd][1] * fw[0]);
-    *reinterpret_cast<float2*>(p1) = make_float2(acc[nd][2] * fw[1], acc[nd][3] * fw[1]);
-  }
-  __syncthreads();
-  // thread = output column; rows < G
-  const int col = tid;
-  for (int row = 0; row < a.G; ++row) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, red_m[w][row]);
-    float L = 0.f, o = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float f = M == -INFINITY ? 0.f : exp2f(red_m[w][row] - M);
-      L += red_l[w][row] * f;
-      o += red[(w * 16 + row) * kHeadDim + col];
+    for (int i = 0; i < 2; ++i) {
+      l_r[i] += __shfl_xor_sync(0xffffffffu, l_r[i], 1);
+      l_r[i] += __shfl_xor_sync(0xffffffffu, l_r[i], 2);
     }
-    const int64_t hq = (int64_t)t * a.Hq + (int64_t)h * a.G + row;
-    const bool empty = !(L > 0.f);
-    static_cast<float*>(ws.o_part)[(hq * a.nsplit + s) * kHeadDim + col] =
-        empty ? 0.f : o * (a.v_scale / L);
-    if (col == 0)
-      ws.lse_part[hq * a.nsplit + s] = empty ? -INFINITY : (M + log2f(L)) * kLn2;
+    named_bar_sync(1, kConsumers * 32);            // previous item fully written out
+    if (tq == 0) {
+      red_m[warp][g] = m_r[0];
+      red_m[warp][g + 8] = m_r[1];
+      red_l[warp][g] = l_r[0];
+      red_l[warp][g + 8] = l_r[1];
+    }
+    named_bar_sync(1, kConsumers * 32);
+    float fw[2], Ltot[2], Mx[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int row = g + 8 * i;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, red_m[w][row]);
+      Mx[i] = M;
+      fw[i] = M == -INFINITY ? 0.f : exp2f(m_r[i] - M);
+      float Ls = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w)
+        Ls += M == -INFINITY ? 0.f : red_l[w][row] * exp2f(red_m[w][row] - M);
+      Ltot[i] = Ls;
+    }
+    if (warp > 0) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int row = g + 8 * i;
+        if (row >= a.G) continue;
+        float* dst = merge + ((warp - 1) * a.G + row) * kHeadDim;
+#pragma unroll
+        for (int nd = 0; nd < 16; ++nd)
+          *reinterpret_cast<float2*>(dst + nd * 8 + 2 * tq) =
+              make_float2(acc[nd][2 * i] * fw[i], acc[nd][2 * i + 1] * fw[i]);
+      }
+    }
+    named_bar_sync(1, kConsumers * 32);
+    if (warp == 0) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int row = g + 8 * i;
+        if (row >= a.G) continue;
+        const int64_t hq = (int64_t)it.t * a.Hq + (int64_t)it.h * a.G + row;
+        const bool empty = !(Ltot[i] > 0.f);
+        const float sc = empty ? 0.f : a.v_scale / Ltot[i];
+        float* dst = static_cast<float*>(ws.o_part) + (hq * a.nsplit + it.s) * kHeadDim;
+#pragma unroll
+        for (int nd = 0; nd < 16; ++nd) {
+          float x0 = acc[nd][2 * i] * fw[i], x1 = acc[nd][2 * i + 1] * fw[i];
+#pragma unroll
+          for (int w = 0; w < kConsumers - 1; ++w) {
+            const float2 v = *reinterpret_cast<const float2*>(merge + (w * a.G + row) * kHeadDim +
+                                                              nd * 8 + 2 * tq);
+            x0 += v.x;
+            x1 += v.y;
+          }
+          *reinterpret_cast<float2*>(dst + nd * 8 + 2 * tq) = make_float2(x0 * sc, x1 * sc);
+        }
+        if (tq == 0)
+          ws.lse_part[hq * a.nsplit + it.s] = empty ? -INFINITY : (Mx[i] + log2f(Ltot[i])) * kLn2;
+      }
+    }
   }
 }
 
@@ -358,24 +484,78 @@ combine_kernel(WsView ws, int Hq, int nsplit, __nv_bfloat16* __restrict__ out,
 }
 
 template <bool FP8>
-size_t decode_smem() {
-  return (size_t)kStages * kTileBytes + (FP8 ? kTileBytes : 0);
+size_t decode_smem(int G) {
+  const size_t ring = FP8 ? (size_t)kFp8Stages * kFp8TileBytes : (size_t)kStages * kTileBytes;
+  const size_t conv = FP8 ? (size_t)kConsumers * kConvBytes : 0;
+  return ring + conv + (size_t)(kConsumers - 1) * G * kHeadDim * 4;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Tensor map of a KV pool viewed as [num_pages * H_kv * 128 rows, 128 columns]:
+// bf16 -> boxes of 64 columns x 128 rows, e4m3 -> 128 x 128, 128-byte swizzle.
+bool make_pool_map(CUtensorMap* m, const void* base, int64_t rows, bool fp8) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * (fp8 ? 1 : 2)};
+  const cuuint32_t box[2] = {fp8 ? 128u : 64u, (cuuint32_t)kBlock};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <bool FP8>
-msa_status ensure_smem_attr() {
+msa_status launch_decode(const WsView& v, const DecodeArgs& a, const CUtensorMap& tk,
+                         const CUtensorMap& tv, cudaStream_t s) {
   static std::mutex mu;
-  static bool done[64] = {false};
+  static int grid_per_dev[64] = {0};
+  static size_t smem_set[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return MSA_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(mu);
-  if (!done[dev]) {
-    if (cudaFuncSetAttribute(decode_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)decode_smem<FP8>()) != cudaSuccess)
-      return MSA_ERR_CUDA;
-    done[dev] = true;
+  const size_t smem = decode_smem<FP8>(a.G);
+  int grid;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (smem_set[dev] < smem) {
+      if (cudaFuncSetAttribute(decode_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem) != cudaSuccess)
+        return MSA_ERR_CUDA;
+      smem_set[dev] = smem;
+      grid_per_dev[dev] = 0;
+    }
+    if (grid_per_dev[dev] == 0) {
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<FP8>, kThreads,
+                                                        smem) != cudaSuccess)
+        return MSA_ERR_CUDA;
+      grid_per_dev[dev] = sm_count() * (per_sm > 0 ? per_sm : 1);
+    }
+    grid = grid_per_dev[dev];
   }
-  return MSA_OK;
+  if (grid > a.n_items) grid = a.n_items;
+  if (grid <= 0) return MSA_OK;
+  decode_kernel<FP8><<<grid, kThreads, smem, s>>>(v, a, tk, tv);
+  return launch_status();
 }
 
 }  // namespace
@@ -388,40 +568,35 @@ extern "C" msa_status msa_sparse_decode(const msa_config* cfg, void* ws, const v
                                         const int32_t* selected, msa_stream_t stream) {
   msa_status st = check_config(cfg);
   if (st != MSA_OK) return st;
+  if (is_prefill(*cfg)) return MSA_ERR_INVALID_ARG;   // prefill uses msa_sparse_prefill
   if (!ws || !q || !k_pages || !v_pages || !selected) return MSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages)) return MSA_ERR_INVALID_ARG;
-  if (is_prefill(*cfg)) return MSA_ERR_INVALID_ARG;   // prefill uses msa_sparse_prefill
-  const int S = width_of(*cfg);
-  if (S > 64 * 1024) return MSA_ERR_UNSUPPORTED;
   DecodeArgs a;
   a.Hkv = cfg->num_kv_heads;
   a.Hq = cfg->num_q_heads;
   a.G = cfg->num_q_heads / cfg->num_kv_heads;
-  a.S = S;
+  a.S = width_of(*cfg);
   a.bps = blocks_per_split_of(*cfg);
   if (a.bps > 32) return MSA_ERR_UNSUPPORTED;   // one warp lists a split's blocks
   a.nsplit = splits_of(*cfg);
   a.max_blocks = cfg->max_blocks_per_req;
+  const int64_t items = (int64_t)max_tokens_of(*cfg) * a.Hkv * a.nsplit;
+  if (items <= 0) return MSA_OK;
+  if (items > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
+  a.n_items = (int)items;
   const bool fp8 = cfg->kv_dtype == MSA_KV_FP8_E4M3;
   a.scale_log2 = cfg->softmax_scale * (fp8 ? cfg->k_scale : 1.f) * kLog2e;
   a.v_scale = fp8 ? cfg->v_scale : 1.f;
   a.q = (const __nv_bfloat16*)q;
-  a.k = (const uint8_t*)k_pages;
-  a.v = (const uint8_t*)v_pages;
   a.selected = selected;
-  const int64_t grid = (int64_t)max_tokens_of(*cfg) * a.Hkv * a.nsplit;
-  if (grid <= 0) return MSA_OK;
-  if (grid > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
+  const int64_t rows = (int64_t)cfg->num_pages * a.Hkv * kBlock;
+  if (rows > 0x7fffffff) return MSA_ERR_UNSUPPORTED;   // TMA row coordinates are int32
+  CUtensorMap tk, tv;
+  if (!make_pool_map(&tk, k_pages, rows, fp8) || !make_pool_map(&tv, v_pages, rows, fp8))
+    return MSA_ERR_CUDA;
   const WsView v = view_of(*cfg, ws);
   cudaStream_t s = (cudaStream_t)stream;
-  if (fp8) {
-    if ((st = ensure_smem_attr<true>()) != MSA_OK) return st;
-    decode_kernel<true><<<(unsigned)grid, kThreads, decode_smem<true>(), s>>>(v, a);
-  } else {
-    if ((st = ensure_smem_attr<false>()) != MSA_OK) return st;
-    decode_kernel<false><<<(unsigned)grid, kThreads, decode_smem<false>(), s>>>(v, a);
-  }
-  return launch_status();
+  return fp8 ? launch_decode<true>(v, a, tk, tv, s) : launch_decode<false>(v, a, tk, tv, s);
 }
 
 extern "C" msa_status msa_combine(const msa_config* cfg, const void* ws, void* out, float* lse,

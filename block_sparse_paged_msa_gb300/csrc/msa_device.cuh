@@ -87,6 +87,13 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// e4m3 byte pair -> f16x2 (exact, hardware conversion).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+  return h;
+}
+
 // e4m3 byte pair -> bf16x2 (exact): via the hardware f16x2 conversion.
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
   uint32_t h;
@@ -94,6 +101,79 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
   const __half2 hh = *reinterpret_cast<const __half2*>(&h);
   const float2 f = __half22float2(hh);
   return pack_bf16(f.x, f.y);
+}
+
+// ---------------------------------------------------------------- mbarrier / TMA
+// Waits are bounded: after kWaitLimit polls the waiter records
+// MSA_DEVERR_TIMEOUT in the workspace error word and carries on, so no CTA can
+// spin forever (the results of that launch are then flagged as invalid).
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity; false on timeout.
+// Once any waiter has timed out (the error word says so), every other wait
+// gives up within a few hundred polls instead of running to its own limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WsHeader* hdr) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u &&
+        (*reinterpret_cast<volatile int*>(&hdr->err) & MSA_DEVERR_TIMEOUT))
+      return false;
+  }
+  atomicOr(&hdr->err, MSA_DEVERR_TIMEOUT);
+  return false;
+}
+
+// 2-D tiled TMA load of box (x, y) into shared memory, completion counted on
+// `bar` in bytes.  x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Named barrier over `count` threads (ids 1.. are free; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Address of 16-byte chunk c (0..15) of row `row` in a 128-row tile of 256-byte
+// rows loaded as two 64-column TMA boxes with 128-byte swizzle: columns 0..63
+// in the first 16 KiB, 64..127 in the second; inside a box the chunk index is
+// XORed with row % 8 (the hardware's SWIZZLE_128B pattern).
+__device__ __forceinline__ uint32_t swz_tma(int row, int c) {
+  return (uint32_t)(((c >> 3) << 14) + row * 128 + ((((c & 7) ^ (row & 7))) << 4));
 }
 
 }  // namespace msa

@@ -21,7 +21,7 @@ MSA_KV_BF16, MSA_KV_FP8_E4M3 = 0, 1
 MSA_MODE_DECODE, MSA_MODE_PREFILL = 0, 1
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED",
           3: "MSA_ERR_CUDA", 4: "MSA_ERR_DEVICE_FLAG"}
-DEVERR_BITS = {1: "PAGE_RANGE", 2: "SEQ_LEN", 4: "SLOT_ALIGN"}
+DEVERR_BITS = {1: "PAGE_RANGE", 2: "SEQ_LEN", 4: "SLOT_ALIGN", 8: "TIMEOUT"}
 
 
 class MsaError(RuntimeError):

@@ -86,7 +86,8 @@ enum {
   MSA_DEVERR_PAGE_RANGE = 1,   /* block table / req_to_token page outside the pool */
   MSA_DEVERR_SEQ_LEN = 2,      /* seq_len > max_blocks_per_req*P, or < query count,
                                   or the step's tokens exceed max_q_tokens        */
-  MSA_DEVERR_SLOT_ALIGN = 4    /* req_to_token slot of a block not page-aligned   */
+  MSA_DEVERR_SLOT_ALIGN = 4,   /* req_to_token slot of a block not page-aligned   */
+  MSA_DEVERR_TIMEOUT = 8       /* a pipeline wait gave up (results invalid)       */
 };
 
 /*
