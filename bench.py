@@ -264,6 +264,8 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     cu = w.cu_seqlens_q if sa.prefill else None
     c = sa.cfg
+    # the step's calls, as msa_decode_step chains them (decode) or
+    # SparseAttention.run does (prefill)
     calls = [
         ("plan", lambda: msa.plan(c, w.seq_lens, w.block_table, sa.ws, cu)),
         ("index_score", lambda: msa.index_score(c, sa.ws, w.idx_q, w.idx_k_pages,

@@ -150,6 +150,8 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
     fence_barrier_init();
   }
   __syncthreads();
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
@@ -443,6 +445,8 @@ combine_kernel(WsView ws, int Hq, int nsplit, __nv_bfloat16* __restrict__ out,
   const int lane = threadIdx.x & 31;
   const int64_t idx = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int t = (int)(idx / Hq);
+  griddep_launch_dependents();
+  griddep_wait();
   if (t >= ws.hdr->num_tokens) return;
   const bool active = ws.tok_req[t] >= 0;
   int nvalid = nsplit;
@@ -554,8 +558,7 @@ msa_status launch_decode(const WsView& v, const DecodeArgs& a, const CUtensorMap
   }
   if (grid > a.n_items) grid = a.n_items;
   if (grid <= 0) return MSA_OK;
-  decode_kernel<FP8><<<grid, kThreads, smem, s>>>(v, a, tk, tv);
-  return launch_status();
+  return launch_pdl(decode_kernel<FP8>, dim3(grid), dim3(kThreads), smem, s, v, a, tk, tv);
 }
 
 }  // namespace
@@ -609,11 +612,12 @@ extern "C" msa_status msa_combine(const msa_config* cfg, const void* ws, void* o
   if (items <= 0) return MSA_OK;
   const int64_t grid = (items + 7) / 8;
   if (grid > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
+  const WsView v = view_of(*cfg, ws);
   if (is_prefill(*cfg))
-    combine_kernel<true><<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
-        view_of(*cfg, ws), cfg->num_q_heads, splits_of(*cfg), (__nv_bfloat16*)out, lse);
-  else
-    combine_kernel<false><<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
-        view_of(*cfg, ws), cfg->num_q_heads, splits_of(*cfg), (__nv_bfloat16*)out, lse);
-  return launch_status();
+    return launch_pdl(combine_kernel<true>, dim3((unsigned)grid), dim3(256), 0,
+                      (cudaStream_t)stream, v, cfg->num_q_heads, splits_of(*cfg),
+                      (__nv_bfloat16*)out, lse);
+  return launch_pdl(combine_kernel<false>, dim3((unsigned)grid), dim3(256), 0,
+                    (cudaStream_t)stream, v, cfg->num_q_heads, splits_of(*cfg),
+                    (__nv_bfloat16*)out, lse);
 }

@@ -75,6 +75,8 @@ index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
       }
     }
   }
+  griddep_launch_dependents();
+  griddep_wait();
   const int batch = ws.hdr->batch;
   const int total = ws.hdr->total_blocks * Hkv;
   const int warps = gridDim.x * (kThreads / 32);
@@ -164,24 +166,40 @@ msa_status launch(const msa_config& c, const WsView& v, const void* idx_q, const
   static std::mutex mu;
   static int occ[64] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return MSA_ERR_CUDA;
   int blocks_per_sm;
   {
     std::lock_guard<std::mutex> lk(mu);
-    if (dev < 64 && occ[dev] == 0) {
+    if (occ[dev] == 0) {
       int n = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, index_score_kernel<DIDX, QL>,
                                                         kThreads, 0) != cudaSuccess)
         return MSA_ERR_CUDA;
       occ[dev] = n > 0 ? n : 1;
     }
-    blocks_per_sm = dev < 64 ? occ[dev] : 1;
+    blocks_per_sm = occ[dev];
   }
   const int grid = sm_count() * blocks_per_sm;
   if (grid <= 0) return MSA_ERR_CUDA;
-  index_score_kernel<DIDX, QL><<<grid, kThreads, 0, s>>>(
-      v, c.num_kv_heads, c.max_blocks_per_req, max_tokens_of(c), (const uint4*)idx_q, (const uint4*)idx_k, scores);
-  return launch_status();
+  return launch_pdl(index_score_kernel<DIDX, QL>, dim3(grid), dim3(kThreads), 0, s, v,
+                    c.num_kv_heads, c.max_blocks_per_req, max_tokens_of(c),
+                    (const uint4*)idx_q, (const uint4*)idx_k, scores);
+}
+
+msa_status dispatch(const msa_config& c, const WsView& v, const void* idx_q, const void* idx_k,
+                    float* scores, cudaStream_t s) {
+  const bool d128 = c.index_dim == 128;
+  switch (c.q_len) {
+    case 1: return d128 ? launch<128, 1>(c, v, idx_q, idx_k, scores, s)
+                        : launch<64, 1>(c, v, idx_q, idx_k, scores, s);
+    case 2: return d128 ? launch<128, 2>(c, v, idx_q, idx_k, scores, s)
+                        : launch<64, 2>(c, v, idx_q, idx_k, scores, s);
+    case 3: return d128 ? launch<128, 3>(c, v, idx_q, idx_k, scores, s)
+                        : launch<64, 3>(c, v, idx_q, idx_k, scores, s);
+    case 4: return d128 ? launch<128, 4>(c, v, idx_q, idx_k, scores, s)
+                        : launch<64, 4>(c, v, idx_q, idx_k, scores, s);
+    default: return MSA_ERR_UNSUPPORTED;
+  }
 }
 
 }  // namespace
@@ -199,16 +217,5 @@ extern "C" msa_status msa_index_score(const msa_config* cfg, const void* ws, con
   const WsView v = view_of(*cfg, ws);
   cudaStream_t s = (cudaStream_t)stream;
   if (is_prefill(*cfg)) return prefill_index_score(*cfg, v, idx_q, idx_k_pages, block_scores, s);
-  const bool d128 = cfg->index_dim == 128;
-  switch (cfg->q_len) {
-    case 1: return d128 ? launch<128, 1>(*cfg, v, idx_q, idx_k_pages, block_scores, s)
-                        : launch<64, 1>(*cfg, v, idx_q, idx_k_pages, block_scores, s);
-    case 2: return d128 ? launch<128, 2>(*cfg, v, idx_q, idx_k_pages, block_scores, s)
-                        : launch<64, 2>(*cfg, v, idx_q, idx_k_pages, block_scores, s);
-    case 3: return d128 ? launch<128, 3>(*cfg, v, idx_q, idx_k_pages, block_scores, s)
-                        : launch<64, 3>(*cfg, v, idx_q, idx_k_pages, block_scores, s);
-    case 4: return d128 ? launch<128, 4>(*cfg, v, idx_q, idx_k_pages, block_scores, s)
-                        : launch<64, 4>(*cfg, v, idx_q, idx_k_pages, block_scores, s);
-    default: return MSA_ERR_UNSUPPORTED;
-  }
+  return dispatch(*cfg, v, idx_q, idx_k_pages, block_scores, s);
 }

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/msa.h"
 
 namespace msa {
@@ -18,10 +20,11 @@ constexpr int kMaxBatch = 65536;
 
 // Workspace header (first 256 bytes).
 struct WsHeader {
-  int32_t err;            // MSA_DEVERR_* bits, reset by msa_plan
+  int32_t err;            // MSA_DEVERR_* bits of the kernels after the plan
   int32_t batch;
   int32_t num_tokens;     // T of the current plan
   int32_t total_blocks;   // sum over requests of ceil(seq_len / P)
+  int32_t max_batch;      // number of plan_err words
 };
 
 inline size_t align_up(size_t x, size_t a = 256) { return (x + a - 1) / a * a; }
@@ -58,7 +61,7 @@ inline int64_t csr_rows_of(const msa_config& c) {
 
 // Byte offsets of every workspace region.
 struct WsLayout {
-  size_t req_seq_len, req_nb, req_cu_nb, req_qstart, tok_req, tok_pos, block_table;
+  size_t plan_err, req_seq_len, req_nb, req_cu_nb, req_qstart, tok_req, tok_pos, block_table;
   size_t o_part, lse_part, total;
 };
 
@@ -67,6 +70,7 @@ inline WsLayout layout_of(const msa_config& c) {
   const size_t B = (size_t)c.max_batch, T = (size_t)max_tokens_of(c);
   const size_t NS = (size_t)splits_of(c), Hq = (size_t)c.num_q_heads;
   size_t o = 256;
+  L.plan_err = o;    o = align_up(o + 4 * (B > 0 ? B : 1));
   L.req_seq_len = o; o = align_up(o + 4 * B);
   L.req_nb = o;      o = align_up(o + 4 * B);
   L.req_cu_nb = o;   o = align_up(o + 4 * (B + 1));
@@ -83,6 +87,7 @@ inline WsLayout layout_of(const msa_config& c) {
 // Typed views of a workspace, passed to kernels by value.
 struct WsView {
   WsHeader* hdr;
+  int32_t* plan_err;      // [max_batch] error bits of each plan CTA, rewritten every plan
   int32_t* req_seq_len;
   int32_t* req_nb;
   int32_t* req_cu_nb;
@@ -99,6 +104,7 @@ inline WsView view_of(const msa_config& c, const void* ws) {
   char* b = (char*)ws;
   WsView v;
   v.hdr = (WsHeader*)b;
+  v.plan_err = (int32_t*)(b + L.plan_err);
   v.req_seq_len = (int32_t*)(b + L.req_seq_len);
   v.req_nb = (int32_t*)(b + L.req_nb);
   v.req_cu_nb = (int32_t*)(b + L.req_cu_nb);
@@ -120,6 +126,33 @@ int sm_count();  // SMs of the current device (cached per device)
 // Launch-status helper: any launch error becomes MSA_ERR_CUDA.
 inline msa_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+// Every kernel of the path is launched with programmatic stream serialization
+// (PDL): its launch and CTA start-up overlap the previous kernel's tail, and
+// the kernel itself calls griddep_wait() before touching anything the previous
+// kernel may still be writing or reading.  Capturable in CUDA graphs.
+template <typename... KArgs, typename... Args>
+inline msa_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...) == cudaSuccess
+             ? MSA_OK
+             : MSA_ERR_CUDA;
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }

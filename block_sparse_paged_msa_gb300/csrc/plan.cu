@@ -98,12 +98,18 @@ __device__ __forceinline__ bool request_flagged(int r, const int* seq_lens, cons
 // One CTA per request copies (and validates) its block-table row; CTA 0 also
 // builds the request / token metadata.
 __global__ void __launch_bounds__(256)
-plan_kernel(WsView ws, int batch, int q_len, int max_blocks, int max_tokens, int num_pages,
-            const int* __restrict__ seq_lens, const int* __restrict__ cu_q,
-            const int* __restrict__ bt, int bt_stride, const int* __restrict__ r2t,
-            int r2t_stride, const int64_t* __restrict__ pool_idx) {
+plan_kernel(WsView ws, int batch, int max_batch, int Hkv, int q_len, int max_blocks,
+            int max_tokens, int num_pages, const int* __restrict__ seq_lens,
+            const int* __restrict__ cu_q, const int* __restrict__ bt, int bt_stride,
+            const int* __restrict__ r2t, int r2t_stride, const int64_t* __restrict__ pool_idx) {
   const int tid = threadIdx.x;
   const int r = blockIdx.x;
+  griddep_launch_dependents();
+  griddep_wait();            // the previous step may still read this workspace
+  if (r == 0 && tid == 0) {
+    ws.hdr->err = 0;         // later kernels' bits; this kernel reports in plan_err
+    ws.hdr->max_batch = max_batch;
+  }
   if (r < batch) {
     ReqInfo ri = request_info(r, seq_lens, cu_q, q_len, max_blocks, max_tokens);
     int bad = 0;
@@ -125,9 +131,16 @@ plan_kernel(WsView ws, int batch, int q_len, int max_blocks, int max_tokens, int
     }
     if (tid == 0 && request_flagged(r, seq_lens, cu_q, q_len, max_blocks, max_tokens))
       bad |= MSA_DEVERR_SEQ_LEN;
-    if (bad) set_error(ws.hdr, bad);
+    __shared__ int bad_s;
+    if (tid == 0) bad_s = 0;
+    __syncthreads();
+    if (bad) atomicOr(&bad_s, bad);
+    __syncthreads();
+    if (tid == 0) ws.plan_err[r] = bad_s;
   }
   if (r != 0) return;
+  for (int i = (batch > 0 ? batch : 0) + tid; i < (max_batch > 0 ? max_batch : 1); i += blockDim.x)
+    ws.plan_err[i] = 0;
 
   // ---- CTA 0: per-request block counts and prefix sums (chunked block scan)
   __shared__ int warp_sums[8];
@@ -170,7 +183,7 @@ plan_kernel(WsView ws, int batch, int q_len, int max_blocks, int max_tokens, int
     if (T < 0) T = 0;
     if (T > max_tokens) {
       T = max_tokens;
-      if (tid == 0) set_error(ws.hdr, MSA_DEVERR_SEQ_LEN);
+      if (tid == 0) set_error(ws.hdr, MSA_DEVERR_SEQ_LEN);   // after the reset above
     }
   }
   if (tid == 0) {
@@ -211,12 +224,11 @@ static msa_status plan_common(const msa_config* cfg, int32_t batch, const int32_
   if (cfg->mode == MSA_MODE_PREFILL && batch > 0 && cu_q == nullptr) return MSA_ERR_INVALID_ARG;
   if (r2t != nullptr && r2t_stride < cfg->max_blocks_per_req * kBlock) return MSA_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), s) != cudaSuccess) return MSA_ERR_CUDA;
   WsView v = view_of(*cfg, ws);
-  plan_kernel<<<batch > 0 ? batch : 1, 256, 0, s>>>(
-      v, batch, cfg->q_len, cfg->max_blocks_per_req, max_tokens_of(*cfg), cfg->num_pages,
-      seq_lens, cu_q, bt, bt_stride, r2t, r2t_stride, pool_idx);
-  return launch_status();
+  return launch_pdl(plan_kernel, dim3(batch > 0 ? batch : 1), dim3(256), 0, s, v, batch,
+                    cfg->max_batch, cfg->num_kv_heads, cfg->q_len, cfg->max_blocks_per_req,
+                    max_tokens_of(*cfg), cfg->num_pages, seq_lens, cu_q, bt, bt_stride, r2t,
+                    r2t_stride, pool_idx);
 }
 
 }  // namespace msa
@@ -273,12 +285,22 @@ msa_status msa_plan_from_req_to_token(const msa_config* cfg, int32_t batch,
 msa_status msa_check_device_error(const void* ws, int32_t* flags, msa_stream_t stream) {
   if (ws == nullptr || flags == nullptr) return MSA_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  int32_t h = 0;
-  if (cudaMemcpyAsync(&h, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  WsHeader h;
+  if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
     return MSA_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return MSA_ERR_CUDA;
-  *flags = h;
-  return h ? MSA_ERR_DEVICE_FLAG : MSA_OK;
+  int32_t bits = h.err;
+  const int n = h.max_batch > 0 ? h.max_batch : 1;
+  if (n <= kMaxBatch) {   // the plan's per-request words follow the 256-byte header
+    std::vector<int32_t> pe(n);
+    if (cudaMemcpyAsync(pe.data(), (const char*)ws + 256, sizeof(int32_t) * n,
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return MSA_ERR_CUDA;
+    for (int32_t e : pe) bits |= e;
+  }
+  *flags = bits;
+  return bits ? MSA_ERR_DEVICE_FLAG : MSA_OK;
 }
 
 }  // extern "C"

@@ -57,6 +57,8 @@ prefill_score_kernel(WsView ws, int Hkv, int max_blocks, const __nv_bfloat16* __
   extern __shared__ __align__(128) uint8_t smem[];   // two K tiles
   __shared__ int seg_r[kScoreTokens + 1], seg_start[kScoreTokens + 1];
   __shared__ int nseg_s;
+  griddep_launch_dependents();
+  griddep_wait();
   const int T = ws.hdr->num_tokens;
   const int t0 = blockIdx.x * kScoreTokens;
   const int h = blockIdx.y;
@@ -166,6 +168,8 @@ csr_rows_kernel(WsView ws, int Hkv, int B, int NB, int S, const int32_t* __restr
                 int32_t* __restrict__ row_ptr, int32_t* __restrict__ q_idx) {
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  griddep_launch_dependents();
+  griddep_wait();
   if (row >= (int64_t)Hkv * B * NB) return;
   const int j = (int)(row % NB);
   const int r = (int)((row / NB) % B);
@@ -200,6 +204,8 @@ csr_rows_kernel(WsView ws, int Hkv, int B, int NB, int S, const int32_t* __restr
 __global__ void __launch_bounds__(1024) csr_scan_kernel(int32_t* __restrict__ row_ptr, int64_t rows) {
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  griddep_launch_dependents();
+  griddep_wait();
   const int64_t seg = (rows + 1023) / 1024;
   const int64_t lo = tid * seg, hi = min(rows, lo + seg);
   int sum = 0;
@@ -248,6 +254,8 @@ __device__ __forceinline__ int slot_of(const int32_t* sel, int n, int j) {
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_attn_kernel(WsView ws, PrefillArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];   // K tile, V tile
+  griddep_launch_dependents();
+  griddep_wait();
   const int64_t row = blockIdx.x;
   const int j = (int)(row % a.NB);
   const int r = (int)((row / a.NB) % a.B);
@@ -416,16 +424,14 @@ msa_status prefill_index_score(const msa_config& c, const WsView& v, const void*
   msa_status st;
   if (c.index_dim == 128) {
     if ((st = set_smem(prefill_score_kernel<128>, smem)) != MSA_OK) return st;
-    prefill_score_kernel<128><<<grid, kScoreThreads, smem, s>>>(
-        v, c.num_kv_heads, c.max_blocks_per_req, (const __nv_bfloat16*)idx_q,
-        (const uint8_t*)idx_k, scores);
-  } else {
-    if ((st = set_smem(prefill_score_kernel<64>, smem)) != MSA_OK) return st;
-    prefill_score_kernel<64><<<grid, kScoreThreads, smem, s>>>(
-        v, c.num_kv_heads, c.max_blocks_per_req, (const __nv_bfloat16*)idx_q,
-        (const uint8_t*)idx_k, scores);
+    return launch_pdl(prefill_score_kernel<128>, grid, dim3(kScoreThreads), smem, s, v,
+                      c.num_kv_heads, c.max_blocks_per_req, (const __nv_bfloat16*)idx_q,
+                      (const uint8_t*)idx_k, scores);
   }
-  return launch_status();
+  if ((st = set_smem(prefill_score_kernel<64>, smem)) != MSA_OK) return st;
+  return launch_pdl(prefill_score_kernel<64>, grid, dim3(kScoreThreads), smem, s, v,
+                    c.num_kv_heads, c.max_blocks_per_req, (const __nv_bfloat16*)idx_q,
+                    (const uint8_t*)idx_k, scores);
 }
 
 }  // namespace msa
@@ -455,14 +461,14 @@ extern "C" msa_status msa_build_k2q_csr(const msa_config* cfg, const void* ws,
   cudaStream_t s = (cudaStream_t)stream;
   const unsigned grid = (unsigned)((rows + 7) / 8);
   const int S = width_of(*cfg);
-  csr_rows_kernel<false><<<grid, 256, 0, s>>>(v, cfg->num_kv_heads, cfg->max_batch,
-                                              cfg->max_blocks_per_req, S, selected, row_ptr,
-                                              q_indices);
-  csr_scan_kernel<<<1, 1024, 0, s>>>(row_ptr, rows);
-  csr_rows_kernel<true><<<grid, 256, 0, s>>>(v, cfg->num_kv_heads, cfg->max_batch,
-                                             cfg->max_blocks_per_req, S, selected, row_ptr,
-                                             q_indices);
-  return launch_status();
+  if ((st = launch_pdl(csr_rows_kernel<false>, dim3(grid), dim3(256), 0, s, v, cfg->num_kv_heads,
+                       cfg->max_batch, cfg->max_blocks_per_req, S, selected, row_ptr,
+                       q_indices)) != MSA_OK)
+    return st;
+  if ((st = launch_pdl(csr_scan_kernel, dim3(1), dim3(1024), 0, s, row_ptr, rows)) != MSA_OK)
+    return st;
+  return launch_pdl(csr_rows_kernel<true>, dim3(grid), dim3(256), 0, s, v, cfg->num_kv_heads,
+                    cfg->max_batch, cfg->max_blocks_per_req, S, selected, row_ptr, q_indices);
 }
 
 extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const void* q,
@@ -494,7 +500,6 @@ extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const 
   a.q_idx = q_indices;
   const size_t smem = 2u * kTileBytes;
   if ((st = set_smem(prefill_attn_kernel, smem)) != MSA_OK) return st;
-  prefill_attn_kernel<<<(unsigned)rows, kPfThreads, smem, (cudaStream_t)stream>>>(
-      view_of(*cfg, ws), a);
-  return launch_status();
+  return launch_pdl(prefill_attn_kernel, dim3((unsigned)rows), dim3(kPfThreads), smem,
+                    (cudaStream_t)stream, view_of(*cfg, ws), a);
 }

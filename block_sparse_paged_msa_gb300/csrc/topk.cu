@@ -53,6 +53,8 @@ topk_kernel(WsView ws, int Hkv, int max_blocks, int init, int local, int topk, i
   __shared__ int pick_bin, pick_rem;
   const int tid = threadIdx.x;
   const int t = blockIdx.x / Hkv, h = blockIdx.x % Hkv;
+  griddep_launch_dependents();
+  griddep_wait();
   if (t >= ws.hdr->num_tokens) return;
   int* out = selected + ((int64_t)t * Hkv + h) * S;
   const int r = ws.tok_req[t];
@@ -157,8 +159,8 @@ extern "C" msa_status msa_topk_select(const msa_config* cfg, const void* ws,
   if (grid <= 0) return MSA_OK;
   if (grid > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
   const size_t smem = sizeof(uint32_t) * cfg->max_blocks_per_req;
-  topk_kernel<<<(unsigned)grid, kThreads, smem, (cudaStream_t)stream>>>(
-      v, cfg->num_kv_heads, cfg->max_blocks_per_req, cfg->init_blocks, cfg->local_blocks,
-      cfg->topk_blocks, width_of(*cfg), block_scores, selected);
-  return launch_status();
+  return launch_pdl(topk_kernel, dim3((unsigned)grid), dim3(kThreads), smem,
+                    (cudaStream_t)stream, v, cfg->num_kv_heads, cfg->max_blocks_per_req,
+                    cfg->init_blocks, cfg->local_blocks, cfg->topk_blocks, width_of(*cfg),
+                    block_scores, selected);
 }

@@ -67,6 +67,8 @@ _SIGNATURES = {
     "msa_check_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "msa_sparse_decode_noalloc": (ctypes.c_int, [_CFG, ctypes.c_int32, _P, _P, ctypes.c_int32,
                                                  _P, _P, _P, _P, _P, _P, _P]),
+    "msa_decode_step": (ctypes.c_int, [_CFG, _P, ctypes.c_int32, _P, _P, ctypes.c_int32, _P, _P,
+                                       _P, _P, _P, _P, _P, _P, _P, _P]),
     "msa_k2q_rows": (ctypes.c_int64, [_CFG]),
     "msa_k2q_capacity": (ctypes.c_int64, [_CFG]),
     "msa_build_k2q_csr": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
@@ -227,6 +229,29 @@ def index_score(cfg, ws, idx_q, idx_k_pages, block_scores, stream=None):
         _stream(stream)))
 
 
+def decode_step(cfg, ws, seq_lens, block_table, idx_q, idx_k_pages, q, k_pages, v_pages,
+                block_scores, selected, out, lse, stream=None):
+    """One decode / verify step in one call (plan, index score, top-k,
+    split-K decode, combine)."""
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(idx_q, "idx_q", torch.bfloat16, 3)
+    _need(idx_k_pages, "idx_k_pages", torch.bfloat16, 4)
+    _need(q, "q", torch.bfloat16, 3)
+    kv = (torch.bfloat16,) if cfg.kv_dtype == MSA_KV_BF16 else (torch.float8_e4m3fn, torch.uint8)
+    _need(k_pages, "k_pages", kv, 4)
+    _need(v_pages, "v_pages", kv, 4)
+    _need(block_scores, "block_scores", torch.float32, 3)
+    _need(selected, "selected", torch.int32, 3)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    _check("msa_decode_step", lib().msa_decode_step(
+        ctypes.byref(cfg), _ptr(ws), seq_lens.shape[0], _ptr(seq_lens), _ptr(block_table),
+        block_table.shape[1], _ptr(idx_q), _ptr(idx_k_pages), _ptr(q), _ptr(k_pages),
+        _ptr(v_pages), _ptr(block_scores), _ptr(selected), _ptr(out), _ptr(lse),
+        _stream(stream)))
+
+
 def topk_select(cfg, ws, block_scores, selected, stream=None):
     _need(block_scores, "block_scores", torch.float32, 3)
     _need(selected, "selected", torch.int32, 3)
@@ -318,10 +343,14 @@ class SparseAttention:
 
     def run(self, seq_lens, block_table, idx_q, idx_k_pages, q, k_pages, v_pages,
             cu_seqlens_q=None, stream=None):
-        """Decode / verify: plan, index score, top-k, split-K decode, combine.
-        Prefill (cu_seqlens_q required): plan, index score, top-k, CSR,
-        sparse prefill tiles, combine."""
+        """Decode / verify: msa_decode_step (plan, index score, top-k,
+        split-K decode, combine).  Prefill (cu_seqlens_q required): plan, index
+        score, top-k, CSR, sparse prefill tiles, combine."""
         c = self.cfg
+        if not self.prefill and cu_seqlens_q is None:
+            decode_step(c, self.ws, seq_lens, block_table, idx_q, idx_k_pages, q, k_pages,
+                        v_pages, self.block_scores, self.selected, self.out, self.lse, stream)
+            return self.out, self.lse
         plan(c, seq_lens, block_table, self.ws, cu_seqlens_q, stream)
         index_score(c, self.ws, idx_q, idx_k_pages, self.block_scores, stream)
         topk_select(c, self.ws, self.block_scores, self.selected, stream)

@@ -286,8 +286,23 @@ msa_status msa_sparse_decode_noalloc(const msa_config* cfg, int32_t batch,
                                      float* lse, msa_stream_t stream);
 
 /*
- * msa_check_device_error -- synchronises `stream`, copies the workspace error
- * word to *flags (host) and returns MSA_ERR_DEVICE_FLAG if any bit is set.
+ * msa_decode_step -- one decode / verify step (decode mode): msa_plan (with
+ * cu_seqlens_q = NULL), msa_index_score, msa_topk_select, msa_sparse_decode,
+ * msa_combine.
+ * Arguments as in those calls.  The kernels are chained with programmatic
+ * dependent launch, so each one's launch overlaps the previous one's tail.
+ */
+msa_status msa_decode_step(const msa_config* cfg, void* ws, int32_t batch,
+                           const int32_t* seq_lens, const int32_t* block_table,
+                           int32_t bt_stride, const void* idx_q, const void* idx_k_pages,
+                           const void* q, const void* k_pages, const void* v_pages,
+                           float* block_scores, int32_t* selected, void* out, float* lse,
+                           msa_stream_t stream);
+
+/*
+ * msa_check_device_error -- synchronises `stream`, reads the workspace error
+ * words (the plan's per-request words and the later kernels' word) into
+ * *flags (host, OR of all) and returns MSA_ERR_DEVICE_FLAG if any bit is set.
  * Never call it inside stream capture.
  */
 msa_status msa_check_device_error(const void* ws, int32_t* flags, msa_stream_t stream);
