@@ -39,12 +39,23 @@ namespace msa {
 namespace {
 
 constexpr int kConsumers = 4;                      // consumer warps
-constexpr int kThreads = (kConsumers + 1) * 32;    // + one producer warp
+constexpr int kScheduler = kConsumers;             // warp ids of the two
+constexpr int kLoader = kConsumers + 1;            // producer warps
+constexpr int kThreads = (kConsumers + 2) * 32;
 constexpr int kStages = 3;                         // ring depth (tiles)
 constexpr int kTileBytes = kBlock * kHeadDim * 2;  // bf16 tile, 32 KiB
 constexpr int kFp8Stages = 4;                      // fp8 tiles are 16 KiB
 constexpr int kFp8TileBytes = kBlock * kHeadDim;
 constexpr int kConvBytes = 32 * 256;               // per consumer warp: 32 rows, f16
+constexpr int kItems = 2;                          // work-item records in flight
+
+// A work item as the producer publishes it: the consumers read only this and
+// the item's Q rows (copied next to it), never the global metadata.
+struct ItemMeta {
+  int t, h, s, nblk;
+  int page[32];        // physical page of each usable block, in slot order
+  uint8_t ntok[32];    // its visible rows (1..128)
+};
 
 struct DecodeArgs {
   int Hkv, Hq, G, S, bps, nsplit, max_blocks, n_items;
@@ -137,8 +148,11 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem;                                      // NST x TB, 1 KiB aligned
   uint8_t* conv = smem + NST * TB;                           // fp8: 4 x 8 KiB
-  float* merge = reinterpret_cast<float*>(conv + (FP8 ? kConsumers * kConvBytes : 0));
+  uint8_t* qbuf = conv + (FP8 ? kConsumers * kConvBytes : 0);   // kItems x G x 256 B
+  float* merge = reinterpret_cast<float*>(qbuf + kItems * a.G * 256);
   __shared__ __align__(8) uint64_t full_bar[NST], empty_bar[NST];
+  __shared__ __align__(8) uint64_t item_full[kItems], item_empty[kItems];
+  __shared__ ItemMeta meta[kItems];
   __shared__ float red_m[kConsumers][16], red_l[kConsumers][16];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -147,46 +161,82 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kConsumers);
     }
+    for (int i = 0; i < kItems; ++i) {
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_empty[i], kConsumers + 1);   // consumers + loader
+    }
     fence_barrier_init();
   }
   __syncthreads();
   griddep_launch_dependents();
   griddep_wait();
 
-  if (warp == kConsumers) {
-    // ------------------------------------------------------------ producer
-    int stage = 0;
-    uint32_t phase = 0;
+  if (warp == kScheduler) {
+    // -------------------------------------------------------- scheduler
+    // Resolves each work item (token metadata -> selected slots -> pages) and
+    // publishes it with the item's Q rows, up to kItems ahead of the others.
+    int islot = 0;
+    uint32_t iphase = 0;
     for (int idx = blockIdx.x; idx < a.n_items; idx += gridDim.x) {
       const Item it = item_of(ws, a, idx);
       if (!it.active) continue;
-      ItemBlocks bl = item_blocks(ws, a, it.t, it.h, it.s, it.r, it.pos, lane);
-      unsigned m = bl.mask;
-      while (m) {
-        const int L = __ffs(m) - 1;
-        m &= m - 1;
-        const int page = __shfl_sync(0xffffffffu, bl.page, L);
-        const int y = (page * a.Hkv + it.h) * kBlock;
+      const ItemBlocks bl = item_blocks(ws, a, it.t, it.h, it.s, it.r, it.pos, lane);
+      if (lane == 0) mbar_wait(&item_empty[islot], iphase ^ 1u, ws.hdr);
+      __syncwarp();
+      if ((bl.mask >> lane) & 1u) {
+        const int p = __popc(bl.mask & ((1u << lane) - 1u));
+        meta[islot].ntok[p] = (uint8_t)bl.ntok;
+        meta[islot].page[p] = bl.page;
+      }
+      if (lane == 0) {
+        meta[islot].t = it.t;
+        meta[islot].h = it.h;
+        meta[islot].s = it.s;
+        meta[islot].nblk = __popc(bl.mask);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t qbytes = (uint32_t)a.G * kHeadDim * 2;
+        mbar_arrive_expect_tx(&item_full[islot], qbytes);
+        bulk_load(qbuf + islot * qbytes,
+                  a.q + ((int64_t)it.t * a.Hq + (int64_t)it.h * a.G) * kHeadDim, qbytes,
+                  &item_full[islot]);
+      }
+      if (++islot == kItems) { islot = 0; iphase ^= 1u; }
+    }
+    if (lane == 0) {                                      // end-of-work record
+      mbar_wait(&item_empty[islot], iphase ^ 1u, ws.hdr);
+      meta[islot].t = -1;
+      mbar_arrive(&item_full[islot]);
+    }
+    return;
+  }
+  if (warp == kLoader) {
+    // -------------------------------------------------------------- loader
+    // For every published item, the K and V tile of each block as 2-D TMA
+    // loads into the stage ring.  Only lane 0 works.
+    if (lane == 0) {
+      int stage = 0, islot = 0;
+      uint32_t phase = 0, iphase = 0;
+      for (;;) {
+        mbar_wait(&item_full[islot], iphase, ws.hdr);
+        if (meta[islot].t < 0) break;
+        const int nblk = meta[islot].nblk, h = meta[islot].h;
+        for (int bi = 0; bi < nblk; ++bi) {
+          const int y = (meta[islot].page[bi] * a.Hkv + h) * kBlock;
 #pragma unroll
-        for (int kind = 0; kind < 2; ++kind) {
-          if (lane == 0) {
+          for (int kind = 0; kind < 2; ++kind) {
             mbar_wait(&empty_bar[stage], phase ^ 1u, ws.hdr);
             mbar_arrive_expect_tx(&full_bar[stage], TB);
             const void* tm = kind == 0 ? (const void*)&tmap_k : (const void*)&tmap_v;
             uint8_t* dst = ring + stage * TB;
-            if (FP8) {
-              tma_load_2d(dst, tm, 0, y, &full_bar[stage]);
-            } else {
-              tma_load_2d(dst, tm, 0, y, &full_bar[stage]);
-              tma_load_2d(dst + TB / 2, tm, 64, y, &full_bar[stage]);
-            }
-          }
-          __syncwarp();
-          if (++stage == NST) {
-            stage = 0;
-            phase ^= 1u;
+            tma_load_2d(dst, tm, 0, y, &full_bar[stage]);
+            if (!FP8) tma_load_2d(dst + TB / 2, tm, 64, y, &full_bar[stage]);
+            if (++stage == NST) { stage = 0; phase ^= 1u; }
           }
         }
+        mbar_arrive(&item_empty[islot]);
+        if (++islot == kItems) { islot = 0; iphase ^= 1u; }
       }
     }
     // No drain needed: the consumers wait for every tile issued here before
@@ -196,20 +246,25 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
 
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, tq = lane & 3;
-  int stage = 0;
-  uint32_t phase = 0;
+  int stage = 0, islot = 0;
+  uint32_t phase = 0, iphase = 0;
   uint8_t* my_conv = conv + warp * kConvBytes;
-  for (int idx = blockIdx.x; idx < a.n_items; idx += gridDim.x) {
-    const Item it = item_of(ws, a, idx);
-    if (!it.active) continue;
-    const ItemBlocks bl = item_blocks(ws, a, it.t, it.h, it.s, it.r, it.pos, lane);
+  for (;;) {
+    mbar_wait(&item_full[islot], iphase, ws.hdr);
+    const int it_t = meta[islot].t;
+    if (it_t < 0) break;                                  // end-of-work record
+    const int it_h = meta[islot].h, it_s = meta[islot].s;
+    const int nblk = meta[islot].nblk;
+    const int my_ntok = lane < nblk ? meta[islot].ntok[lane] : 0;
 
-    // Q fragments: rows = the group's query heads (zero past G).  fp8: f16
-    // operands with the index dim permuted so that a thread's four K values of
-    // a k-step are one 32-bit shared load (d = 16ks + 4tq + {0,1 | 2,3}).
+    // Q fragments from the item's smem copy: rows = the group's query heads
+    // (zero past G).  fp8: f16 operands with the index dim permuted so that a
+    // thread's four K values of a k-step are one 32-bit shared load
+    // (d = 16ks + 4tq + {0,1 | 2,3}).
     uint32_t qa[8][4];
     {
-      const __nv_bfloat16* qb = a.q + ((int64_t)it.t * a.Hq + (int64_t)it.h * a.G) * kHeadDim;
+      const __nv_bfloat16* qb =
+          reinterpret_cast<const __nv_bfloat16*>(qbuf + islot * a.G * kHeadDim * 2);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
@@ -229,17 +284,17 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&item_empty[islot]);       // Q and metadata are in registers
+    if (++islot == kItems) { islot = 0; iphase ^= 1u; }
     float acc[16][4];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     float m_r[2] = {-INFINITY, -INFINITY};   // running max (log2 domain), rows g, g+8
     float l_r[2] = {0.f, 0.f};
 
-    unsigned m = bl.mask;
-    while (m) {
-      const int L = __ffs(m) - 1;
-      m &= m - 1;
-      const int ntok = __shfl_sync(0xffffffffu, bl.ntok, L);
+    for (int bi = 0; bi < nblk; ++bi) {
+      const int ntok = __shfl_sync(0xffffffffu, my_ntok, bi);
       // ---------------- K tile: S = Q K^T for this warp's 32 tokens
       mbar_wait(&full_bar[stage], phase, ws.hdr);
       const uint8_t* kt = ring + stage * TB;
@@ -412,10 +467,10 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
       for (int i = 0; i < 2; ++i) {
         const int row = g + 8 * i;
         if (row >= a.G) continue;
-        const int64_t hq = (int64_t)it.t * a.Hq + (int64_t)it.h * a.G + row;
+        const int64_t hq = (int64_t)it_t * a.Hq + (int64_t)it_h * a.G + row;
         const bool empty = !(Ltot[i] > 0.f);
         const float sc = empty ? 0.f : a.v_scale / Ltot[i];
-        float* dst = static_cast<float*>(ws.o_part) + (hq * a.nsplit + it.s) * kHeadDim;
+        float* dst = static_cast<float*>(ws.o_part) + (hq * a.nsplit + it_s) * kHeadDim;
 #pragma unroll
         for (int nd = 0; nd < 16; ++nd) {
           float x0 = acc[nd][2 * i] * fw[i], x1 = acc[nd][2 * i + 1] * fw[i];
@@ -429,7 +484,7 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
           *reinterpret_cast<float2*>(dst + nd * 8 + 2 * tq) = make_float2(x0 * sc, x1 * sc);
         }
         if (tq == 0)
-          ws.lse_part[hq * a.nsplit + it.s] = empty ? -INFINITY : (Mx[i] + log2f(Ltot[i])) * kLn2;
+          ws.lse_part[hq * a.nsplit + it_s] = empty ? -INFINITY : (Mx[i] + log2f(Ltot[i])) * kLn2;
       }
     }
   }
@@ -491,7 +546,8 @@ template <bool FP8>
 size_t decode_smem(int G) {
   const size_t ring = FP8 ? (size_t)kFp8Stages * kFp8TileBytes : (size_t)kStages * kTileBytes;
   const size_t conv = FP8 ? (size_t)kConsumers * kConvBytes : 0;
-  return ring + conv + (size_t)(kConsumers - 1) * G * kHeadDim * 4;
+  return ring + conv + (size_t)kItems * G * kHeadDim * 2 +
+         (size_t)(kConsumers - 1) * G * kHeadDim * 4;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
