@@ -550,40 +550,6 @@ size_t decode_smem(int G) {
          (size_t)(kConsumers - 1) * G * kHeadDim * 4;
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static std::once_flag once;
-  static EncodeTiledFn fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// Tensor map of a KV pool viewed as [num_pages * H_kv * 128 rows, 128 columns]:
-// bf16 -> boxes of 64 columns x 128 rows, e4m3 -> 128 x 128, 128-byte swizzle.
-bool make_pool_map(CUtensorMap* m, const void* base, int64_t rows, bool fp8) {
-  EncodeTiledFn enc = encode_fn();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * (fp8 ? 1 : 2)};
-  const cuuint32_t box[2] = {fp8 ? 128u : 64u, (cuuint32_t)kBlock};
-  const cuuint32_t estr[2] = {1u, 1u};
-  return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <bool FP8>
 msa_status launch_decode(const WsView& v, const DecodeArgs& a, const CUtensorMap& tk,
                          const CUtensorMap& tv, cudaStream_t s) {

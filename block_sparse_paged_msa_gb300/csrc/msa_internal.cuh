@@ -2,6 +2,7 @@
 // argument checks and small device helpers.  Not part of the ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -62,7 +63,7 @@ inline int64_t csr_rows_of(const msa_config& c) {
 // Byte offsets of every workspace region.
 struct WsLayout {
   size_t plan_err, req_seq_len, req_nb, req_cu_nb, req_qstart, tok_req, tok_pos, block_table;
-  size_t o_part, lse_part, total;
+  size_t sched, csr_slot, o_part, lse_part, total;
 };
 
 inline WsLayout layout_of(const msa_config& c) {
@@ -78,6 +79,8 @@ inline WsLayout layout_of(const msa_config& c) {
   L.tok_req = o;     o = align_up(o + 4 * T);
   L.tok_pos = o;     o = align_up(o + 4 * T);
   L.block_table = o; o = align_up(o + 4 * B * (size_t)c.max_blocks_per_req);
+  L.sched = o;       o = align_up(o + (is_prefill(c) ? 4 * (size_t)(csr_rows_of(c) + 1) : 0));
+  L.csr_slot = o;    o = align_up(o + (is_prefill(c) ? 2 * T * (size_t)c.num_kv_heads * width_of(c) : 0));
   L.o_part = o;      o = align_up(o + part_elem_bytes(c) * T * Hq * NS * kHeadDim);
   L.lse_part = o;    o = align_up(o + 4 * T * Hq * NS);
   L.total = o;
@@ -95,6 +98,9 @@ struct WsView {
   int32_t* tok_req;
   int32_t* tok_pos;
   int32_t* block_table;   // [max_batch, max_blocks_per_req], -1 = invalid
+  int32_t* sched;         // prefill: [csr rows + 1] first work item of each CSR row
+  int16_t* csr_slot;      // prefill: per CSR entry, the slot of the row's block in the
+                          // token's selected list
   void* o_part;           // [T, H_q, NS, D] fp32 (decode) | fp16 (prefill)
   float* lse_part;        // [T, H_q, NS]
 };
@@ -112,12 +118,17 @@ inline WsView view_of(const msa_config& c, const void* ws) {
   v.tok_req = (int32_t*)(b + L.tok_req);
   v.tok_pos = (int32_t*)(b + L.tok_pos);
   v.block_table = (int32_t*)(b + L.block_table);
+  v.sched = (int32_t*)(b + L.sched);
+  v.csr_slot = (int16_t*)(b + L.csr_slot);
   v.o_part = (void*)(b + L.o_part);
   v.lse_part = (float*)(b + L.lse_part);
   return v;
 }
 
 msa_status check_config(const msa_config* c);
+// Tensor map of a KV pool viewed as [num_pages * H_kv * 128 rows, 128 columns]:
+// bf16 -> boxes of 64 columns x 128 rows, e4m3 -> 128 x 128, 128-byte swizzle.
+bool make_pool_map(CUtensorMap* m, const void* base, int64_t rows, bool fp8);
 // Index scores of a prefill chunk (tensor-core tiles; prefill.cu).
 msa_status prefill_index_score(const msa_config& c, const WsView& v, const void* idx_q,
                                const void* idx_k, float* scores, cudaStream_t s);

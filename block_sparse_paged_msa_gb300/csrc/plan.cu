@@ -8,6 +8,8 @@
 // MiniMaxM3SparseMSAMetadataBuilder.build hands block_table, seq_lens and
 // decode_query_len to the decode kernel.  Here everything is derived on the
 // device into a fixed-shape workspace so that a captured graph can replay it.
+#include <cuda.h>
+
 #include <mutex>
 #include <vector>
 
@@ -19,13 +21,18 @@ int32_t blocks_per_split_of(const msa_config& c) {
   const int32_t S = width_of(c);
   if (S <= 0) return 1;
   if (c.blocks_per_split > 0) return c.blocks_per_split < S ? c.blocks_per_split : S;
-  // Aim for about 2048 split-K work items per step (several waves of two CTAs
-  // per SM), never fewer than one block per split.
+  // The decode kernel is persistent (two CTAs per SM) and streams across item
+  // boundaries, so items only need to outnumber the CTAs: aim for about 512
+  // (fewer, longer items mean fewer partials to merge; measured flat from 2
+  // to 20 blocks per item on the medium decode workload), at most 32 blocks
+  // per item (one warp lists an item's blocks).
   const int64_t items = (int64_t)max_tokens_of(c) * c.num_kv_heads;
-  int64_t ns = items > 0 ? (2048 + items - 1) / items : 1;
+  int64_t ns = items > 0 ? (512 + items - 1) / items : 1;
   if (ns < 1) ns = 1;
   if (ns > S) ns = S;
-  return (int32_t)((S + ns - 1) / ns);
+  int32_t bps = (int32_t)((S + ns - 1) / ns);
+  if (bps > 32) bps = (S + (S + 31) / 32 - 1) / ((S + 31) / 32);
+  return bps;
 }
 
 msa_status check_config(const msa_config* c) {
@@ -50,6 +57,38 @@ msa_status check_config(const msa_config* c) {
     return MSA_ERR_UNSUPPORTED;
   if ((int64_t)max_tokens_of(*c) * c->num_q_heads > (int64_t)1 << 30) return MSA_ERR_UNSUPPORTED;
   return MSA_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool make_pool_map(CUtensorMap* m, const void* base, int64_t rows, bool fp8) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * (fp8 ? 1 : 2)};
+  const cuuint32_t box[2] = {fp8 ? 128u : 64u, (cuuint32_t)kBlock};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int sm_count() {

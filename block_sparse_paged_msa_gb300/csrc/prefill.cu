@@ -20,15 +20,18 @@
 //    ascending selected list (binary search); ballots give the count (first
 //    pass) and the ordered positions (second pass), so every row lists its
 //    tokens ascending and the structure is deterministic.
-//  * prefill_attn_kernel: one CTA per CSR row keeps the block's K and V tiles
-//    (64 KiB) in shared memory and streams the row's tokens through it, 16
-//    rows (tokens x GQA heads) per warp: S = Q K^T (bf16), causal mask, softmax
-//    over the block's 128 keys, O = P V (fp16: P keeps 11 significant bits; the
-//    V tile is converted once per CTA), then a normalised fp16 partial and its
-//    LSE per (token, query head, slot).  msa_combine merges the slots.
+//  * prefill_tc_kernel (msa_sparse_prefill): fifth-generation tensor cores.
+//    A persistent CTA per SM walks work items of up to 16 M-tiles of one CSR
+//    row; per row the K and V tiles arrive by TMA and V is transposed once to
+//    fp16.  M-tiles of 128 rows (tokens x GQA heads) alternate between two
+//    softmax warpgroups: one thread issues tcgen05.mma for S = Q K^T (bf16)
+//    and O = P V (fp16) with fp32 accumulators in TMEM; each warpgroup thread
+//    owns one row (tcgen05.ld), applies the causal mask, the softmax, and
+//    writes the normalised fp16 partial and its LSE per (token, query head,
+//    slot).  msa_combine merges the slots.
 #include <mutex>
 
-#include "msa_device.cuh"
+#include "tcgen05.cuh"
 
 namespace msa {
 namespace {
@@ -153,13 +156,14 @@ prefill_score_kernel(WsView ws, int Hkv, int max_blocks, const __nv_bfloat16* __
 }
 
 // ------------------------------------------------------------ CSR
-__device__ __forceinline__ bool has_block(const int32_t* sel, int n, int j) {
-  int lo = 0, hi = n;            // sel[0..n) ascending
+// Slot of block j in the ascending list sel[0..n), or -1.
+__device__ __forceinline__ int find_block(const int32_t* sel, int n, int j) {
+  int lo = 0, hi = n;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
     if (sel[mid] < j) lo = mid + 1; else hi = mid;
   }
-  return lo < n && sel[lo] == j;
+  return lo < n && sel[lo] == j ? lo : -1;
 }
 
 template <bool FILL>
@@ -180,16 +184,21 @@ csr_rows_kernel(WsView ws, int Hkv, int B, int NB, int S, const int32_t* __restr
     const int qs = ws.req_qstart[r], qe = ws.req_qstart[r + 1];
     for (int t0 = qs; t0 < qe; t0 += 32) {
       const int t = t0 + lane;
-      bool in = false;
+      int slot = -1;
       if (t < qe && ws.tok_req[t] == r) {
         const int p = ws.tok_pos[t];
         if (j * kBlock <= p) {
           const int n = min(p / kBlock + 1, S);
-          in = has_block(selected + ((int64_t)t * Hkv + h) * S, n, j);
+          slot = find_block(selected + ((int64_t)t * Hkv + h) * S, n, j);
         }
       }
+      const bool in = slot >= 0;
       const unsigned bal = __ballot_sync(0xffffffffu, in);
-      if (FILL && in) q_idx[base + count + __popc(bal & ((1u << lane) - 1u))] = t;
+      if (FILL && in) {
+        const int e = base + count + __popc(bal & ((1u << lane) - 1u));
+        q_idx[e] = t;
+        ws.csr_slot[e] = (int16_t)slot;
+      }
       count += __popc(bal);
     }
   }
@@ -228,180 +237,327 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(int32_t* __restrict__ ro
 }
 
 // ------------------------------------------------------------ attention
-constexpr int kPfThreads = 256;
+// Work items: a CSR row's tokens in chunks of kTilesPerItem M-tiles of 128
+// rows (tokens x GQA heads); msa_build_k2q_csr writes the first item of every
+// row (ws.sched), so the huge rows of the init / local blocks are split
+// instead of dominating the tail.
+constexpr int kTilesPerItem = 16;
+constexpr int kTcThreads = 9 * 32;       // 2 softmax warpgroups + 1 MMA-issuer warp
 constexpr int kTileBytes = kBlock * kHeadDim * 2;
 
 struct PrefillArgs {
   int Hkv, Hq, G, S, B, NB;
   float scale_log2;
   const __nv_bfloat16* q;
-  const uint8_t* k;
-  const uint8_t* v;
-  const int32_t* selected;
   const int32_t* row_ptr;
   const int32_t* q_idx;
 };
 
-__device__ __forceinline__ int slot_of(const int32_t* sel, int n, int j) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (sel[mid] < j) lo = mid + 1; else hi = mid;
+// 32 fp32 accumulator columns -> 32 normalised fp16 values (four 16-byte stores).
+__device__ __forceinline__ void store_row_chunk(uint4* dst, const uint32_t (&r)[32], float inv) {
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    uint32_t o4[4];
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2)
+      o4[e2] = pack_f16(__uint_as_float(r[q4 * 8 + 2 * e2]) * inv,
+                        __uint_as_float(r[q4 * 8 + 2 * e2 + 1]) * inv);
+    dst[q4] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
   }
-  return lo;
 }
 
-__global__ void __launch_bounds__(kPfThreads, 1)
-prefill_attn_kernel(WsView ws, PrefillArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];   // K tile, V tile
+// Persistent: one CTA per SM walks the work items.  Per CSR row (KV head h,
+// request r, key block j) the K tile and the V tile arrive by TMA; V is
+// transposed once into an fp16 K-major tile (V^T) so that both MMAs read
+// K-major operands.  M-tiles alternate between the two softmax warpgroups:
+//   issuer:  S_t = Q_t K^T   (bf16, fp32 accumulator in TMEM)
+//   WG:      S_t -> registers (thread = row), causal mask, softmax, P_t (fp16)
+//   issuer:  O_t = P_t V     (fp16, fp32 accumulator in TMEM)
+//   WG:      O_t -> normalised fp16 partial + LSE per (token, query head, slot)
+// The issuer orders S0 S1 | PV0 PV1 S2 S3 | PV2 PV3 S4 S5 ..., so one
+// warpgroup's softmax overlaps the other's MMAs.  Each thread copies its own
+// Q row for its warpgroup's next tile as soon as the tensor core has read the
+// current one, with the row's (token, position, slot) fetched two tiles ahead.
+__global__ void __launch_bounds__(kTcThreads, 1)
+prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v, int64_t rows) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* Kt = smem;                          // K tile, bf16, K-major SW128 [key][d]
+  uint8_t* VT = smem + kTileBytes;             // V^T, fp16, K-major SW128 [d][key]
+  uint8_t* Pb = smem + 2 * kTileBytes;         // P[2], fp16 [row][key]
+  uint8_t* Vst = Pb + kTileBytes;              // V staging (bf16 [key][d]) = P[1]
+  uint8_t* Qb = smem + 4 * kTileBytes;         // Q[2], bf16 [row][d]
+  __shared__ __align__(8) uint64_t kv_full, q_ready[2], s_ready[2], p_ready[2], o_ready[2];
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool issuer = warp == 8;
+  const int wg = warp >> 2;                    // softmax warpgroup (0, 1)
+  const int wtid = tid & 127;                  // = this thread's row / TMEM lane
+  if (tid == 0) {
+    mbar_init(&kv_full, 1);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&q_ready[w], 128);
+      mbar_init(&s_ready[w], 1);
+      mbar_init(&p_ready[w], 128);
+      mbar_init(&o_ready[w], 1);
+    }
+    fence_barrier_init();
+  }
+  if (issuer) {
+    tmem_alloc(&tmem_base, 512);               // S and O for each warpgroup
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
   griddep_launch_dependents();
   griddep_wait();
-  const int64_t row = blockIdx.x;
-  const int j = (int)(row % a.NB);
-  const int r = (int)((row / a.NB) % a.B);
-  const int h = (int)(row / ((int64_t)a.NB * a.B));
-  const int beg = a.row_ptr[row], end = a.row_ptr[row + 1];
-  if (beg >= end) return;
-  const int page = ws.block_table[(int64_t)r * a.NB + j];
-  if (page < 0) return;
-  const int ntok = min(kBlock, ws.req_seq_len[r] - j * kBlock);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, tq = lane & 3;
-  {
-    const uint32_t dst = smem_u32(smem);
-#pragma unroll
-    for (int kind = 0; kind < 2; ++kind) {
-      const uint8_t* src = (kind == 0 ? a.k : a.v) +
-                           ((int64_t)page * a.Hkv + h) * (int64_t)kTileBytes;
-#pragma unroll
-      for (int k = 0; k < kBlock * 16 / kPfThreads; ++k) {
-        const int idx = k * kPfThreads + tid;
-        const int rr = idx >> 4, c = idx & 15;
-        const bool ok = rr < ntok;
-        cp_async16(dst + kind * kTileBytes + swz(rr, c), src + (ok ? rr * 256 + c * 16 : 0),
-                   ok ? 16 : 0);
+
+  const int G = a.G, TPT = kBlock / G;         // tokens per M-tile
+  const int tok_per_item = kTilesPerItem * TPT;
+  const int n_items = ws.sched[rows];
+  const uint32_t idesc_s = idesc_f16(1, 128, 128), idesc_o = idesc_f16(0, 128, 128);
+  uint32_t kv_phase = 0, qpar[2] = {0, 0}, ppar[2] = {0, 0};   // issuer-side parities
+  uint32_t spar = 0, opar = 0;                                  // warpgroup-side parities
+  int cur_row = -1;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    int lo = 0, hi = (int)rows - 1;            // row of this item
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ws.sched[mid] <= item) lo = mid; else hi = mid - 1;
+    }
+    const int row = lo, chunk = item - ws.sched[row];
+    const int j = row % a.NB, r = (row / a.NB) % a.B, h = row / (a.NB * a.B);
+    const int beg = a.row_ptr[row] + chunk * tok_per_item;
+    const int end = min(a.row_ptr[row + 1], beg + tok_per_item);
+    const int page = ws.block_table[(int64_t)r * a.NB + j];
+    if (page < 0 || beg >= end) continue;      // flagged by the plan (uniform)
+    const int ntok = min(kBlock, ws.req_seq_len[r] - j * kBlock);
+    const int ntiles = (end - beg + TPT - 1) / TPT;
+
+    named_bar_sync(1, kTcThreads);             // the previous item's MMAs and reads are done
+    if (row != cur_row) {
+      if (issuer && lane == 0) {
+        const int y = (page * a.Hkv + h) * kBlock;
+        mbar_arrive_expect_tx(&kv_full, 2 * kTileBytes);
+        tma_load_2d(Kt, &tmap_k, 0, y, &kv_full);
+        tma_load_2d(Kt + kTileBytes / 2, &tmap_k, 64, y, &kv_full);
+        tma_load_2d(Vst, &tmap_v, 0, y, &kv_full);
+        tma_load_2d(Vst + kTileBytes / 2, &tmap_v, 64, y, &kv_full);
       }
+      mbar_wait(&kv_full, kv_phase, ws.hdr);
+      kv_phase ^= 1u;
+      if (!issuer) {
+        // V [key][d] bf16 -> V^T [d][key] fp16 (keys past the last visible
+        // token become 0, whatever the page holds there)
+        const uint32_t vs = smem_u32(Vst);
+        for (int b = warp * 8; b < warp * 8 + 8; ++b) {
+          const int kc = b >> 2, dc4 = (b & 3) * 4;
+          uint32_t m0, m1, m2, m3;
+          ldsm_x4_t(vs + swz_tma(kc * 8 + (lane & 7), dc4 + (lane >> 3)), m0, m1, m2, m3);
+          const uint32_t mm[4] = {m0, m1, m2, m3};
+          const int g = lane >> 2, tq = lane & 3;
+          const int key0 = kc * 8 + 2 * tq;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            uint32_t hv = bf16x2_to_f16x2(mm[m]);
+            if (key0 >= ntok) hv &= 0xffff0000u;
+            if (key0 + 1 >= ntok) hv &= 0x0000ffffu;
+            *reinterpret_cast<uint32_t*>(VT + kmaj_off((dc4 + m) * 8 + g, kc, 128) + 4 * tq) = hv;
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(1, kTcThreads);
+      cur_row = row;
     }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-    // V to fp16 in place: P V runs as an fp16 MMA, so the probabilities keep
-    // 11 significant bits instead of bf16's 8.
-    uint4* vt = reinterpret_cast<uint4*>(smem + kTileBytes);
-    for (int i = tid; i < kTileBytes / 16; i += kPfThreads) {
-      uint4 w = vt[i];
-      w.x = bf16x2_to_f16x2(w.x); w.y = bf16x2_to_f16x2(w.y);
-      w.z = bf16x2_to_f16x2(w.z); w.w = bf16x2_to_f16x2(w.w);
-      vt[i] = w;
+
+    if (issuer) {
+      if (lane == 0) {
+        const uint32_t kts = smem_u32(Kt), vts = smem_u32(VT);
+        auto issue_s = [&](int t) {
+          const int w = t & 1;
+          mbar_wait(&q_ready[w], qpar[w], ws.hdr);
+          qpar[w] ^= 1u;
+          tc_fence_after();
+          const uint32_t qs = smem_u32(Qb + w * kTileBytes);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_f16(tbase + 256 * w, kstep_desc(qs, ks, 128), kstep_desc(kts, ks, 128), idesc_s,
+                     ks > 0);
+          umma_commit(&s_ready[w]);
+        };
+        auto issue_o = [&](int t) {
+          const int w = t & 1;
+          mbar_wait(&p_ready[w], ppar[w], ws.hdr);
+          ppar[w] ^= 1u;
+          tc_fence_after();
+          const uint32_t ps = smem_u32(Pb + w * kTileBytes);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_f16(tbase + 256 * w + 128, kstep_desc(ps, ks, 128), kstep_desc(vts, ks, 128),
+                     idesc_o, ks > 0);
+          umma_commit(&o_ready[w]);
+        };
+        issue_s(0);
+        if (ntiles > 1) issue_s(1);
+        for (int t = 0; t < ntiles; t += 2) {
+          issue_o(t);
+          if (t + 1 < ntiles) issue_o(t + 1);
+          if (t + 2 < ntiles) issue_s(t + 2);
+          if (t + 3 < ntiles) issue_s(t + 3);
+        }
+      }
+      __syncwarp();
+      continue;
     }
-    __syncthreads();
+
+    // ---------------------------------------------------- softmax warpgroups
+    const uint32_t qdst = smem_u32(Qb + wg * kTileBytes);
+    const int hq = h * G + wtid % G;
+    // Metadata of this thread's row of tile t: (token, position, slot); tok
+    // < 0 past the end of the item.  Fetched two tiles ahead, so that neither
+    // the Q copy nor the softmax waits on a dependent global load.
+    struct RowMeta { int tok, pos, slot; };
+    auto row_meta = [&](int t) {
+      RowMeta rm{-1, -1, -1};
+      const int e = beg + t * TPT + wtid / G;
+      if (t < ntiles && e < end) {
+        rm.tok = a.q_idx[e];
+        rm.slot = ws.csr_slot[e];
+      }
+      return rm;
+    };
+    auto row_pos = [&](RowMeta& rm) {
+      if (rm.tok >= 0 && rm.pos < 0) rm.pos = ws.tok_pos[rm.tok];
+    };
+    auto load_q = [&](const RowMeta& rm) {   // this thread copies its own 256-byte row
+      const __nv_bfloat16* src =
+          a.q + ((int64_t)(rm.tok < 0 ? 0 : rm.tok) * a.Hq + hq) * kHeadDim;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        cp_async16(qdst + kmaj_off(wtid, c, 128), src + c * 8, rm.tok < 0 ? 0 : 16);
+      cp_async_commit();
+    };
+    RowMeta cur = row_meta(wg), nxt = row_meta(wg + 2);
+    if (wg < ntiles) load_q(cur);
+    row_pos(cur);
+    const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + 256 * wg;
+    for (int t = wg; t < ntiles; t += 2) {
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(&q_ready[wg]);
+      const int tok = cur.tok, pos = cur.pos, slot = cur.slot;
+      const bool valid = tok >= 0;
+
+      mbar_wait(&s_ready[wg], spar, ws.hdr);
+      spar ^= 1u;
+      tc_fence_after();
+      float sv[128];
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(tlane, r0);                      // four loads, one wait
+        tmem_ld32(tlane + 32, r1);
+        tmem_ld32(tlane + 64, r2);
+        tmem_ld32(tlane + 96, r3);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          sv[i] = __uint_as_float(r0[i]);
+          sv[32 + i] = __uint_as_float(r1[i]);
+          sv[64 + i] = __uint_as_float(r2[i]);
+          sv[96 + i] = __uint_as_float(r3[i]);
+        }
+      }
+      tc_fence_before();
+      RowMeta far = row_meta(t + 4);               // loads in flight for two tiles
+      if (t + 2 < ntiles) load_q(nxt);             // Q[wg] was consumed by S_t
+      row_pos(nxt);
+      // causal mask (only the diagonal / last block needs one), softmax in
+      // the exp2 domain with the scale folded into one FMA, P in fp16.
+      const int lim = valid ? min(ntok, pos - j * kBlock + 1) : 0;
+      if (lim < 128) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) sv[i] = i < lim ? sv[i] : -INFINITY;
+      }
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = sv[k];
+#pragma unroll
+      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], mx[k + 4]);
+      const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));   // raw scores
+      const float msc = m == -INFINITY ? 0.f : m * a.scale_log2;
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint8_t* prow = Pb + wg * kTileBytes;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const float p0 = ex2_approx(fmaf(sv[c * 8 + 2 * e2], a.scale_log2, -msc));
+          const float p1 = ex2_approx(fmaf(sv[c * 8 + 2 * e2 + 1], a.scale_log2, -msc));
+          ls[(c & 3) * 2] += p0;
+          ls[(c & 3) * 2 + 1] += p1;
+          pk[e2] = pack_f16(p0, p1);
+        }
+        *reinterpret_cast<uint4*>(prow + kmaj_off(wtid, c, 128)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      const float l = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_ready[wg]);
+
+      mbar_wait(&o_ready[wg], opar, ws.hdr);
+      opar ^= 1u;
+      tc_fence_after();
+      // tcgen05.ld is warp-collective: every lane loads, only valid rows store
+      const bool store = valid && l > 0.f && slot >= 0;
+      const int64_t pi = store ? ((int64_t)tok * a.Hq + hq) * a.S + slot : 0;
+      uint4* op = reinterpret_cast<uint4*>(static_cast<__half*>(ws.o_part) + pi * kHeadDim);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(tlane + 128, r0);
+        tmem_ld32(tlane + 160, r1);
+        tmem_ld32(tlane + 192, r2);
+        tmem_ld32(tlane + 224, r3);
+        tmem_ld_wait();
+        tc_fence_before();
+        if (store) {
+          store_row_chunk(op, r0, inv);
+          store_row_chunk(op + 4, r1, inv);
+          store_row_chunk(op + 8, r2, inv);
+          store_row_chunk(op + 12, r3, inv);
+          ws.lse_part[pi] = (msc + log2f(l)) * kLn2;
+        }
+      }
+      cur = nxt;
+      nxt = far;
+    }
   }
-  const uint32_t ktile = smem_u32(smem), vtile = ktile + kTileBytes;
-  const int TPW = kMaxGroup / a.G;                 // tokens per warp per pass
-  const int lt0 = warp * TPW + g / a.G, lt1 = warp * TPW + (g + 8) / a.G;
-  const int hg0 = g % a.G, hg1 = (g + 8) % a.G;
-  for (int base = beg; base < end; base += 8 * TPW) {
-    const int i0 = base + lt0, i1 = base + lt1;
-    const bool v0 = i0 < end, v1 = i1 < end;
-    const int t_0 = v0 ? a.q_idx[i0] : 0, t_1 = v1 ? a.q_idx[i1] : 0;
-    const int p0 = v0 ? ws.tok_pos[t_0] : -1, p1 = v1 ? ws.tok_pos[t_1] : -1;
-    uint32_t qa[8][4];
-    {
-      const __nv_bfloat16* q0 = a.q + ((int64_t)t_0 * a.Hq + h * a.G + hg0) * kHeadDim;
-      const __nv_bfloat16* q1 = a.q + ((int64_t)t_1 * a.Hq + h * a.G + hg1) * kHeadDim;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int c0 = ks * 16 + 2 * tq, c1 = c0 + 8;
-        qa[ks][0] = v0 ? ld_u32(q0 + c0) : 0u;
-        qa[ks][1] = v1 ? ld_u32(q1 + c0) : 0u;
-        qa[ks][2] = v0 ? ld_u32(q0 + c1) : 0u;
-        qa[ks][3] = v1 ? ld_u32(q1 + c1) : 0u;
-      }
-    }
-    float sc[16][4];
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-      const int krow = nt * 8 + (lane & 7);
-#pragma unroll
-      for (int ks = 0; ks < 8; ks += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(ktile + swz(krow, 2 * ks + (lane >> 3)), b0, b1, b2, b3);
-        mma_bf16(sc[nt], qa[ks], b0, b1);
-        mma_bf16(sc[nt], qa[ks + 1], b2, b3);
-      }
-    }
-    float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = nt * 8 + 2 * tq + (e & 1);
-        const int p = e < 2 ? p0 : p1;
-        const bool ok = key < ntok && j * kBlock + key <= p;
-        sc[nt][e] = ok ? sc[nt][e] * a.scale_log2 : -INFINITY;
-        if (e < 2) m0 = fmaxf(m0, sc[nt][e]); else m1 = fmaxf(m1, sc[nt][e]);
-      }
-    }
-    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
-    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
-    const float mr0 = m0 == -INFINITY ? 0.f : m0, mr1 = m1 == -INFINITY ? 0.f : m1;
-    float l0 = 0.f, l1 = 0.f;
-    uint32_t pa[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const __half2 h01 = __floats2half2_rn(exp2f(sc[nt][0] - mr0), exp2f(sc[nt][1] - mr0));
-      const __half2 h23 = __floats2half2_rn(exp2f(sc[nt][2] - mr1), exp2f(sc[nt][3] - mr1));
-      const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-      l0 += f01.x + f01.y;            // normalise by the probabilities actually used
-      l1 += f23.x + f23.y;
-      pa[nt >> 1][(nt & 1) * 2 + 0] = *reinterpret_cast<const uint32_t*>(&h01);
-      pa[nt >> 1][(nt & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
-    }
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    float o[16][4];
-#pragma unroll
-    for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int vrow = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-#pragma unroll
-      for (int nd = 0; nd < 16; nd += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vtile + swz(vrow, nd + (lane >> 4)), b0, b1, b2, b3);
-        mma_f16(o[nd], pa[kk], b0, b1);
-        mma_f16(o[nd + 1], pa[kk], b2, b3);
-      }
-    }
-    // normalised fp16 partial + LSE for (token, head, slot of j)
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const bool ok = half == 0 ? v0 : v1;
-      if (!ok) continue;
-      const int t = half == 0 ? t_0 : t_1;
-      const int p = half == 0 ? p0 : p1;
-      const int hq = h * a.G + (half == 0 ? hg0 : hg1);
-      const float l = half == 0 ? l0 : l1;
-      const float m = half == 0 ? m0 : m1;
-      const int nsel = min(p / kBlock + 1, a.S);
-      const int slot = slot_of(a.selected + ((int64_t)t * a.Hkv + h) * a.S, nsel, j);
-      if (slot >= nsel) continue;                  // j not selected: cannot happen for a CSR entry
-      const int64_t pi = ((int64_t)t * a.Hq + hq) * a.S + slot;
-      __half* op = static_cast<__half*>(ws.o_part) + pi * kHeadDim;
-      const float inv = 1.f / l;
-#pragma unroll
-      for (int nd = 0; nd < 16; ++nd) {
-        const float x0 = o[nd][half * 2] * inv, x1 = o[nd][half * 2 + 1] * inv;
-        *reinterpret_cast<uint32_t*>(op + nd * 8 + 2 * tq) = pack_f16(x0, x1);
-      }
-      if (tq == 0) ws.lse_part[pi] = (m + log2f(l)) * kLn2;
-    }
+  tc_fence_before();
+  __syncthreads();
+  if (issuer) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
   }
+}
+
+// First work item of every CSR row: ceil(row size / tokens per item), scanned.
+__global__ void __launch_bounds__(256)
+sched_count_kernel(const int32_t* __restrict__ row_ptr, int32_t* __restrict__ sched, int64_t rows,
+                   int tok_per_item) {
+  griddep_launch_dependents();
+  griddep_wait();
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < rows; i += (int64_t)gridDim.x * 256) {
+    const int n = row_ptr[i + 1] - row_ptr[i];
+    sched[i + 1] = (n + tok_per_item - 1) / tok_per_item;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) sched[0] = 0;
 }
 
 template <typename K>
@@ -467,8 +623,18 @@ extern "C" msa_status msa_build_k2q_csr(const msa_config* cfg, const void* ws,
     return st;
   if ((st = launch_pdl(csr_scan_kernel, dim3(1), dim3(1024), 0, s, row_ptr, rows)) != MSA_OK)
     return st;
-  return launch_pdl(csr_rows_kernel<true>, dim3(grid), dim3(256), 0, s, v, cfg->num_kv_heads,
-                    cfg->max_batch, cfg->max_blocks_per_req, S, selected, row_ptr, q_indices);
+  if ((st = launch_pdl(csr_rows_kernel<true>, dim3(grid), dim3(256), 0, s, v, cfg->num_kv_heads,
+                       cfg->max_batch, cfg->max_blocks_per_req, S, selected, row_ptr,
+                       q_indices)) != MSA_OK)
+    return st;
+  // work schedule of msa_sparse_prefill: items of up to 16 M-tiles per row
+  const int G = cfg->num_q_heads / cfg->num_kv_heads;
+  const int tok_per_item = kTilesPerItem * (kBlock / G);
+  const unsigned sgrid = (unsigned)((rows + 255) / 256 < 1024 ? (rows + 255) / 256 : 1024);
+  if ((st = launch_pdl(sched_count_kernel, dim3(sgrid), dim3(256), 0, s, (const int32_t*)row_ptr,
+                       v.sched, rows, tok_per_item)) != MSA_OK)
+    return st;
+  return launch_pdl(csr_scan_kernel, dim3(1), dim3(1024), 0, s, v.sched, rows);
 }
 
 extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const void* q,
@@ -493,13 +659,18 @@ extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const 
   a.NB = cfg->max_blocks_per_req;
   a.scale_log2 = cfg->softmax_scale * kLog2e;
   a.q = (const __nv_bfloat16*)q;
-  a.k = (const uint8_t*)k_pages;
-  a.v = (const uint8_t*)v_pages;
-  a.selected = selected;
   a.row_ptr = row_ptr;
   a.q_idx = q_indices;
-  const size_t smem = 2u * kTileBytes;
-  if ((st = set_smem(prefill_attn_kernel, smem)) != MSA_OK) return st;
-  return launch_pdl(prefill_attn_kernel, dim3((unsigned)rows), dim3(kPfThreads), smem,
-                    (cudaStream_t)stream, view_of(*cfg, ws), a);
+  (void)selected;   // the CSR build recorded each entry's slot in ws
+  const int64_t prow = (int64_t)cfg->num_pages * a.Hkv * kBlock;
+  if (prow > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
+  CUtensorMap tk, tv;
+  if (!make_pool_map(&tk, k_pages, prow, false) || !make_pool_map(&tv, v_pages, prow, false))
+    return MSA_ERR_CUDA;
+  const size_t smem = 6u * kTileBytes;
+  if ((st = set_smem(prefill_tc_kernel, smem)) != MSA_OK) return st;
+  const int grid = sm_count();
+  if (grid <= 0) return MSA_ERR_CUDA;
+  return launch_pdl(prefill_tc_kernel, dim3(grid), dim3(kTcThreads), smem, (cudaStream_t)stream,
+                    view_of(*cfg, ws), a, tk, tv, rows);
 }
