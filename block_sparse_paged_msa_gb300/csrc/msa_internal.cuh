@@ -126,9 +126,11 @@ inline WsView view_of(const msa_config& c, const void* ws) {
 }
 
 msa_status check_config(const msa_config* c);
-// Tensor map of a KV pool viewed as [num_pages * H_kv * 128 rows, 128 columns]:
-// bf16 -> boxes of 64 columns x 128 rows, e4m3 -> 128 x 128, 128-byte swizzle.
-bool make_pool_map(CUtensorMap* m, const void* base, int64_t rows, bool fp8);
+// Tensor map of a row-major [rows, 128 columns] array (a KV pool viewed as
+// num_pages * H_kv * 128 rows, or the queries as tokens * H_q rows): bf16 ->
+// boxes of 64 columns x box_rows, e4m3 -> 128 x box_rows, 128-byte swizzle.
+bool make_pool_map(CUtensorMap* m, const void* base, int64_t rows, bool fp8,
+                   int box_rows = kBlock);
 // Index scores of a prefill chunk (tensor-core tiles; prefill.cu).
 msa_status prefill_index_score(const msa_config& c, const WsView& v, const void* idx_q,
                                const void* idx_k, float* scores, cudaStream_t s);

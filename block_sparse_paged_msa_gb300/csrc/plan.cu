@@ -78,12 +78,12 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool make_pool_map(CUtensorMap* m, const void* base, int64_t rows, bool fp8) {
+bool make_pool_map(CUtensorMap* m, const void* base, int64_t rows, bool fp8, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * (fp8 ? 1 : 2)};
-  const cuuint32_t box[2] = {fp8 ? 128u : 64u, (cuuint32_t)kBlock};
+  const cuuint32_t box[2] = {fp8 ? 128u : 64u, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1u, 1u};
   return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

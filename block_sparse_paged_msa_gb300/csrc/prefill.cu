@@ -242,8 +242,14 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(int32_t* __restrict__ ro
 // row (ws.sched), so the huge rows of the init / local blocks are split
 // instead of dominating the tail.
 constexpr int kTilesPerItem = 16;
-constexpr int kTcThreads = 9 * 32;       // 2 softmax warpgroups + 1 MMA-issuer warp
+constexpr int kTcThreads = 10 * 32;      // 2 softmax warpgroups, MMA issuer, Q loader
 constexpr int kTileBytes = kBlock * kHeadDim * 2;
+// A P tile doubles as the output staging area: 128 rows of 256 bytes at a
+// 272-byte stride, so that the 16-byte stores of 8 consecutive rows fall in 8
+// different bank groups.
+constexpr int kStageStride = 272;
+constexpr int kPBytes = kBlock * kStageStride;          // 34 KB, a multiple of 1 KB
+constexpr int kTcSmemBytes = 4 * kTileBytes + 2 * kPBytes + 1024;
 
 struct PrefillArgs {
   int Hkv, Hq, G, S, B, NB;
@@ -253,50 +259,47 @@ struct PrefillArgs {
   const int32_t* q_idx;
 };
 
-// 32 fp32 accumulator columns -> 32 normalised fp16 values (four 16-byte stores).
-__device__ __forceinline__ void store_row_chunk(uint4* dst, const uint32_t (&r)[32], float inv) {
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
-    uint32_t o4[4];
-#pragma unroll
-    for (int e2 = 0; e2 < 4; ++e2)
-      o4[e2] = pack_f16(__uint_as_float(r[q4 * 8 + 2 * e2]) * inv,
-                        __uint_as_float(r[q4 * 8 + 2 * e2 + 1]) * inv);
-    dst[q4] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-  }
-}
-
 // Persistent: one CTA per SM walks the work items.  Per CSR row (KV head h,
 // request r, key block j) the K tile and the V tile arrive by TMA; V is
 // transposed once into an fp16 K-major tile (V^T) so that both MMAs read
-// K-major operands.  M-tiles alternate between the two softmax warpgroups:
-//   issuer:  S_t = Q_t K^T   (bf16, fp32 accumulator in TMEM)
-//   WG:      S_t -> registers (thread = row), causal mask, softmax, P_t (fp16)
-//   issuer:  O_t = P_t V     (fp16, fp32 accumulator in TMEM)
-//   WG:      O_t -> normalised fp16 partial + LSE per (token, query head, slot)
-// The issuer orders S0 S1 | PV0 PV1 S2 S3 | PV2 PV3 S4 S5 ..., so one
-// warpgroup's softmax overlaps the other's MMAs.  Each thread copies its own
-// Q row for its warpgroup's next tile as soon as the tensor core has read the
-// current one, with the row's (token, position, slot) fetched two tiles ahead.
+// K-major operands.  M-tiles alternate between the two softmax warpgroups;
+// warpgroup w's k-th tile (counted over the whole kernel) goes through
+//   loader:  Q_k rows -> Q[w]        once S_{k-1} has read Q[w]      (q_full)
+//   issuer:  S_k = Q_k K^T (bf16)    once Q_k landed, S_{k-1} read   (s_ready)
+//   WG:      S_k -> registers (thread = row)                        (s_free)
+//            causal mask, softmax, P_k (fp16) -> P[w]                (p_ready)
+//   issuer:  O_k = P_k V (fp16)                                      (o_ready)
+//   WG:      O_k -> normalised fp16 row -> P[w] (row-major) -> one 256-byte
+//            bulk store per row into the partials, LSE beside it.
+// Accumulators live in TMEM (S and O per warpgroup, 512 columns).  The
+// issuer polls both warpgroups and serves whichever is ready, so S_{k+1}
+// already runs while warpgroup w is still in the softmax of tile k, and the
+// two warpgroups drift out of phase.
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
-                  const __grid_constant__ CUtensorMap tmap_v, int64_t rows) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+                  const __grid_constant__ CUtensorMap tmap_v,
+                  const __grid_constant__ CUtensorMap tmap_q, int64_t rows) {
+  extern __shared__ __align__(16) uint8_t tc_smem_raw[];
+  // swizzled operand tiles want 1 KB alignment: round the base up (the
+  // launch asks for 1 KB of slack)
+  uint8_t* smem = tc_smem_raw + ((1024u - (smem_u32(tc_smem_raw) & 1023u)) & 1023u);
   uint8_t* Kt = smem;                          // K tile, bf16, K-major SW128 [key][d]
   uint8_t* VT = smem + kTileBytes;             // V^T, fp16, K-major SW128 [d][key]
-  uint8_t* Pb = smem + 2 * kTileBytes;         // P[2], fp16 [row][key]
-  uint8_t* Vst = Pb + kTileBytes;              // V staging (bf16 [key][d]) = P[1]
-  uint8_t* Qb = smem + 4 * kTileBytes;         // Q[2], bf16 [row][d]
-  __shared__ __align__(8) uint64_t kv_full, q_ready[2], s_ready[2], p_ready[2], o_ready[2];
+  uint8_t* Pb = smem + 2 * kTileBytes;         // P[2], fp16 [row][key] / O staging
+  uint8_t* Vst = Pb + kPBytes;                 // V staging (bf16 [key][d]) = P[1]
+  uint8_t* Qb = Pb + 2 * kPBytes;              // Q[2], bf16 [row][d]
+  __shared__ __align__(8) uint64_t kv_full, q_full[2], s_free[2], s_ready[2], p_ready[2],
+      o_ready[2];
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool issuer = warp == 8;
+  const bool issuer = warp == 8, loader = warp == 9;
   const int wg = warp >> 2;                    // softmax warpgroup (0, 1)
   const int wtid = tid & 127;                  // = this thread's row / TMEM lane
   if (tid == 0) {
     mbar_init(&kv_full, 1);
     for (int w = 0; w < 2; ++w) {
-      mbar_init(&q_ready[w], 128);
+      mbar_init(&q_full[w], 1);
+      mbar_init(&s_free[w], 128);
       mbar_init(&s_ready[w], 1);
       mbar_init(&p_ready[w], 128);
       mbar_init(&o_ready[w], 1);
@@ -315,11 +318,14 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   griddep_wait();
 
   const int G = a.G, TPT = kBlock / G;         // tokens per M-tile
+  const int lgG = __ffs(G) - 1;                // G divides 16
   const int tok_per_item = kTilesPerItem * TPT;
   const int n_items = ws.sched[rows];
   const uint32_t idesc_s = idesc_f16(1, 128, 128), idesc_o = idesc_f16(0, 128, 128);
-  uint32_t kv_phase = 0, qpar[2] = {0, 0}, ppar[2] = {0, 0};   // issuer-side parities
-  uint32_t spar = 0, opar = 0;                                  // warpgroup-side parities
+  uint32_t kv_phase = 0;
+  int kS[2] = {0, 0}, kP[2] = {0, 0};          // issuer: S / PV issued per warpgroup
+  int kL0 = 0, kL1 = 0;                        // loader: Q tiles loaded per warpgroup
+  int kW = 0;                                  // warpgroup: tiles done
   int cur_row = -1;
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     int lo = 0, hi = (int)rows - 1;            // row of this item
@@ -336,7 +342,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     const int ntok = min(kBlock, ws.req_seq_len[r] - j * kBlock);
     const int ntiles = (end - beg + TPT - 1) / TPT;
 
-    named_bar_sync(1, kTcThreads);             // the previous item's MMAs and reads are done
+    // the previous item's MMAs are done; a new row also overwrites P[1] (V
+    // staging), so the output rows staged there must have been read
+    if (warp < 8 && row != cur_row) bulk_wait_read();
+    named_bar_sync(1, kTcThreads);
     if (row != cur_row) {
       if (issuer && lane == 0) {
         const int y = (page * a.Hkv + h) * kBlock;
@@ -348,7 +357,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
       }
       mbar_wait(&kv_full, kv_phase, ws.hdr);
       kv_phase ^= 1u;
-      if (!issuer) {
+      if (warp < 8) {
         // V [key][d] bf16 -> V^T [d][key] fp16 (keys past the last visible
         // token become 0, whatever the page holds there)
         const uint32_t vs = smem_u32(Vst);
@@ -373,40 +382,101 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
       cur_row = row;
     }
 
+    if (loader) {
+      // ------------------------------------------------------------ Q rows
+      // Tile row rr is token rr / G, query head h * G + rr % G.  G >= 8: one
+      // TMA box of G rows x 64 columns per token and half (1 KB-aligned in
+      // the swizzled tile), completing on q_full[w] by transaction count;
+      // rows of tokens past the end keep stale (finite) data, which the
+      // softmax masks.  G < 8: 16-byte cp.async copies, 2 rows per instruction.
+      for (int t = 0; t < ntiles; ++t) {
+        const int w = t & 1;
+        const int n = w ? kL1 : kL0;
+        if (n > 0) mbar_wait(&s_ready[w], (uint32_t)((n - 1) & 1), ws.hdr);
+        const int e0 = beg + t * TPT;
+        if (w) ++kL1; else ++kL0;
+        if (G >= 8) {
+          const int nt = min(TPT, end - e0);
+          if (lane == 0) mbar_arrive_expect_tx(&q_full[w], (uint32_t)(nt * G * 256));
+          __syncwarp();
+          if (lane < nt) {
+            const int y = a.q_idx[e0 + lane] * a.Hq + h * G;
+            uint8_t* dst = Qb + w * kTileBytes + lane * G * 128;
+            tma_load_2d(dst, &tmap_q, 0, y, &q_full[w]);
+            tma_load_2d(dst + kTileBytes / 2, &tmap_q, 64, y, &q_full[w]);
+          }
+          continue;
+        }
+        const uint32_t qdst = smem_u32(Qb + w * kTileBytes);
+        int my_tok = -1;                         // G == 4: lane i < TPT holds token i
+        if (lane < TPT && e0 + lane < end) my_tok = a.q_idx[e0 + lane];
+#pragma unroll 4
+        for (int i = 0; i < 64; ++i) {
+          const int rr = 2 * i + (lane >> 4);    // tile row: token rr / G, head rr % G
+          const int c = lane & 15;
+          int tk;
+          if (TPT <= 32) {
+            tk = __shfl_sync(0xffffffffu, my_tok, rr >> lgG);
+          } else {
+            const int e = e0 + (rr >> lgG);
+            tk = e < end ? a.q_idx[e] : -1;
+          }
+          const __nv_bfloat16* src = a.q + ((int64_t)(tk < 0 ? 0 : tk) * a.Hq + h * G +
+                                            (rr & (G - 1))) * kHeadDim + c * 8;
+          cp_async16(qdst + kmaj_off(rr, c, 128), src, tk < 0 ? 0 : 16);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full[w]);
+      }
+      continue;
+    }
+
     if (issuer) {
       if (lane == 0) {
         const uint32_t kts = smem_u32(Kt), vts = smem_u32(VT);
-        auto issue_s = [&](int t) {
-          const int w = t & 1;
-          mbar_wait(&q_ready[w], qpar[w], ws.hdr);
-          qpar[w] ^= 1u;
-          tc_fence_after();
-          const uint32_t qs = smem_u32(Qb + w * kTileBytes);
+        int nS[2] = {0, 0}, nP[2] = {0, 0};      // this item's S / PV per warpgroup
+        const int want[2] = {(ntiles + 1) / 2, ntiles / 2};
+        uint32_t spins = 0;
+        while (nP[0] < want[0] || nP[1] < want[1]) {
+          bool did = false;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            umma_f16(tbase + 256 * w, kstep_desc(qs, ks, 128), kstep_desc(kts, ks, 128), idesc_s,
-                     ks > 0);
-          umma_commit(&s_ready[w]);
-        };
-        auto issue_o = [&](int t) {
-          const int w = t & 1;
-          mbar_wait(&p_ready[w], ppar[w], ws.hdr);
-          ppar[w] ^= 1u;
-          tc_fence_after();
-          const uint32_t ps = smem_u32(Pb + w * kTileBytes);
+          for (int w = 0; w < 2; ++w) {
+            if (nS[w] < want[w] &&
+                mbar_try_wait(&q_full[w], (uint32_t)(kS[w] & 1)) &&
+                (kS[w] == 0 || mbar_try_wait(&s_free[w], (uint32_t)((kS[w] - 1) & 1)))) {
+              tc_fence_after();
+              const uint32_t qs = smem_u32(Qb + w * kTileBytes);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            umma_f16(tbase + 256 * w + 128, kstep_desc(ps, ks, 128), kstep_desc(vts, ks, 128),
-                     idesc_o, ks > 0);
-          umma_commit(&o_ready[w]);
-        };
-        issue_s(0);
-        if (ntiles > 1) issue_s(1);
-        for (int t = 0; t < ntiles; t += 2) {
-          issue_o(t);
-          if (t + 1 < ntiles) issue_o(t + 1);
-          if (t + 2 < ntiles) issue_s(t + 2);
-          if (t + 3 < ntiles) issue_s(t + 3);
+              for (int ks = 0; ks < 8; ++ks)
+                umma_f16(tbase + 256 * w, kstep_desc(qs, ks, 128), kstep_desc(kts, ks, 128),
+                         idesc_s, ks > 0);
+              umma_commit(&s_ready[w]);
+              ++kS[w];
+              ++nS[w];
+              did = true;
+            }
+            if (nP[w] < nS[w] && mbar_try_wait(&p_ready[w], (uint32_t)(kP[w] & 1))) {
+              tc_fence_after();
+              const uint32_t ps = smem_u32(Pb + w * kPBytes);
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks)
+                umma_f16(tbase + 256 * w + 128, kstep_desc(ps, ks, 128), kstep_desc(vts, ks, 128),
+                         idesc_o, ks > 0);
+              umma_commit(&o_ready[w]);
+              ++kP[w];
+              ++nP[w];
+              did = true;
+            }
+          }
+          if (did) {
+            spins = 0;
+          } else if (++spins > kWaitLimit) {      // bounded like every other wait
+            atomicOr(&ws.hdr->err, MSA_DEVERR_TIMEOUT);
+            break;
+          }
         }
       }
       __syncwarp();
@@ -414,131 +484,120 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     }
 
     // ---------------------------------------------------- softmax warpgroups
-    const uint32_t qdst = smem_u32(Qb + wg * kTileBytes);
     const int hq = h * G + wtid % G;
-    // Metadata of this thread's row of tile t: (token, position, slot); tok
-    // < 0 past the end of the item.  Fetched two tiles ahead, so that neither
-    // the Q copy nor the softmax waits on a dependent global load.
-    struct RowMeta { int tok, pos, slot; };
-    auto row_meta = [&](int t) {
-      RowMeta rm{-1, -1, -1};
+    uint8_t* prow = Pb + wg * kPBytes;
+    const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + 256 * wg;
+    // this thread's row of tile t: (token, position, slot), tok < 0 past the end
+    auto meta = [&](int t, int& tok, int& slot) {
+      tok = -1;
+      slot = -1;
       const int e = beg + t * TPT + wtid / G;
       if (t < ntiles && e < end) {
-        rm.tok = a.q_idx[e];
-        rm.slot = ws.csr_slot[e];
+        tok = a.q_idx[e];
+        slot = ws.csr_slot[e];
       }
-      return rm;
     };
-    auto row_pos = [&](RowMeta& rm) {
-      if (rm.tok >= 0 && rm.pos < 0) rm.pos = ws.tok_pos[rm.tok];
-    };
-    auto load_q = [&](const RowMeta& rm) {   // this thread copies its own 256-byte row
-      const __nv_bfloat16* src =
-          a.q + ((int64_t)(rm.tok < 0 ? 0 : rm.tok) * a.Hq + hq) * kHeadDim;
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        cp_async16(qdst + kmaj_off(wtid, c, 128), src + c * 8, rm.tok < 0 ? 0 : 16);
-      cp_async_commit();
-    };
-    RowMeta cur = row_meta(wg), nxt = row_meta(wg + 2);
-    if (wg < ntiles) load_q(cur);
-    row_pos(cur);
-    const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + 256 * wg;
+    int tok, slot, ntk, nsl;
+    meta(wg, tok, slot);
+    meta(wg + 2, ntk, nsl);
+    int pos = tok >= 0 ? ws.tok_pos[tok] : -1;
     for (int t = wg; t < ntiles; t += 2) {
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(&q_ready[wg]);
-      const int tok = cur.tok, pos = cur.pos, slot = cur.slot;
+      int ftk, fsl;
+      meta(t + 4, ftk, fsl);                        // two tiles ahead
+      const int npos = ntk >= 0 ? ws.tok_pos[ntk] : -1;
       const bool valid = tok >= 0;
+      const int lim = valid ? min(ntok, pos - j * kBlock + 1) : 0;
 
-      mbar_wait(&s_ready[wg], spar, ws.hdr);
-      spar ^= 1u;
+      mbar_wait(&s_ready[wg], (uint32_t)(kW & 1), ws.hdr);
       tc_fence_after();
-      float sv[128];
-      {
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(tlane, r0);                      // four loads, one wait
-        tmem_ld32(tlane + 32, r1);
-        tmem_ld32(tlane + 64, r2);
-        tmem_ld32(tlane + 96, r3);
+      // pass 1: row max (raw scores); the causal mask only cuts the diagonal /
+      // last block
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t rg[64];
+        tmem_ld64(tlane + 64 * cb, rg);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          sv[i] = __uint_as_float(r0[i]);
-          sv[32 + i] = __uint_as_float(r1[i]);
-          sv[64 + i] = __uint_as_float(r2[i]);
-          sv[96 + i] = __uint_as_float(r3[i]);
-        }
+        for (int i = 0; i < 64; ++i)
+          mx[i & 3] = fmaxf(mx[i & 3], 64 * cb + i < lim ? __uint_as_float(rg[i]) : -INFINITY);
       }
-      tc_fence_before();
-      RowMeta far = row_meta(t + 4);               // loads in flight for two tiles
-      if (t + 2 < ntiles) load_q(nxt);             // Q[wg] was consumed by S_t
-      row_pos(nxt);
-      // causal mask (only the diagonal / last block needs one), softmax in
-      // the exp2 domain with the scale folded into one FMA, P in fp16.
-      const int lim = valid ? min(ntok, pos - j * kBlock + 1) : 0;
-      if (lim < 128) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i) sv[i] = i < lim ? sv[i] : -INFINITY;
-      }
-      float mx[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = sv[k];
-#pragma unroll
-      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], mx[k + 4]);
-      const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));   // raw scores
+      const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float msc = m == -INFINITY ? 0.f : m * a.scale_log2;
-      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint8_t* prow = Pb + wg * kTileBytes;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          const float p0 = ex2_approx(fmaf(sv[c * 8 + 2 * e2], a.scale_log2, -msc));
-          const float p1 = ex2_approx(fmaf(sv[c * 8 + 2 * e2 + 1], a.scale_log2, -msc));
-          ls[(c & 3) * 2] += p0;
-          ls[(c & 3) * 2 + 1] += p1;
-          pk[e2] = pack_f16(p0, p1);
+      // pass 2: probabilities (exp2 domain, scale folded into one FMA), fp16 P
+      bulk_wait_read();                             // P[wg] no longer read by the last stores
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t rg[64];
+        tmem_ld64(tlane + 64 * cb, rg);
+        tmem_ld_wait();
+        if (cb == 1) {                              // S_k is in registers / P: free TMEM
+          tc_fence_before();
+          mbar_arrive(&s_free[wg]);
         }
-        *reinterpret_cast<uint4*>(prow + kmaj_off(wtid, c, 128)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const int i = c8 * 8 + 2 * e2;
+            const float s0 = 64 * cb + i < lim ? __uint_as_float(rg[i]) : -INFINITY;
+            const float s1 = 64 * cb + i + 1 < lim ? __uint_as_float(rg[i + 1]) : -INFINITY;
+            const float p0 = ex2_approx(fmaf(s0, a.scale_log2, -msc));
+            const float p1 = ex2_approx(fmaf(s1, a.scale_log2, -msc));
+            ls[e2] += p0 + p1;
+            pk[e2] = pack_f16(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(prow + kmaj_off(wtid, cb * 8 + c8, 128)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
       }
-      const float l = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      const float l = (ls[0] + ls[1]) + (ls[2] + ls[3]);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_ready[wg]);
 
-      mbar_wait(&o_ready[wg], opar, ws.hdr);
-      opar ^= 1u;
+      mbar_wait(&o_ready[wg], (uint32_t)(kW & 1), ws.hdr);
       tc_fence_after();
-      // tcgen05.ld is warp-collective: every lane loads, only valid rows store
+      // O_k -> normalised fp16 row, staged row-major in P[wg] (the MMA has
+      // finished reading it), then one bulk store per row.  tcgen05.ld is
+      // warp-collective: every lane loads, only valid rows store.
       const bool store = valid && l > 0.f && slot >= 0;
-      const int64_t pi = store ? ((int64_t)tok * a.Hq + hq) * a.S + slot : 0;
-      uint4* op = reinterpret_cast<uint4*>(static_cast<__half*>(ws.o_part) + pi * kHeadDim);
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      {
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(tlane + 128, r0);
-        tmem_ld32(tlane + 160, r1);
-        tmem_ld32(tlane + 192, r2);
-        tmem_ld32(tlane + 224, r3);
+      uint4* stage = reinterpret_cast<uint4*>(prow + wtid * kStageStride);
+#pragma unroll 1
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t rg[64];
+        tmem_ld64(tlane + 128 + 64 * cb, rg);
         tmem_ld_wait();
-        tc_fence_before();
-        if (store) {
-          store_row_chunk(op, r0, inv);
-          store_row_chunk(op + 4, r1, inv);
-          store_row_chunk(op + 8, r2, inv);
-          store_row_chunk(op + 12, r3, inv);
-          ws.lse_part[pi] = (msc + log2f(l)) * kLn2;
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+          uint32_t o4[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2)
+            o4[e2] = pack_f16(__uint_as_float(rg[q8 * 8 + 2 * e2]) * inv,
+                              __uint_as_float(rg[q8 * 8 + 2 * e2 + 1]) * inv);
+          stage[cb * 8 + q8] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
         }
       }
-      cur = nxt;
-      nxt = far;
+      tc_fence_before();
+      if (store) {
+        const int64_t pi = ((int64_t)tok * a.Hq + hq) * a.S + slot;
+        fence_proxy_async_smem();
+        bulk_store(static_cast<__half*>(ws.o_part) + pi * kHeadDim, stage, 256);
+        bulk_commit();
+        ws.lse_part[pi] = (msc + log2f(l)) * kLn2;
+      }
+      ++kW;
+      tok = ntk;
+      slot = nsl;
+      pos = npos;
+      ntk = ftk;
+      nsl = fsl;
     }
   }
+  if (warp < 8) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (issuer) {
@@ -664,13 +723,16 @@ extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const 
   (void)selected;   // the CSR build recorded each entry's slot in ws
   const int64_t prow = (int64_t)cfg->num_pages * a.Hkv * kBlock;
   if (prow > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tq;
   if (!make_pool_map(&tk, k_pages, prow, false) || !make_pool_map(&tv, v_pages, prow, false))
     return MSA_ERR_CUDA;
-  const size_t smem = 6u * kTileBytes;
+  // queries as [tokens * H_q, 128]; boxes of one token's G heads (G >= 8)
+  if (!make_pool_map(&tq, q, (int64_t)max_tokens_of(*cfg) * a.Hq, false, a.G >= 8 ? a.G : 8))
+    return MSA_ERR_CUDA;
+  const size_t smem = kTcSmemBytes;
   if ((st = set_smem(prefill_tc_kernel, smem)) != MSA_OK) return st;
   const int grid = sm_count();
   if (grid <= 0) return MSA_ERR_CUDA;
   return launch_pdl(prefill_tc_kernel, dim3(grid), dim3(kTcThreads), smem, (cudaStream_t)stream,
-                    view_of(*cfg, ws), a, tk, tv, rows);
+                    view_of(*cfg, ws), a, tk, tv, tq, rows);
 }

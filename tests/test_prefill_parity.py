@@ -31,8 +31,10 @@ def _csr_matches_oracle(w, sa):
 
 @pytest.mark.parametrize("kw", [dict(), dict(num_q_heads=32, num_kv_heads=2),
                                 dict(num_q_heads=16, num_kv_heads=4, index_dim=64),
-                                dict(seq_lens=(700, 129), q_len=129, topk_blocks=2)],
-                         ids=["g8", "g16", "g4_d64", "chunk129_topk2"])
+                                dict(seq_lens=(700, 129), q_len=129, topk_blocks=2),
+                                dict(num_q_heads=4, num_kv_heads=4),
+                                dict(num_q_heads=8, num_kv_heads=4, seq_lens=(300, 1100))],
+                         ids=["g8", "g16", "g4_d64", "chunk129_topk2", "g1", "g2"])
 def test_small_prefill_every_element(kw):
     spec = wl.small("prefill", **kw)
     w = wl.make_workload(spec, device="cuda")
