@@ -490,10 +490,8 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
   }
 }
 
-// ---- combine: one warp per (token, query head), splits merged in a fixed
-// order.  PREFILL: fp16 partials, one per selected slot, of which the first
-// min(nb, S) exist (nb = the token's visible blocks).
-template <bool PREFILL>
+// ---- combine (decode): one warp per (token, query head), splits merged in a
+// fixed order.
 __global__ void __launch_bounds__(256)
 combine_kernel(WsView ws, int Hq, int nsplit, __nv_bfloat16* __restrict__ out,
                float* __restrict__ lse) {
@@ -504,32 +502,21 @@ combine_kernel(WsView ws, int Hq, int nsplit, __nv_bfloat16* __restrict__ out,
   griddep_wait();
   if (t >= ws.hdr->num_tokens) return;
   const bool active = ws.tok_req[t] >= 0;
-  int nvalid = nsplit;
-  if (PREFILL) nvalid = active ? min(nsplit, ws.tok_pos[t] / kBlock + 1) : 0;
   const float* lp = ws.lse_part + idx * nsplit;
   float M = -INFINITY;
   if (active)
-    for (int s = lane; s < nvalid; s += 32) M = fmaxf(M, lp[s]);
+    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, lp[s]);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
     float L = 0.f;
-    for (int s = 0; s < nvalid; ++s) L += exp2f((lp[s] - M) * kLog2e);
+    for (int s = 0; s < nsplit; ++s) L += exp2f((lp[s] - M) * kLog2e);
     const float lse_tot = M + logf(L);
-    for (int s = 0; s < nvalid; ++s) {
+    for (int s = 0; s < nsplit; ++s) {
       const float w = expf(lp[s] - lse_tot);
-      float4 v;
-      if (PREFILL) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(
-            static_cast<const __half*>(ws.o_part) + (idx * nsplit + s) * kHeadDim + 4 * lane);
-        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-        v = make_float4(a.x, a.y, b.x, b.y);
-      } else {
-        v = *reinterpret_cast<const float4*>(static_cast<const float*>(ws.o_part) +
-                                             (idx * nsplit + s) * kHeadDim + 4 * lane);
-      }
+      const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(ws.o_part) +
+                                                        (idx * nsplit + s) * kHeadDim + 4 * lane);
       o.x = fmaf(w, v.x, o.x); o.y = fmaf(w, v.y, o.y);
       o.z = fmaf(w, v.z, o.z); o.w = fmaf(w, v.w, o.w);
     }
@@ -540,6 +527,62 @@ combine_kernel(WsView ws, int Hq, int nsplit, __nv_bfloat16* __restrict__ out,
   __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
   uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
   *reinterpret_cast<uint2*>(out + idx * kHeadDim + 4 * lane) = pk;
+}
+
+// ---- combine (prefill): 16 threads per (token, query head), 8 dimensions
+// each.  The token's selected blocks are its slots 0 .. min(nb, S) - 1 (nb =
+// its visible blocks); slot s of (t, KV head h) is CSR entry slot_entry[t, h,
+// s], whose fp16 partial row is entry * G + g.  Merged in slot order.
+__global__ void __launch_bounds__(256)
+combine_prefill_kernel(WsView ws, int Hq, int Hkv, int S, __nv_bfloat16* __restrict__ out,
+                       float* __restrict__ lse) {
+  const int64_t idx = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4);
+  const int c = threadIdx.x & 15;
+  griddep_launch_dependents();
+  griddep_wait();
+  const int t = (int)(idx / Hq);
+  if (t >= ws.hdr->num_tokens) return;
+  const int hq = (int)(idx % Hq), G = Hq / Hkv, h = hq / G, g = hq % G;
+  const int nvalid = ws.tok_req[t] >= 0 ? min(S, ws.tok_pos[t] / kBlock + 1) : 0;
+  const int32_t* ent = ws.slot_entry + ((int64_t)t * Hkv + h) * S;
+  // running max / sum of exp over the slots' LSE
+  float M = -INFINITY, L = 0.f;
+  for (int s = 0; s < nvalid; ++s) {
+    const float x = __ldg(ws.lse_part + (int64_t)__ldg(ent + s) * G + g);
+    if (x > M) {
+      L = L * exp2f((M - x) * kLog2e) + 1.f;
+      M = x;
+    } else if (x != -INFINITY) {
+      L += exp2f((x - M) * kLog2e);
+    }
+  }
+  float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float lse_tot = -INFINITY;
+  if (M != -INFINITY) {
+    lse_tot = M + logf(L);
+    const __half* part = static_cast<const __half*>(ws.o_part);
+#pragma unroll 4
+    for (int s = 0; s < nvalid; ++s) {
+      const int64_t row = (int64_t)__ldg(ent + s) * G + g;
+      const float w = expf(__ldg(ws.lse_part + row) - lse_tot);
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(part + row * kHeadDim) + c);
+      const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[k]));
+        o[2 * k] = fmaf(w, f.x, o[2 * k]);
+        o[2 * k + 1] = fmaf(w, f.y, o[2 * k + 1]);
+      }
+    }
+  }
+  if (c == 0) lse[idx] = lse_tot;
+  uint32_t pk[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(o[2 * k], o[2 * k + 1]);
+    pk[k] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  reinterpret_cast<uint4*>(out + idx * kHeadDim)[c] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
 }
 
 template <bool FP8>
@@ -629,17 +672,20 @@ extern "C" msa_status msa_combine(const msa_config* cfg, const void* ws, void* o
   msa_status st = check_config(cfg);
   if (st != MSA_OK) return st;
   if (!ws || !out || !lse) return MSA_ERR_INVALID_ARG;
-  if (((uintptr_t)out & 7) != 0) return MSA_ERR_INVALID_ARG;
+  if (((uintptr_t)out & (is_prefill(*cfg) ? 15 : 7)) != 0) return MSA_ERR_INVALID_ARG;
   const int64_t items = (int64_t)max_tokens_of(*cfg) * cfg->num_q_heads;
   if (items <= 0) return MSA_OK;
+  const WsView v = view_of(*cfg, ws);
+  if (is_prefill(*cfg)) {
+    const int64_t pgrid = (items + 15) / 16;
+    if (pgrid > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
+    return launch_pdl(combine_prefill_kernel, dim3((unsigned)pgrid), dim3(256), 0,
+                      (cudaStream_t)stream, v, cfg->num_q_heads, cfg->num_kv_heads,
+                      width_of(*cfg), (__nv_bfloat16*)out, lse);
+  }
   const int64_t grid = (items + 7) / 8;
   if (grid > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
-  const WsView v = view_of(*cfg, ws);
-  if (is_prefill(*cfg))
-    return launch_pdl(combine_kernel<true>, dim3((unsigned)grid), dim3(256), 0,
-                      (cudaStream_t)stream, v, cfg->num_q_heads, splits_of(*cfg),
-                      (__nv_bfloat16*)out, lse);
-  return launch_pdl(combine_kernel<false>, dim3((unsigned)grid), dim3(256), 0,
+  return launch_pdl(combine_kernel, dim3((unsigned)grid), dim3(256), 0,
                     (cudaStream_t)stream, v, cfg->num_q_heads, splits_of(*cfg),
                     (__nv_bfloat16*)out, lse);
 }

@@ -171,6 +171,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
       "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+// Tile store of one box from shared memory at (x, y) of `tmap`, tracked by
+// this thread's bulk groups (bulk_commit / bulk_wait_read).  Rows outside the
+// tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   tmap),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
 
 // 1-D bulk copy (TMA engine) of `bytes` (multiple of 16, both addresses 16-byte
 // aligned) into shared memory, completion counted on `bar`.

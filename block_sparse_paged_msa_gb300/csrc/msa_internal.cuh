@@ -63,7 +63,7 @@ inline int64_t csr_rows_of(const msa_config& c) {
 // Byte offsets of every workspace region.
 struct WsLayout {
   size_t plan_err, req_seq_len, req_nb, req_cu_nb, req_qstart, tok_req, tok_pos, block_table;
-  size_t sched, csr_slot, o_part, lse_part, total;
+  size_t sched, slot_entry, o_part, lse_part, total;
 };
 
 inline WsLayout layout_of(const msa_config& c) {
@@ -80,7 +80,7 @@ inline WsLayout layout_of(const msa_config& c) {
   L.tok_pos = o;     o = align_up(o + 4 * T);
   L.block_table = o; o = align_up(o + 4 * B * (size_t)c.max_blocks_per_req);
   L.sched = o;       o = align_up(o + (is_prefill(c) ? 4 * (size_t)(csr_rows_of(c) + 1) : 0));
-  L.csr_slot = o;    o = align_up(o + (is_prefill(c) ? 2 * T * (size_t)c.num_kv_heads * width_of(c) : 0));
+  L.slot_entry = o;  o = align_up(o + (is_prefill(c) ? 4 * T * (size_t)c.num_kv_heads * width_of(c) : 0));
   L.o_part = o;      o = align_up(o + part_elem_bytes(c) * T * Hq * NS * kHeadDim);
   L.lse_part = o;    o = align_up(o + 4 * T * Hq * NS);
   L.total = o;
@@ -99,10 +99,14 @@ struct WsView {
   int32_t* tok_pos;
   int32_t* block_table;   // [max_batch, max_blocks_per_req], -1 = invalid
   int32_t* sched;         // prefill: [csr rows + 1] first work item of each CSR row
-  int16_t* csr_slot;      // prefill: per CSR entry, the slot of the row's block in the
-                          // token's selected list
-  void* o_part;           // [T, H_q, NS, D] fp32 (decode) | fp16 (prefill)
-  float* lse_part;        // [T, H_q, NS]
+  int32_t* slot_entry;    // prefill: [T, H_kv, S] the CSR entry that holds (token, KV
+                          // head, slot of the selected list)
+  // Partial outputs and their LSE.  Decode: [T, H_q, NS, D] fp32 and [T, H_q, NS]
+  // (NS splits).  Prefill: fp16 rows indexed entry * G + g, where entry is the
+  // CSR entry of (token, KV head h, block) and g the query head within h's
+  // group, so an M-tile's rows are contiguous; [T * H_q * S] rows of D.
+  void* o_part;
+  float* lse_part;
 };
 
 inline WsView view_of(const msa_config& c, const void* ws) {
@@ -119,7 +123,7 @@ inline WsView view_of(const msa_config& c, const void* ws) {
   v.tok_pos = (int32_t*)(b + L.tok_pos);
   v.block_table = (int32_t*)(b + L.block_table);
   v.sched = (int32_t*)(b + L.sched);
-  v.csr_slot = (int16_t*)(b + L.csr_slot);
+  v.slot_entry = (int32_t*)(b + L.slot_entry);
   v.o_part = (void*)(b + L.o_part);
   v.lse_part = (float*)(b + L.lse_part);
   return v;

@@ -197,7 +197,7 @@ csr_rows_kernel(WsView ws, int Hkv, int B, int NB, int S, const int32_t* __restr
       if (FILL && in) {
         const int e = base + count + __popc(bal & ((1u << lane) - 1u));
         q_idx[e] = t;
-        ws.csr_slot[e] = (int16_t)slot;
+        ws.slot_entry[((int64_t)t * Hkv + h) * S + slot] = e;
       }
       count += __popc(bal);
     }
@@ -242,14 +242,10 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(int32_t* __restrict__ ro
 // row (ws.sched), so the huge rows of the init / local blocks are split
 // instead of dominating the tail.
 constexpr int kTilesPerItem = 16;
-constexpr int kTcThreads = 10 * 32;      // 2 softmax warpgroups, MMA issuer, Q loader
+constexpr int kLoaderWarps = 3;          // Q loaders (TMA issue from one warp is slow)
+constexpr int kTcThreads = (9 + kLoaderWarps) * 32;   // 2 softmax warpgroups, MMA issuer
 constexpr int kTileBytes = kBlock * kHeadDim * 2;
-// A P tile doubles as the output staging area: 128 rows of 256 bytes at a
-// 272-byte stride, so that the 16-byte stores of 8 consecutive rows fall in 8
-// different bank groups.
-constexpr int kStageStride = 272;
-constexpr int kPBytes = kBlock * kStageStride;          // 34 KB, a multiple of 1 KB
-constexpr int kTcSmemBytes = 4 * kTileBytes + 2 * kPBytes + 1024;
+constexpr int kTcSmemBytes = 6 * kTileBytes + 1024;
 
 struct PrefillArgs {
   int Hkv, Hq, G, S, B, NB;
@@ -278,7 +274,9 @@ struct PrefillArgs {
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
-                  const __grid_constant__ CUtensorMap tmap_q, int64_t rows) {
+                  const __grid_constant__ CUtensorMap tmap_q,
+                  const __grid_constant__ CUtensorMap tmap_o,
+                  const __grid_constant__ CUtensorMap tmap_o8, int64_t rows) {
   extern __shared__ __align__(16) uint8_t tc_smem_raw[];
   // swizzled operand tiles want 1 KB alignment: round the base up (the
   // launch asks for 1 KB of slack)
@@ -286,19 +284,20 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   uint8_t* Kt = smem;                          // K tile, bf16, K-major SW128 [key][d]
   uint8_t* VT = smem + kTileBytes;             // V^T, fp16, K-major SW128 [d][key]
   uint8_t* Pb = smem + 2 * kTileBytes;         // P[2], fp16 [row][key] / O staging
-  uint8_t* Vst = Pb + kPBytes;                 // V staging (bf16 [key][d]) = P[1]
-  uint8_t* Qb = Pb + 2 * kPBytes;              // Q[2], bf16 [row][d]
+  uint8_t* Vst = Pb + kTileBytes;              // V staging (bf16 [key][d]) = P[1]
+  uint8_t* Qb = Pb + 2 * kTileBytes;           // Q[2], bf16 [row][d]
   __shared__ __align__(8) uint64_t kv_full, q_full[2], s_free[2], s_ready[2], p_ready[2],
       o_ready[2];
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool issuer = warp == 8, loader = warp == 9;
+  const bool issuer = warp == 8, loader = warp >= 9;
+  const int lw = warp - 9;                     // loader warp index
   const int wg = warp >> 2;                    // softmax warpgroup (0, 1)
   const int wtid = tid & 127;                  // = this thread's row / TMEM lane
   if (tid == 0) {
     mbar_init(&kv_full, 1);
     for (int w = 0; w < 2; ++w) {
-      mbar_init(&q_full[w], 1);
+      mbar_init(&q_full[w], kLoaderWarps);
       mbar_init(&s_free[w], 128);
       mbar_init(&s_ready[w], 1);
       mbar_init(&p_ready[w], 128);
@@ -389,6 +388,8 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
       // the swizzled tile), completing on q_full[w] by transaction count;
       // rows of tokens past the end keep stale (finite) data, which the
       // softmax masks.  G < 8: 16-byte cp.async copies, 2 rows per instruction.
+      // The loader warps share each tile's copies (box / instruction k goes to
+      // warp k % kLoaderWarps) and each arrives on q_full[w] once.
       for (int t = 0; t < ntiles; ++t) {
         const int w = t & 1;
         const int n = w ? kL1 : kL0;
@@ -397,21 +398,23 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
         if (w) ++kL1; else ++kL0;
         if (G >= 8) {
           const int nt = min(TPT, end - e0);
-          if (lane == 0) mbar_arrive_expect_tx(&q_full[w], (uint32_t)(nt * G * 256));
-          __syncwarp();
-          if (lane < nt) {
-            const int y = a.q_idx[e0 + lane] * a.Hq + h * G;
-            uint8_t* dst = Qb + w * kTileBytes + lane * G * 128;
-            tma_load_2d(dst, &tmap_q, 0, y, &q_full[w]);
-            tma_load_2d(dst + kTileBytes / 2, &tmap_q, 64, y, &q_full[w]);
+          if (lane == 0) {
+            if (lw == 0) mbar_arrive_expect_tx(&q_full[w], (uint32_t)(nt * G * 256));
+            else mbar_arrive(&q_full[w]);
+          }
+          const int b = lane * kLoaderWarps + lw;   // box: token b / 2, half b % 2
+          if (b < 2 * nt) {
+            const int y = a.q_idx[e0 + (b >> 1)] * a.Hq + h * G;
+            uint8_t* dst = Qb + w * kTileBytes + (b >> 1) * G * 128 + (b & 1) * (kTileBytes / 2);
+            tma_load_2d(dst, &tmap_q, (b & 1) * 64, y, &q_full[w]);
           }
           continue;
         }
         const uint32_t qdst = smem_u32(Qb + w * kTileBytes);
         int my_tok = -1;                         // G == 4: lane i < TPT holds token i
         if (lane < TPT && e0 + lane < end) my_tok = a.q_idx[e0 + lane];
-#pragma unroll 4
-        for (int i = 0; i < 64; ++i) {
+#pragma unroll 2
+        for (int i = lw; i < 64; i += kLoaderWarps) {
           const int rr = 2 * i + (lane >> 4);    // tile row: token rr / G, head rr % G
           const int c = lane & 15;
           int tk;
@@ -460,7 +463,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
             }
             if (nP[w] < nS[w] && mbar_try_wait(&p_ready[w], (uint32_t)(kP[w] & 1))) {
               tc_fence_after();
-              const uint32_t ps = smem_u32(Pb + w * kPBytes);
+              const uint32_t ps = smem_u32(Pb + w * kTileBytes);
 #pragma unroll
               for (int ks = 0; ks < 8; ++ks)
                 umma_f16(tbase + 256 * w + 128, kstep_desc(ps, ks, 128), kstep_desc(vts, ks, 128),
@@ -484,26 +487,18 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     }
 
     // ---------------------------------------------------- softmax warpgroups
-    const int hq = h * G + wtid % G;
-    uint8_t* prow = Pb + wg * kPBytes;
+    uint8_t* prow = Pb + wg * kTileBytes;
     const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + 256 * wg;
-    // this thread's row of tile t: (token, position, slot), tok < 0 past the end
-    auto meta = [&](int t, int& tok, int& slot) {
-      tok = -1;
-      slot = -1;
-      const int e = beg + t * TPT + wtid / G;
-      if (t < ntiles && e < end) {
-        tok = a.q_idx[e];
-        slot = ws.csr_slot[e];
-      }
+    const bool leader = wtid == 0;                  // issues the warpgroup's output stores
+    // this thread's row of tile t: its token (< 0 past the end of the item)
+    auto token_of = [&](int t) {
+      const int e = beg + t * TPT + (wtid >> lgG);
+      return t < ntiles && e < end ? a.q_idx[e] : -1;
     };
-    int tok, slot, ntk, nsl;
-    meta(wg, tok, slot);
-    meta(wg + 2, ntk, nsl);
+    int tok = token_of(wg), ntk = token_of(wg + 2);
     int pos = tok >= 0 ? ws.tok_pos[tok] : -1;
     for (int t = wg; t < ntiles; t += 2) {
-      int ftk, fsl;
-      meta(t + 4, ftk, fsl);                        // two tiles ahead
+      const int ftk = token_of(t + 4);              // two tiles ahead
       const int npos = ntk >= 0 ? ws.tok_pos[ntk] : -1;
       const bool valid = tok >= 0;
       const int lim = valid ? min(ntok, pos - j * kBlock + 1) : 0;
@@ -524,8 +519,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
       }
       const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float msc = m == -INFINITY ? 0.f : m * a.scale_log2;
+      // P[wg] still holds the previous tile's output until its stores read it
+      if (leader) bulk_wait_read();
+      named_bar_sync(2 + wg, 128);
       // pass 2: probabilities (exp2 domain, scale folded into one FMA), fp16 P
-      bulk_wait_read();                             // P[wg] no longer read by the last stores
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
       for (int cb = 0; cb < 2; ++cb) {
@@ -560,12 +557,17 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
 
       mbar_wait(&o_ready[wg], (uint32_t)(kW & 1), ws.hdr);
       tc_fence_after();
-      // O_k -> normalised fp16 row, staged row-major in P[wg] (the MMA has
-      // finished reading it), then one bulk store per row.  tcgen05.ld is
-      // warp-collective: every lane loads, only valid rows store.
-      const bool store = valid && l > 0.f && slot >= 0;
+      // O_k -> normalised fp16 row, staged in P[wg] in the swizzled K-major
+      // layout (the MMA has finished reading P).  The tile's rows are the
+      // partial rows e0 * G ... of consecutive CSR entries, so the leader
+      // stores them as TMA boxes: 128 rows for a full tile, 8-row boxes for
+      // the last one, whose rows past a multiple of 8 (G < 8 only) their own
+      // threads write.  tcgen05.ld is warp-collective: every lane loads.
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* stage = reinterpret_cast<uint4*>(prow + wtid * kStageStride);
+      const int e0 = beg + t * TPT;
+      const int nrows = min(TPT, end - e0) * G;     // valid rows of this tile
+      const bool tail_row = wtid >= (nrows & ~7) && wtid < nrows;
+      __half* grow = static_cast<__half*>(ws.o_part) + ((int64_t)e0 * G + wtid) * kHeadDim;
 #pragma unroll 1
       for (int cb = 0; cb < 2; ++cb) {
         uint32_t rg[64];
@@ -578,23 +580,32 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
           for (int e2 = 0; e2 < 4; ++e2)
             o4[e2] = pack_f16(__uint_as_float(rg[q8 * 8 + 2 * e2]) * inv,
                               __uint_as_float(rg[q8 * 8 + 2 * e2 + 1]) * inv);
-          stage[cb * 8 + q8] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+          const uint4 v4 = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+          *reinterpret_cast<uint4*>(prow + kmaj_off(wtid, cb * 8 + q8, 128)) = v4;
+          if (tail_row) reinterpret_cast<uint4*>(grow)[cb * 8 + q8] = v4;
         }
       }
       tc_fence_before();
-      if (store) {
-        const int64_t pi = ((int64_t)tok * a.Hq + hq) * a.S + slot;
-        fence_proxy_async_smem();
-        bulk_store(static_cast<__half*>(ws.o_part) + pi * kHeadDim, stage, 256);
+      if (wtid < nrows)
+        ws.lse_part[(int64_t)e0 * G + wtid] = l > 0.f ? (msc + log2f(l)) * kLn2 : -INFINITY;
+      fence_proxy_async_smem();
+      named_bar_sync(2 + wg, 128);
+      if (leader) {
+        if (nrows == kBlock) {
+          tma_store_2d(&tmap_o, 0, e0 * G, prow);
+          tma_store_2d(&tmap_o, 64, e0 * G, prow + kTileBytes / 2);
+        } else {
+          for (int b8 = 0; b8 < (nrows >> 3); ++b8) {
+            tma_store_2d(&tmap_o8, 0, e0 * G + 8 * b8, prow + 1024 * b8);
+            tma_store_2d(&tmap_o8, 64, e0 * G + 8 * b8, prow + kTileBytes / 2 + 1024 * b8);
+          }
+        }
         bulk_commit();
-        ws.lse_part[pi] = (msc + log2f(l)) * kLn2;
       }
       ++kW;
       tok = ntk;
-      slot = nsl;
       pos = npos;
       ntk = ftk;
-      nsl = fsl;
     }
   }
   if (warp < 8) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -729,10 +740,18 @@ extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const 
   // queries as [tokens * H_q, 128]; boxes of one token's G heads (G >= 8)
   if (!make_pool_map(&tq, q, (int64_t)max_tokens_of(*cfg) * a.Hq, false, a.G >= 8 ? a.G : 8))
     return MSA_ERR_CUDA;
+  // fp16 partial rows [T * H_q * S, 128] (2-byte elements, copied as bits):
+  // whole M-tiles and 8-row boxes
+  const int64_t orows = (int64_t)max_tokens_of(*cfg) * a.Hq * a.S;
+  if (orows > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
+  CUtensorMap to, to8;
+  const void* o_part = view_of(*cfg, ws).o_part;
+  if (!make_pool_map(&to, o_part, orows, false) || !make_pool_map(&to8, o_part, orows, false, 8))
+    return MSA_ERR_CUDA;
   const size_t smem = kTcSmemBytes;
   if ((st = set_smem(prefill_tc_kernel, smem)) != MSA_OK) return st;
   const int grid = sm_count();
   if (grid <= 0) return MSA_ERR_CUDA;
   return launch_pdl(prefill_tc_kernel, dim3(grid), dim3(kTcThreads), smem, (cudaStream_t)stream,
-                    view_of(*cfg, ws), a, tk, tv, tq, rows);
+                    view_of(*cfg, ws), a, tk, tv, tq, to, to8, rows);
 }
