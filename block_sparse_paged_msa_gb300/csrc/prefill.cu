@@ -448,8 +448,8 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
 #pragma unroll
           for (int w = 0; w < 2; ++w) {
             if (nS[w] < want[w] &&
-                mbar_try_wait(&q_full[w], (uint32_t)(kS[w] & 1)) &&
-                (kS[w] == 0 || mbar_try_wait(&s_free[w], (uint32_t)((kS[w] - 1) & 1)))) {
+                mbar_test_wait(&q_full[w], (uint32_t)(kS[w] & 1)) &&
+                (kS[w] == 0 || mbar_test_wait(&s_free[w], (uint32_t)((kS[w] - 1) & 1)))) {
               tc_fence_after();
               const uint32_t qs = smem_u32(Qb + w * kTileBytes);
 #pragma unroll
@@ -461,7 +461,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
               ++nS[w];
               did = true;
             }
-            if (nP[w] < nS[w] && mbar_try_wait(&p_ready[w], (uint32_t)(kP[w] & 1))) {
+            if (nP[w] < nS[w] && mbar_test_wait(&p_ready[w], (uint32_t)(kP[w] & 1))) {
               tc_fence_after();
               const uint32_t ps = smem_u32(Pb + w * kTileBytes);
 #pragma unroll
@@ -476,7 +476,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
           }
           if (did) {
             spins = 0;
-          } else if (++spins > kWaitLimit) {      // bounded like every other wait
+          } else if (++spins > 16u * kWaitLimit) {  // bounded like every other wait
             atomicOr(&ws.hdr->err, MSA_DEVERR_TIMEOUT);
             break;
           }
@@ -505,17 +505,29 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
 
       mbar_wait(&s_ready[wg], (uint32_t)(kW & 1), ws.hdr);
       tc_fence_after();
-      // pass 1: row max (raw scores); the causal mask only cuts the diagonal /
-      // last block
+      // pass 1: row max (raw scores).  The causal mask / the end of the
+      // sequence only cut the diagonal / last block: a warp whose rows all see
+      // the whole block skips the per-element mask.
+      const bool full = __all_sync(0xffffffffu, lim >= kBlock);
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
       for (int cb = 0; cb < 2; ++cb) {
         uint32_t rg[64];
         tmem_ld64(tlane + 64 * cb, rg);
         tmem_ld_wait();
+        if (full) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          mx[i & 3] = fmaxf(mx[i & 3], 64 * cb + i < lim ? __uint_as_float(rg[i]) : -INFINITY);
+          for (int i = 0; i < 64; i += 8) {
+            mx[0] = fmax3(mx[0], __uint_as_float(rg[i]), __uint_as_float(rg[i + 1]));
+            mx[1] = fmax3(mx[1], __uint_as_float(rg[i + 2]), __uint_as_float(rg[i + 3]));
+            mx[2] = fmax3(mx[2], __uint_as_float(rg[i + 4]), __uint_as_float(rg[i + 5]));
+            mx[3] = fmax3(mx[3], __uint_as_float(rg[i + 6]), __uint_as_float(rg[i + 7]));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            mx[i & 3] = fmaxf(mx[i & 3], 64 * cb + i < lim ? __uint_as_float(rg[i]) : -INFINITY);
+        }
       }
       const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float msc = m == -INFINITY ? 0.f : m * a.scale_log2;
@@ -523,7 +535,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
       if (leader) bulk_wait_read();
       named_bar_sync(2 + wg, 128);
       // pass 2: probabilities (exp2 domain, scale folded into one FMA), fp16 P
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      // Pairs of columns go through packed fp32 FMA / add; masked columns
+      // (only outside the fast path) become -inf before the exponential.
+      const uint64_t sc2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-msc, -msc);
+      uint64_t ls2[4] = {0, 0, 0, 0};               // (+0.f, +0.f) pairs
 #pragma unroll 1
       for (int cb = 0; cb < 2; ++cb) {
         uint32_t rg[64];
@@ -533,24 +548,33 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
           tc_fence_before();
           mbar_arrive(&s_free[wg]);
         }
+        if (!full) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (64 * cb + i >= lim) rg[i] = __float_as_uint(-INFINITY);
+        }
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
           uint32_t pk[4];
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
             const int i = c8 * 8 + 2 * e2;
-            const float s0 = 64 * cb + i < lim ? __uint_as_float(rg[i]) : -INFINITY;
-            const float s1 = 64 * cb + i + 1 < lim ? __uint_as_float(rg[i + 1]) : -INFINITY;
-            const float p0 = ex2_approx(fmaf(s0, a.scale_log2, -msc));
-            const float p1 = ex2_approx(fmaf(s1, a.scale_log2, -msc));
-            ls[e2] += p0 + p1;
+            float x0, x1;
+            f2_split(fma_f2(f2u(rg[i], rg[i + 1]), sc2, nm2), x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            ls2[e2] = add_f2(ls2[e2], f2(p0, p1));
             pk[e2] = pack_f16(p0, p1);
           }
           *reinterpret_cast<uint4*>(prow + kmaj_off(wtid, cb * 8 + c8, 128)) =
               make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
-      const float l = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      float l;
+      {
+        float a0, a1;
+        f2_split(add_f2(add_f2(ls2[0], ls2[1]), add_f2(ls2[2], ls2[3])), a0, a1);
+        l = a0 + a1;
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_ready[wg]);
@@ -564,6 +588,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
       // the last one, whose rows past a multiple of 8 (G < 8 only) their own
       // threads write.  tcgen05.ld is warp-collective: every lane loads.
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      const uint64_t inv2 = f2(inv, inv);
       const int e0 = beg + t * TPT;
       const int nrows = min(TPT, end - e0) * G;     // valid rows of this tile
       const bool tail_row = wtid >= (nrows & ~7) && wtid < nrows;
@@ -577,9 +602,11 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
         for (int q8 = 0; q8 < 8; ++q8) {
           uint32_t o4[4];
 #pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2)
-            o4[e2] = pack_f16(__uint_as_float(rg[q8 * 8 + 2 * e2]) * inv,
-                              __uint_as_float(rg[q8 * 8 + 2 * e2 + 1]) * inv);
+          for (int e2 = 0; e2 < 4; ++e2) {
+            float o0, o1;
+            f2_split(mul_f2(f2u(rg[q8 * 8 + 2 * e2], rg[q8 * 8 + 2 * e2 + 1]), inv2), o0, o1);
+            o4[e2] = pack_f16(o0, o1);
+          }
           const uint4 v4 = make_uint4(o4[0], o4[1], o4[2], o4[3]);
           *reinterpret_cast<uint4*>(prow + kmaj_off(wtid, cb * 8 + q8, 128)) = v4;
           if (tail_row) reinterpret_cast<uint4*>(grow)[cb * 8 + q8] = v4;
