@@ -257,20 +257,21 @@ struct PrefillArgs {
 
 // Persistent: one CTA per SM walks the work items.  Per CSR row (KV head h,
 // request r, key block j) the K tile and the V tile arrive by TMA; V is
-// transposed once into an fp16 K-major tile (V^T) so that both MMAs read
-// K-major operands.  M-tiles alternate between the two softmax warpgroups;
-// warpgroup w's k-th tile (counted over the whole kernel) goes through
-//   loader:  Q_k rows -> Q[w]        once S_{k-1} has read Q[w]      (q_full)
-//   issuer:  S_k = Q_k K^T (bf16)    once Q_k landed, S_{k-1} read   (s_ready)
-//   WG:      S_k -> registers (thread = row)                        (s_free)
-//            causal mask, softmax, P_k (fp16) -> P[w]                (p_ready)
-//   issuer:  O_k = P_k V (fp16)                                      (o_ready)
-//   WG:      O_k -> normalised fp16 row -> P[w] (row-major) -> one 256-byte
-//            bulk store per row into the partials, LSE beside it.
-// Accumulators live in TMEM (S and O per warpgroup, 512 columns).  The
-// issuer polls both warpgroups and serves whichever is ready, so S_{k+1}
-// already runs while warpgroup w is still in the softmax of tile k, and the
-// two warpgroups drift out of phase.
+// transposed once into an fp16 K-major tile (V^T), the B operand of O = P V.
+// M-tiles alternate between the two softmax warpgroups; warpgroup w's k-th
+// tile (counted over the whole kernel) goes through
+//   loaders: Q_k rows -> Q[w] (TMA)  once S_{k-1} has read Q[w]      (q_full)
+//   issuer:  S_k = Q_k K^T (bf16) into TMEM region w, once Q_k landed and
+//            O_{k-1} = P_{k-1} V has finished reading P_{k-1}      (s_ready)
+//   WG:      S_k -> registers (thread = row), causal mask, softmax; P_k
+//            (fp16) written over S_k's first 64 TMEM columns      (p_ready)
+//   issuer:  O_k = P_k V (A operand from TMEM, fp16)                (o_ready)
+//   WG:      O_k -> normalised fp16 row -> P[w] staging tile (swizzled) ->
+//            TMA tile stores into the partials, LSE beside them.
+// TMEM: per warpgroup 128 columns of S / P and 128 of O (512 in all).  P
+// never touches shared memory, which the two SS MMAs of 128 x 128 tiles
+// otherwise keep close to saturated.  The issuer polls both warpgroups and
+// serves whichever is ready.
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
@@ -283,11 +284,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   uint8_t* smem = tc_smem_raw + ((1024u - (smem_u32(tc_smem_raw) & 1023u)) & 1023u);
   uint8_t* Kt = smem;                          // K tile, bf16, K-major SW128 [key][d]
   uint8_t* VT = smem + kTileBytes;             // V^T, fp16, K-major SW128 [d][key]
-  uint8_t* Pb = smem + 2 * kTileBytes;         // P[2], fp16 [row][key] / O staging
+  uint8_t* Pb = smem + 2 * kTileBytes;         // O staging tiles [2], fp16 [row][d]
   uint8_t* Vst = Pb + kTileBytes;              // V staging (bf16 [key][d]) = P[1]
   uint8_t* Qb = Pb + 2 * kTileBytes;           // Q[2], bf16 [row][d]
-  __shared__ __align__(8) uint64_t kv_full, q_full[2], s_free[2], s_ready[2], p_ready[2],
-      o_ready[2];
+  __shared__ __align__(8) uint64_t kv_full, q_full[2], s_ready[2], p_ready[2], o_ready[2];
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool issuer = warp == 8, loader = warp >= 9;
@@ -298,7 +298,6 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     mbar_init(&kv_full, 1);
     for (int w = 0; w < 2; ++w) {
       mbar_init(&q_full[w], kLoaderWarps);
-      mbar_init(&s_free[w], 128);
       mbar_init(&s_ready[w], 1);
       mbar_init(&p_ready[w], 128);
       mbar_init(&o_ready[w], 1);
@@ -447,9 +446,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
           bool did = false;
 #pragma unroll
           for (int w = 0; w < 2; ++w) {
+            // S_k overwrites P_{k-1}: only once O_{k-1} = P_{k-1} V completed
             if (nS[w] < want[w] &&
                 mbar_test_wait(&q_full[w], (uint32_t)(kS[w] & 1)) &&
-                (kS[w] == 0 || mbar_test_wait(&s_free[w], (uint32_t)((kS[w] - 1) & 1)))) {
+                (kS[w] == 0 || mbar_test_wait(&o_ready[w], (uint32_t)((kS[w] - 1) & 1)))) {
               tc_fence_after();
               const uint32_t qs = smem_u32(Qb + w * kTileBytes);
 #pragma unroll
@@ -463,11 +463,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
             }
             if (nP[w] < nS[w] && mbar_test_wait(&p_ready[w], (uint32_t)(kP[w] & 1))) {
               tc_fence_after();
-              const uint32_t ps = smem_u32(Pb + w * kTileBytes);
 #pragma unroll
               for (int ks = 0; ks < 8; ++ks)
-                umma_f16(tbase + 256 * w + 128, kstep_desc(ps, ks, 128), kstep_desc(vts, ks, 128),
-                         idesc_o, ks > 0);
+                umma_f16_ts(tbase + 256 * w + 128, tbase + 256 * w + 8 * ks,
+                            kstep_desc(vts, ks, 128), idesc_o, ks > 0);
               umma_commit(&o_ready[w]);
               ++kP[w];
               ++nP[w];
@@ -531,12 +530,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
       }
       const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float msc = m == -INFINITY ? 0.f : m * a.scale_log2;
-      // P[wg] still holds the previous tile's output until its stores read it
-      if (leader) bulk_wait_read();
-      named_bar_sync(2 + wg, 128);
       // pass 2: probabilities (exp2 domain, scale folded into one FMA), fp16 P
-      // Pairs of columns go through packed fp32 FMA / add; masked columns
-      // (only outside the fast path) become -inf before the exponential.
+      // into TMEM over the S columns already read.  Pairs of columns go
+      // through packed fp32 FMA / add; masked columns (only outside the fast
+      // path) become -inf before the exponential.
       const uint64_t sc2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-msc, -msc);
       uint64_t ls2[4] = {0, 0, 0, 0};               // (+0.f, +0.f) pairs
 #pragma unroll 1
@@ -544,30 +541,21 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
         uint32_t rg[64];
         tmem_ld64(tlane + 64 * cb, rg);
         tmem_ld_wait();
-        if (cb == 1) {                              // S_k is in registers / P: free TMEM
-          tc_fence_before();
-          mbar_arrive(&s_free[wg]);
-        }
         if (!full) {
 #pragma unroll
           for (int i = 0; i < 64; ++i)
             if (64 * cb + i >= lim) rg[i] = __float_as_uint(-INFINITY);
         }
+        uint32_t pk[32];
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const int i = c8 * 8 + 2 * e2;
-            float x0, x1;
-            f2_split(fma_f2(f2u(rg[i], rg[i + 1]), sc2, nm2), x0, x1);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            ls2[e2] = add_f2(ls2[e2], f2(p0, p1));
-            pk[e2] = pack_f16(p0, p1);
-          }
-          *reinterpret_cast<uint4*>(prow + kmaj_off(wtid, cb * 8 + c8, 128)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int i2 = 0; i2 < 32; ++i2) {
+          float x0, x1;
+          f2_split(fma_f2(f2u(rg[2 * i2], rg[2 * i2 + 1]), sc2, nm2), x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          ls2[i2 & 3] = add_f2(ls2[i2 & 3], f2(p0, p1));
+          pk[i2] = pack_f16(p0, p1);
         }
+        tmem_st32(tlane + 32 * cb, pk);             // keys 64cb.. -> columns 32cb..
       }
       float l;
       {
@@ -575,14 +563,17 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
         f2_split(add_f2(add_f2(ls2[0], ls2[1]), add_f2(ls2[2], ls2[3])), a0, a1);
         l = a0 + a1;
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_ready[wg]);
 
+      // the staging tile still holds the previous tile's output until its
+      // stores have read it
+      if (leader) bulk_wait_read();
+      named_bar_sync(2 + wg, 128);
       mbar_wait(&o_ready[wg], (uint32_t)(kW & 1), ws.hdr);
       tc_fence_after();
-      // O_k -> normalised fp16 row, staged in P[wg] in the swizzled K-major
-      // layout (the MMA has finished reading P).  The tile's rows are the
+      // O_k -> normalised fp16 row, staged in the swizzled K-major layout.  The tile's rows are the
       // partial rows e0 * G ... of consecutive CSR entries, so the leader
       // stores them as TMA boxes: 128 rows for a full tile, 8-row boxes for
       // the last one, whose rows past a multiple of 8 (G < 8 only) their own
