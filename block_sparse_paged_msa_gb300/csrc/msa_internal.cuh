@@ -60,10 +60,20 @@ inline int64_t csr_rows_of(const msa_config& c) {
   return (int64_t)c.num_kv_heads * c.max_batch * c.max_blocks_per_req;
 }
 
+// Prefill CSR build: per (KV head, key block) a bitmap over the step's query
+// tokens, request r's tokens from word (first token / 32) + r, so requests
+// never share a word.  Words per (head, block):
+inline int64_t csr_words_per_row(const msa_config& c) {
+  return (int64_t)(max_tokens_of(c) + 31) / 32 + c.max_batch;
+}
+inline int64_t csr_words_of(const msa_config& c) {
+  return (int64_t)c.num_kv_heads * c.max_blocks_per_req * csr_words_per_row(c);
+}
+
 // Byte offsets of every workspace region.
 struct WsLayout {
   size_t plan_err, req_seq_len, req_nb, req_cu_nb, req_qstart, tok_req, tok_pos, block_table;
-  size_t sched, slot_entry, o_part, lse_part, total;
+  size_t sched, slot_entry, csr_bits, csr_wpre, o_part, lse_part, total;
 };
 
 inline WsLayout layout_of(const msa_config& c) {
@@ -81,6 +91,8 @@ inline WsLayout layout_of(const msa_config& c) {
   L.block_table = o; o = align_up(o + 4 * B * (size_t)c.max_blocks_per_req);
   L.sched = o;       o = align_up(o + (is_prefill(c) ? 4 * (size_t)(csr_rows_of(c) + 1) : 0));
   L.slot_entry = o;  o = align_up(o + (is_prefill(c) ? 4 * T * (size_t)c.num_kv_heads * width_of(c) : 0));
+  L.csr_bits = o;    o = align_up(o + (is_prefill(c) ? 4 * csr_words_of(c) : 0));
+  L.csr_wpre = o;    o = align_up(o + (is_prefill(c) ? 4 * csr_words_of(c) : 0));
   L.o_part = o;      o = align_up(o + part_elem_bytes(c) * T * Hq * NS * kHeadDim);
   L.lse_part = o;    o = align_up(o + 4 * T * Hq * NS);
   L.total = o;
@@ -101,6 +113,8 @@ struct WsView {
   int32_t* sched;         // prefill: [csr rows + 1] first work item of each CSR row
   int32_t* slot_entry;    // prefill: [T, H_kv, S] the CSR entry that holds (token, KV
                           // head, slot of the selected list)
+  uint32_t* csr_bits;     // prefill: [H_kv, NB, words] token bitmaps of the CSR rows
+  int32_t* csr_wpre;      // prefill: same shape, set bits before each word within its row
   // Partial outputs and their LSE.  Decode: [T, H_q, NS, D] fp32 and [T, H_q, NS]
   // (NS splits).  Prefill: fp16 rows indexed entry * G + g, where entry is the
   // CSR entry of (token, KV head h, block) and g the query head within h's
@@ -124,6 +138,8 @@ inline WsView view_of(const msa_config& c, const void* ws) {
   v.block_table = (int32_t*)(b + L.block_table);
   v.sched = (int32_t*)(b + L.sched);
   v.slot_entry = (int32_t*)(b + L.slot_entry);
+  v.csr_bits = (uint32_t*)(b + L.csr_bits);
+  v.csr_wpre = (int32_t*)(b + L.csr_wpre);
   v.o_part = (void*)(b + L.o_part);
   v.lse_part = (float*)(b + L.lse_part);
   return v;

@@ -15,20 +15,20 @@
 //    dense [64 x d] x [d x 128] contraction (m16n8k16 bf16 MMA, fp32
 //    accumulation, exact for integer-valued index vectors), followed by a
 //    causal row max; K tiles stream through a double-buffered smem ring.
-//  * csr_rows_kernel: one warp per CSR row (KV head, request, key block) walks
-//    the request's tokens in order and tests membership in each token's
-//    ascending selected list (binary search); ballots give the count (first
-//    pass) and the ordered positions (second pass), so every row lists its
-//    tokens ascending and the structure is deterministic.
+//  * csr_mark / csr_count / csr_fill kernels: the CSR built token-major from
+//    per-(KV head, key block) token bitmaps, so every row lists its tokens
+//    ascending and the structure is deterministic.
 //  * prefill_tc_kernel (msa_sparse_prefill): fifth-generation tensor cores.
 //    A persistent CTA per SM walks work items of up to 16 M-tiles of one CSR
 //    row; per row the K and V tiles arrive by TMA and V is transposed once to
 //    fp16.  M-tiles of 128 rows (tokens x GQA heads) alternate between two
 //    softmax warpgroups: one thread issues tcgen05.mma for S = Q K^T (bf16)
-//    and O = P V (fp16) with fp32 accumulators in TMEM; each warpgroup thread
-//    owns one row (tcgen05.ld), applies the causal mask, the softmax, and
-//    writes the normalised fp16 partial and its LSE per (token, query head,
-//    slot).  msa_combine merges the slots.
+//    and O = P V (fp16, P from TMEM) with fp32 accumulators in TMEM; each
+//    warpgroup thread owns one row (tcgen05.ld), applies the causal mask and
+//    the softmax; the normalised fp16 partial rows of a tile, contiguous in
+//    CSR-entry order, leave by TMA tile stores with their LSE beside them.
+//    msa_combine merges each token's slots.
+#include <algorithm>
 #include <mutex>
 
 #include "tcgen05.cuh"
@@ -156,20 +156,55 @@ prefill_score_kernel(WsView ws, int Hkv, int max_blocks, const __nv_bfloat16* __
 }
 
 // ------------------------------------------------------------ CSR
-// Slot of block j in the ascending list sel[0..n), or -1.
-__device__ __forceinline__ int find_block(const int32_t* sel, int n, int j) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (sel[mid] < j) lo = mid + 1; else hi = mid;
-  }
-  return lo < n && sel[lo] == j ? lo : -1;
+// Row (h, r, j) of the key-block -> query CSR lists, ascending, the tokens of
+// request r whose selection for KV head h holds block j.  Built token-major
+// and deterministically: every selected entry sets its token's bit in the
+// bitmap of (h, j) (csr_mark_kernel); a warp per row counts the bits of the
+// request's words and records the count before each word (csr_count_kernel);
+// after the scan of the counts, an entry's CSR position is the row start +
+// the bits before it (csr_fill_kernel).  An entry counts when its block is
+// visible to the token (j <= position / P, j < the request's block count).
+
+struct CsrEntry {
+  bool ok;
+  int r, j;
+  int64_t word;      // bitmap word of (h, j, token)
+  uint32_t bit;
+};
+
+__device__ __forceinline__ CsrEntry csr_entry(const WsView& ws, const int32_t* selected, int t,
+                                              int h, int s, int Hkv, int NB, int S,
+                                              int64_t wpr) {
+  CsrEntry c;
+  c.ok = false;
+  c.r = ws.tok_req[t];
+  if (c.r < 0) return c;
+  c.j = selected[((int64_t)t * Hkv + h) * S + s];
+  if (c.j < 0 || c.j >= NB || c.j >= ws.req_nb[c.r] || c.j * kBlock > ws.tok_pos[t]) return c;
+  const int qs = ws.req_qstart[c.r];
+  const int wl = t - qs;
+  c.word = ((int64_t)h * NB + c.j) * wpr + (qs >> 5) + c.r + (wl >> 5);
+  c.bit = 1u << (wl & 31);
+  c.ok = true;
+  return c;
 }
 
-template <bool FILL>
 __global__ void __launch_bounds__(256)
-csr_rows_kernel(WsView ws, int Hkv, int B, int NB, int S, const int32_t* __restrict__ selected,
-                int32_t* __restrict__ row_ptr, int32_t* __restrict__ q_idx) {
+csr_mark_kernel(WsView ws, int Hkv, int NB, int S, int64_t wpr, const int32_t* __restrict__ selected) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int64_t n = (int64_t)ws.hdr->num_tokens * Hkv * S;
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+    const int s = (int)(i % S), h = (int)((i / S) % Hkv), t = (int)(i / ((int64_t)S * Hkv));
+    const CsrEntry c = csr_entry(ws, selected, t, h, s, Hkv, NB, S, wpr);
+    if (c.ok) atomicOr(ws.csr_bits + c.word, c.bit);
+  }
+}
+
+// One warp per row (h, r, j): popcounts of request r's words, exclusive
+// prefix per word, the row's count into row_ptr[row + 1].
+__global__ void __launch_bounds__(256)
+csr_count_kernel(WsView ws, int Hkv, int B, int NB, int64_t wpr, int32_t* __restrict__ row_ptr) {
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   griddep_launch_dependents();
@@ -178,33 +213,45 @@ csr_rows_kernel(WsView ws, int Hkv, int B, int NB, int S, const int32_t* __restr
   const int j = (int)(row % NB);
   const int r = (int)((row / NB) % B);
   const int h = (int)(row / ((int64_t)NB * B));
-  int count = 0;
-  const int base = FILL ? row_ptr[row] : 0;
+  int total = 0;
   if (r < ws.hdr->batch && j < ws.req_nb[r]) {
-    const int qs = ws.req_qstart[r], qe = ws.req_qstart[r + 1];
-    for (int t0 = qs; t0 < qe; t0 += 32) {
-      const int t = t0 + lane;
-      int slot = -1;
-      if (t < qe && ws.tok_req[t] == r) {
-        const int p = ws.tok_pos[t];
-        if (j * kBlock <= p) {
-          const int n = min(p / kBlock + 1, S);
-          slot = find_block(selected + ((int64_t)t * Hkv + h) * S, n, j);
-        }
+    const int qs = ws.req_qstart[r], nq = ws.req_qstart[r + 1] - qs;
+    const int64_t base = ((int64_t)h * NB + j) * wpr + (qs >> 5) + r;
+    const int nw = (nq + 31) >> 5;
+    for (int w0 = 0; w0 < nw; w0 += 32) {
+      const int w = w0 + lane;
+      const int c = w < nw ? __popc(ws.csr_bits[base + w]) : 0;
+      int x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
       }
-      const bool in = slot >= 0;
-      const unsigned bal = __ballot_sync(0xffffffffu, in);
-      if (FILL && in) {
-        const int e = base + count + __popc(bal & ((1u << lane) - 1u));
-        q_idx[e] = t;
-        ws.slot_entry[((int64_t)t * Hkv + h) * S + slot] = e;
-      }
-      count += __popc(bal);
+      if (w < nw) ws.csr_wpre[base + w] = total + x - c;
+      total += __shfl_sync(0xffffffffu, x, 31);
     }
   }
-  if (!FILL && lane == 0) {
-    row_ptr[row + 1] = count;
+  if (lane == 0) {
+    row_ptr[row + 1] = total;
     if (row == 0) row_ptr[0] = 0;
+  }
+}
+
+__global__ void __launch_bounds__(256)
+csr_fill_kernel(WsView ws, int Hkv, int B, int NB, int S, int64_t wpr,
+                const int32_t* __restrict__ selected, const int32_t* __restrict__ row_ptr,
+                int32_t* __restrict__ q_idx) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int64_t n = (int64_t)ws.hdr->num_tokens * Hkv * S;
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+    const int s = (int)(i % S), h = (int)((i / S) % Hkv), t = (int)(i / ((int64_t)S * Hkv));
+    const CsrEntry c = csr_entry(ws, selected, t, h, s, Hkv, NB, S, wpr);
+    if (!c.ok) continue;
+    const int64_t row = ((int64_t)h * B + c.r) * NB + c.j;
+    const int e = row_ptr[row] + ws.csr_wpre[c.word] + __popc(ws.csr_bits[c.word] & (c.bit - 1u));
+    q_idx[e] = t;
+    ws.slot_entry[i] = e;
   }
 }
 
@@ -705,15 +752,22 @@ extern "C" msa_status msa_build_k2q_csr(const msa_config* cfg, const void* ws,
   cudaStream_t s = (cudaStream_t)stream;
   const unsigned grid = (unsigned)((rows + 7) / 8);
   const int S = width_of(*cfg);
-  if ((st = launch_pdl(csr_rows_kernel<false>, dim3(grid), dim3(256), 0, s, v, cfg->num_kv_heads,
-                       cfg->max_batch, cfg->max_blocks_per_req, S, selected, row_ptr,
-                       q_indices)) != MSA_OK)
+  const int NB = cfg->max_blocks_per_req, B = cfg->max_batch, Hkv = cfg->num_kv_heads;
+  const int64_t wpr = csr_words_per_row(*cfg);
+  const int64_t entries = (int64_t)max_tokens_of(*cfg) * Hkv * S;
+  const int egrid = (int)std::min<int64_t>((entries + 255) / 256, 8 * 1024);
+  if (cudaMemsetAsync(v.csr_bits, 0, 4 * (size_t)csr_words_of(*cfg), s) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  if ((st = launch_pdl(csr_mark_kernel, dim3(egrid), dim3(256), 0, s, v, Hkv, NB, S, wpr,
+                       selected)) != MSA_OK)
+    return st;
+  if ((st = launch_pdl(csr_count_kernel, dim3(grid), dim3(256), 0, s, v, Hkv, B, NB, wpr,
+                       row_ptr)) != MSA_OK)
     return st;
   if ((st = launch_pdl(csr_scan_kernel, dim3(1), dim3(1024), 0, s, row_ptr, rows)) != MSA_OK)
     return st;
-  if ((st = launch_pdl(csr_rows_kernel<true>, dim3(grid), dim3(256), 0, s, v, cfg->num_kv_heads,
-                       cfg->max_batch, cfg->max_blocks_per_req, S, selected, row_ptr,
-                       q_indices)) != MSA_OK)
+  if ((st = launch_pdl(csr_fill_kernel, dim3(egrid), dim3(256), 0, s, v, Hkv, B, NB, S, wpr,
+                       selected, (const int32_t*)row_ptr, q_indices)) != MSA_OK)
     return st;
   // work schedule of msa_sparse_prefill: items of up to 16 M-tiles per row
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
