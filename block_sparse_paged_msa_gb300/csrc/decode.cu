@@ -532,47 +532,91 @@ combine_kernel(WsView ws, int Hq, int nsplit, __nv_bfloat16* __restrict__ out,
 // ---- combine (prefill): 16 threads per (token, query head), 8 dimensions
 // each.  The token's selected blocks are its slots 0 .. min(nb, S) - 1 (nb =
 // its visible blocks); slot s of (t, KV head h) is CSR entry slot_entry[t, h,
-// s], whose fp16 partial row is entry * G + g.  Merged in slot order.
-__global__ void __launch_bounds__(256)
+// s], whose fp16 partial row is entry * G + g.  Thread c of the group looks up
+// the entries and LSEs of slots c and 16 + c (slots from 32 on are looked up
+// again in each pass) and the group shares them by shuffles, so that the
+// partial rows load independently of one another.  Merged in slot order.
+__device__ __forceinline__ void combine_rows(const uint4* __restrict__ part, int64_t row, float w,
+                                             int n, int c, unsigned gmask, float (&o)[8]) {
+#pragma unroll
+  for (int k0 = 0; k0 < 16; k0 += 8) {
+    if (k0 >= n) break;                          // uniform per group
+    uint4 raw[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int64_t rk = __shfl_sync(gmask, row, k0 + k, 16);
+      raw[k] = k0 + k < n ? __ldg(part + rk * (kHeadDim / 8) + c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float wk = __shfl_sync(gmask, w, k0 + k, 16);
+      const uint32_t u[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[q]));
+        o[2 * q] = fmaf(wk, f.x, o[2 * q]);
+        o[2 * q + 1] = fmaf(wk, f.y, o[2 * q + 1]);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256, 4)
 combine_prefill_kernel(WsView ws, int Hq, int Hkv, int S, __nv_bfloat16* __restrict__ out,
                        float* __restrict__ lse) {
   const int64_t idx = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4);
   const int c = threadIdx.x & 15;
+  const unsigned gmask = 0xffffu << (threadIdx.x & 16);   // this half-warp
   griddep_launch_dependents();
   griddep_wait();
   const int t = (int)(idx / Hq);
-  if (t >= ws.hdr->num_tokens) return;
+  if (t >= ws.hdr->num_tokens) return;                    // uniform per half-warp
   const int hq = (int)(idx % Hq), G = Hq / Hkv, h = hq / G, g = hq % G;
   const int nvalid = ws.tok_req[t] >= 0 ? min(S, ws.tok_pos[t] / kBlock + 1) : 0;
   const int32_t* ent = ws.slot_entry + ((int64_t)t * Hkv + h) * S;
-  // running max / sum of exp over the slots' LSE
-  float M = -INFINITY, L = 0.f;
-  for (int s = 0; s < nvalid; ++s) {
-    const float x = __ldg(ws.lse_part + (int64_t)__ldg(ent + s) * G + g);
-    if (x > M) {
-      L = L * exp2f((M - x) * kLog2e) + 1.f;
-      M = x;
-    } else if (x != -INFINITY) {
-      L += exp2f((x - M) * kLog2e);
+  auto lookup = [&](int s, int64_t& row, float& x) {
+    row = 0;
+    x = -INFINITY;
+    if (s < nvalid) {
+      row = (int64_t)__ldg(ent + s) * G + g;
+      x = __ldg(ws.lse_part + row);
     }
+  };
+  int64_t r0, r1;
+  float x0, x1;
+  lookup(c, r0, x0);
+  lookup(16 + c, r1, x1);
+  // max and sum of exp over the slots' LSE
+  float M = fmaxf(x0, x1);
+  for (int s0 = 32; s0 < nvalid; s0 += 16) {
+    int64_t rr;
+    float xx;
+    lookup(s0 + c, rr, xx);
+    M = fmaxf(M, xx);
   }
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(gmask, M, o, 16));
   float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float lse_tot = -INFINITY;
   if (M != -INFINITY) {
-    lse_tot = M + logf(L);
-    const __half* part = static_cast<const __half*>(ws.o_part);
-#pragma unroll 4
-    for (int s = 0; s < nvalid; ++s) {
-      const int64_t row = (int64_t)__ldg(ent + s) * G + g;
-      const float w = expf(__ldg(ws.lse_part + row) - lse_tot);
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(part + row * kHeadDim) + c);
-      const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+    float L = exp2f((x0 - M) * kLog2e) + exp2f((x1 - M) * kLog2e);
+    for (int s0 = 32; s0 < nvalid; s0 += 16) {
+      int64_t rr;
+      float xx;
+      lookup(s0 + c, rr, xx);
+      L += exp2f((xx - M) * kLog2e);
+    }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[k]));
-        o[2 * k] = fmaf(w, f.x, o[2 * k]);
-        o[2 * k + 1] = fmaf(w, f.y, o[2 * k + 1]);
-      }
+    for (int o2 = 8; o2 >= 1; o2 >>= 1) L += __shfl_xor_sync(gmask, L, o2, 16);
+    lse_tot = M + logf(L);
+    const uint4* part = static_cast<const uint4*>(ws.o_part);
+    combine_rows(part, r0, expf(x0 - lse_tot), min(16, nvalid), c, gmask, o);
+    if (nvalid > 16) combine_rows(part, r1, expf(x1 - lse_tot), min(16, nvalid - 16), c, gmask, o);
+    for (int s0 = 32; s0 < nvalid; s0 += 16) {
+      int64_t rr;
+      float xx;
+      lookup(s0 + c, rr, xx);
+      combine_rows(part, rr, expf(xx - lse_tot), min(16, nvalid - s0), c, gmask, o);
     }
   }
   if (c == 0) lse[idx] = lse_tot;
