@@ -151,6 +151,10 @@ msa_status check_config(const msa_config* c);
 // boxes of 64 columns x box_rows, e4m3 -> 128 x box_rows, 128-byte swizzle.
 bool make_pool_map(CUtensorMap* m, const void* base, int64_t rows, bool fp8,
                    int box_rows = kBlock);
+// General bf16 tensor map with 128-byte swizzle: dims / box innermost first,
+// strides_bytes[i] = byte stride of dimension i + 1.
+bool make_bf16_map(CUtensorMap* m, const void* base, int rank, const int64_t* dims,
+                   const int64_t* strides_bytes, const int* box);
 // Index scores of a prefill chunk (tensor-core tiles; prefill.cu).
 msa_status prefill_index_score(const msa_config& c, const WsView& v, const void* idx_q,
                                const void* idx_k, float* scores, cudaStream_t s);

@@ -78,6 +78,23 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
+bool make_bf16_map(CUtensorMap* m, const void* base, int rank, const int64_t* dims,
+                   const int64_t* strides_bytes, const int* box) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr || rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], estr[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = (cuuint64_t)dims[i];
+    bx[i] = (cuuint32_t)box[i];
+    estr[i] = 1u;
+    if (i > 0) st[i - 1] = (cuuint64_t)strides_bytes[i - 1];
+  }
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, st,
+             bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_pool_map(CUtensorMap* m, const void* base, int64_t rows, bool fp8, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;

@@ -1,5 +1,5 @@
-// Chunked-prefill path: index scores for every query token of the chunk, the
-// key-block -> query CSR, and block-sparse attention tiles per CSR row.
+// Chunked-prefill path: the key-block -> query CSR and block-sparse attention
+// tiles per CSR row (the chunk's index scores are in prefill_index.cu).
 //
 // vLLM minimax_m3/nvidia/sparse_attention_msa.py (MiniMaxM3SparseMSAImpl.forward)
 // runs prefill as build_k2q_csr(prefill_topk [H, tokens, MK], cu_seqlens_q,
@@ -11,10 +11,6 @@
 // index-K cache, cu_seqlens and prefix lengths.
 //
 // Here:
-//  * prefill_score_kernel: a 64-token query tile x one 128-key block is a
-//    dense [64 x d] x [d x 128] contraction (m16n8k16 bf16 MMA, fp32
-//    accumulation, exact for integer-valued index vectors), followed by a
-//    causal row max; K tiles stream through a double-buffered smem ring.
 //  * csr_mark / csr_count / csr_fill kernels: the CSR built token-major from
 //    per-(KV head, key block) token bitmaps, so every row lists its tokens
 //    ascending and the structure is deterministic.
@@ -35,125 +31,6 @@
 
 namespace msa {
 namespace {
-
-// ------------------------------------------------------------ index scores
-constexpr int kScoreTokens = 64;
-constexpr int kScoreThreads = 128;
-
-__device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
-  return *reinterpret_cast<const uint32_t*>(p);
-}
-
-template <int DIDX>
-__device__ __forceinline__ uint32_t swz_idx(int row, int c) {
-  return DIDX == 128 ? swz(row, c) : swz128(row, c);
-}
-
-template <int DIDX>
-__global__ void __launch_bounds__(kScoreThreads)
-prefill_score_kernel(WsView ws, int Hkv, int max_blocks, const __nv_bfloat16* __restrict__ idx_q,
-                     const uint8_t* __restrict__ idx_k, float* __restrict__ scores) {
-  constexpr int kRowBytes = DIDX * 2;
-  constexpr int kChunks = kRowBytes / 16;
-  constexpr int kTile = kBlock * kRowBytes;
-  constexpr int KS = DIDX / 16;
-  extern __shared__ __align__(128) uint8_t smem[];   // two K tiles
-  __shared__ int seg_r[kScoreTokens + 1], seg_start[kScoreTokens + 1];
-  __shared__ int nseg_s;
-  griddep_launch_dependents();
-  griddep_wait();
-  const int T = ws.hdr->num_tokens;
-  const int t0 = blockIdx.x * kScoreTokens;
-  const int h = blockIdx.y;
-  if (t0 >= T) return;
-  const int t1 = min(T, t0 + kScoreTokens);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, tq = lane & 3;
-  if (tid == 0) {   // runs of consecutive tokens of one request
-    int n = 0;
-    for (int t = t0; t < t1; ++t) {
-      const int r = ws.tok_req[t];
-      if (n == 0 || r != seg_r[n - 1]) {
-        seg_r[n] = r;
-        seg_start[n] = t;
-        ++n;
-      }
-    }
-    seg_start[n] = t1;
-    nseg_s = n;
-  }
-  __syncthreads();
-  const int nseg = nseg_s;
-  const int rowA = t0 + warp * 16 + g, rowB = rowA + 8;
-  for (int sg = 0; sg < nseg; ++sg) {
-    const int r = seg_r[sg];
-    if (r < 0) continue;                       // CTA-uniform
-    const int a = seg_start[sg], b = seg_start[sg + 1];
-    const bool inA = rowA >= a && rowA < b, inB = rowB >= a && rowB < b;
-    const int pA = inA ? ws.tok_pos[rowA] : -1, pB = inB ? ws.tok_pos[rowB] : -1;
-    const int nblk = ws.tok_pos[b - 1] / kBlock + 1;
-    uint32_t qa[KS][4];
-    {
-      const __nv_bfloat16* qA = idx_q + ((int64_t)rowA * Hkv + h) * DIDX;
-      const __nv_bfloat16* qB = idx_q + ((int64_t)rowB * Hkv + h) * DIDX;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const int c0 = ks * 16 + 2 * tq, c1 = c0 + 8;
-        qa[ks][0] = inA ? ld_u32(qA + c0) : 0u;
-        qa[ks][1] = inB ? ld_u32(qB + c0) : 0u;
-        qa[ks][2] = inA ? ld_u32(qA + c1) : 0u;
-        qa[ks][3] = inB ? ld_u32(qB + c1) : 0u;
-      }
-    }
-    auto issue = [&](int j, int buf) {
-      const int page = ws.block_table[(int64_t)r * max_blocks + j];
-      const uint8_t* src = idx_k + ((int64_t)(page < 0 ? 0 : page) * Hkv + h) * (int64_t)kTile;
-      const uint32_t dst = smem_u32(smem + buf * kTile);
-#pragma unroll
-      for (int k = 0; k < kBlock * kChunks / kScoreThreads; ++k) {
-        const int idx = k * kScoreThreads + tid;
-        const int row = idx / kChunks, c = idx % kChunks;
-        cp_async16(dst + swz_idx<DIDX>(row, c), src + row * kRowBytes + c * 16, page < 0 ? 0 : 16);
-      }
-      cp_async_commit();
-    };
-    issue(0, 0);
-    for (int j = 0; j < nblk; ++j) {
-      if (j + 1 < nblk) issue(j + 1, (j + 1) & 1); else cp_async_commit();
-      cp_async_wait<1>();
-      __syncthreads();
-      const uint32_t tile = smem_u32(smem + (j & 1) * kTile);
-      float mA = -INFINITY, mB = -INFINITY;
-#pragma unroll 4
-      for (int nt = 0; nt < 16; ++nt) {
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        const int krow = nt * 8 + (lane & 7);
-#pragma unroll
-        for (int ks = 0; ks < KS; ks += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(tile + swz_idx<DIDX>(krow, 2 * ks + (lane >> 3)), b0, b1, b2, b3);
-          mma_bf16(c, qa[ks], b0, b1);
-          mma_bf16(c, qa[ks + 1], b2, b3);
-        }
-        const int key = j * kBlock + nt * 8 + 2 * tq;
-        if (key <= pA) mA = fmaxf(mA, c[0]);
-        if (key + 1 <= pA) mA = fmaxf(mA, c[1]);
-        if (key <= pB) mB = fmaxf(mB, c[2]);
-        if (key + 1 <= pB) mB = fmaxf(mB, c[3]);
-      }
-      mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, 1));
-      mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, 2));
-      mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, 1));
-      mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, 2));
-      if (tq == 0) {
-        if (inA && j * kBlock <= pA) scores[((int64_t)rowA * Hkv + h) * max_blocks + j] = mA;
-        if (inB && j * kBlock <= pB) scores[((int64_t)rowB * Hkv + h) * max_blocks + j] = mB;
-      }
-      __syncthreads();
-    }
-    cp_async_wait<0>();
-  }
-}
 
 // ------------------------------------------------------------ CSR
 // Row (h, r, j) of the key-block -> query CSR lists, ascending, the tokens of
@@ -706,24 +583,6 @@ msa_status set_smem(K kernel, size_t bytes) {
 }
 
 }  // namespace
-
-msa_status prefill_index_score(const msa_config& c, const WsView& v, const void* idx_q,
-                               const void* idx_k, float* scores, cudaStream_t s) {
-  const int T = max_tokens_of(c);
-  dim3 grid((T + kScoreTokens - 1) / kScoreTokens, c.num_kv_heads);
-  const size_t smem = 2u * kBlock * c.index_dim * 2;
-  msa_status st;
-  if (c.index_dim == 128) {
-    if ((st = set_smem(prefill_score_kernel<128>, smem)) != MSA_OK) return st;
-    return launch_pdl(prefill_score_kernel<128>, grid, dim3(kScoreThreads), smem, s, v,
-                      c.num_kv_heads, c.max_blocks_per_req, (const __nv_bfloat16*)idx_q,
-                      (const uint8_t*)idx_k, scores);
-  }
-  if ((st = set_smem(prefill_score_kernel<64>, smem)) != MSA_OK) return st;
-  return launch_pdl(prefill_score_kernel<64>, grid, dim3(kScoreThreads), smem, s, v,
-                    c.num_kv_heads, c.max_blocks_per_req, (const __nv_bfloat16*)idx_q,
-                    (const uint8_t*)idx_k, scores);
-}
 
 }  // namespace msa
 
