@@ -44,9 +44,9 @@ FALLBACK_HBM_GBS = 6800.0
 # kernel, from the ncu capture summarised in profiles/ (None until captured for
 # the current kernel).
 NCU_TRAFFIC_BYTES = {
-    # batch-8 / 2048-page capture: 372.6 MB for 367.7 MB algorithmic, scaled by
-    # bytes to a full medium-decode launch (1.2608 GB algorithmic)
-    ("medium_decode", "index_score"): 1.2776e9,
+    # batch-8 / 2048-page capture of the current kernel: 372.4 MB for 367.7 MB
+    # algorithmic, scaled by bytes to a full medium-decode launch (1.2608 GB)
+    ("medium_decode", "index_score"): 1.2769e9,
 }
 
 
