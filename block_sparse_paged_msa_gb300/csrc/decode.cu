@@ -10,10 +10,12 @@
 //
 // Work item = (query token t, KV head h, split s); a split is a run of
 // consecutive slots of t's selected list.  Design (GB300):
-//  * a persistent grid (two 160-thread CTAs per SM) strides over the work
-//    items; in each CTA one producer warp streams, for every selected block,
-//    the block's K tile and V tile ([128 tokens][128 dims], contiguous per page
-//    and KV head in the HND pool: 32 KiB bf16, 16 KiB e4m3) with 2-D TMA loads
+//  * a persistent grid (two 192-thread CTAs per SM) strides over the work
+//    items; in each CTA a scheduler warp resolves the next items (pages and
+//    visible rows of their blocks, the item's Q rows) into a small ring of
+//    item records, and a loader warp streams, for every selected block, the
+//    block's K tile and V tile ([128 tokens][128 dims], contiguous per page and
+//    KV head in the HND pool: 32 KiB bf16, 16 KiB e4m3) with 2-D TMA loads
 //    (128-byte swizzle) into a ring of shared-memory stages guarded by
 //    mbarriers -- so the copies of the next items are already in flight while
 //    the current one is being finished;

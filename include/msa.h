@@ -186,7 +186,8 @@ msa_status msa_plan_from_req_to_token(const msa_config* cfg, int32_t batch,
  * tests).  Entries j >= the token's visible block count are not written.
  * Decode mode: bandwidth-bound, every visible index key read once per request
  * (q_len <= 4 queries share each load).  Prefill mode: tensor-core tiles of
- * 64 query tokens x one 128-key block, causal.
+ * 128 query tokens x two 128-key blocks (tcgen05, fp32 accumulators in tensor
+ * memory), causal.  idx_q and idx_k_pages must be 16-byte aligned.
  */
 msa_status msa_index_score(const msa_config* cfg, const void* ws, const void* idx_q,
                            const void* idx_k_pages, float* block_scores,
@@ -221,7 +222,10 @@ msa_status msa_sparse_decode(const msa_config* cfg, void* ws, const void* q,
  * msa_combine -- log-sum-exp merge of the split-K partials in ws
  * (FlashMLA decode in sglang flashmla_backend.py returns (o, lse) per split
  * plan): lse = ln sum_s exp(lse_s), out = sum_s exp(lse_s - lse) o_s, out
- * rounded to bf16.  All splits empty -> out = 0, lse = -inf.
+ * rounded to bf16.  All splits empty -> out = 0, lse = -inf.  Decode mode
+ * merges the splits of msa_sparse_decode; prefill mode the selected slots of
+ * msa_sparse_prefill (each token's first min(nb, S) slots).  out must be
+ * 8-byte aligned (decode) or 16-byte aligned (prefill).
  */
 msa_status msa_combine(const msa_config* cfg, const void* ws, void* out, float* lse,
                        msa_stream_t stream);
@@ -236,7 +240,11 @@ msa_status msa_combine(const msa_config* cfg, const void* ws, void* out, float* 
  *   msa_k2q_capacity(cfg)  an upper bound of the entries (q_indices length)
  * msa_build_k2q_csr (prefill mode only) fills row_ptr (prefix sums, row_ptr[0]
  * = 0) and q_indices: row (h, r, j) lists, ascending, the token indices t of
- * request r whose selected[t, h, :] contains j.  Deterministic.
+ * request r whose selected[t, h, :] contains j (j visible to t).
+ * Deterministic.  It also records in ws, for every (token, KV head, slot of
+ * the selected list), the CSR entry that holds it, which msa_sparse_prefill's
+ * output layout and msa_combine use: run it on the selections of this step,
+ * after msa_plan, before msa_sparse_prefill.
  */
 int64_t msa_k2q_rows(const msa_config* cfg);
 int64_t msa_k2q_capacity(const msa_config* cfg);
@@ -249,8 +257,11 @@ msa_status msa_build_k2q_csr(const msa_config* cfg, const void* ws, const int32_
  * causal = True, page_table and the CSR).  One tile per CSR row: the row's
  * tokens x their GQA query heads against the block's 128 keys, causal inside
  * the block that holds the token.  Writes one normalised fp16 partial and its
- * LSE per (token, query head, selected slot) into ws; msa_combine merges them
- * into out / lse.  Prefill mode, bf16 KV only (fp8 -> MSA_ERR_UNSUPPORTED).
+ * LSE per (CSR entry, query head of the entry's KV group) into ws, row entry *
+ * G + g, so that a tile's rows are contiguous; msa_combine merges each token's
+ * slots into out / lse.  selected is not read (the CSR build recorded what it
+ * needs).  q, k_pages and v_pages must be 16-byte aligned.  Prefill mode, bf16
+ * KV only (fp8 -> MSA_ERR_UNSUPPORTED).
  */
 msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const void* q,
                               const void* k_pages, const void* v_pages,
