@@ -251,15 +251,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
-
-// 1-D bulk copy (TMA engine) from shared to global memory, tracked in this
-// thread's bulk-async group; `bytes` a multiple of 16, both addresses 16-byte
-// aligned.
-__device__ __forceinline__ void bulk_store(void* gdst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
-               "r"(smem_u32(src)), "r"(bytes)
-               : "memory");
-}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

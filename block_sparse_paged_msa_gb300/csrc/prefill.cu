@@ -171,6 +171,18 @@ constexpr int kTcThreads = (9 + kLoaderWarps) * 32;   // 2 softmax warpgroups, M
 constexpr int kTileBytes = kBlock * kHeadDim * 2;
 constexpr int kTcSmemBytes = 6 * kTileBytes + 1024;
 
+// Q tile layout ("half-interleaved", K-major, 128-byte swizzle): rows in
+// groups of 8; a group holds its rows' columns 0..63 (1 KB, one swizzle atom)
+// then columns 64..127 (1 KB), so one token's 8 rows x 128 columns are one
+// contiguous 2 KB TMA box.  Byte offset of 16-byte chunk c of row r:
+__device__ __forceinline__ uint32_t qmaj_off(int r, int c) {
+  return (uint32_t)((r >> 3) * 2048 + (c >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+// Descriptor of K step ks (16 columns) of that tile: 2 KB between 8-row groups.
+__device__ __forceinline__ uint64_t qstep_desc(uint32_t base, int ks) {
+  return sdesc_sw128_sbo(base + (uint32_t)((ks >> 2) * 1024 + (ks & 3) * 32), 2048);
+}
+
 struct PrefillArgs {
   int Hkv, Hq, G, S, B, NB;
   float scale_log2;
@@ -325,11 +337,14 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
             if (lw == 0) mbar_arrive_expect_tx(&q_full[w], (uint32_t)(nt * G * 256));
             else mbar_arrive(&q_full[w]);
           }
-          const int b = lane * kLoaderWarps + lw;   // box: token b / 2, half b % 2
-          if (b < 2 * nt) {
-            const int y = a.q_idx[e0 + (b >> 1)] * a.Hq + h * G;
-            uint8_t* dst = Qb + w * kTileBytes + (b >> 1) * G * 128 + (b & 1) * (kTileBytes / 2);
-            tma_load_2d(dst, &tmap_q, (b & 1) * 64, y, &q_full[w]);
+          // box b: 8 rows (token b / (G / 8), rows 8 (b % (G / 8)) ...) x both
+          // 64-column halves, one 2 KB group of the half-interleaved Q tile
+          const int gpt = G >> 3;
+          const int b = lane * kLoaderWarps + lw;
+          if (b < nt * gpt) {
+            const int tk = b / gpt, sub = b - tk * gpt;
+            const int y = a.q_idx[e0 + tk] * a.Hq + h * G + 8 * sub;
+            tma_load_3d(Qb + w * kTileBytes + b * 2048, &tmap_q, 0, y, 0, &q_full[w]);
           }
           continue;
         }
@@ -349,7 +364,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
           }
           const __nv_bfloat16* src = a.q + ((int64_t)(tk < 0 ? 0 : tk) * a.Hq + h * G +
                                             (rr & (G - 1))) * kHeadDim + c * 8;
-          cp_async16(qdst + kmaj_off(rr, c, 128), src, tk < 0 ? 0 : 16);
+          cp_async16(qdst + qmaj_off(rr, c), src, tk < 0 ? 0 : 16);
         }
         cp_async_commit();
         cp_async_wait<0>();
@@ -378,7 +393,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
               const uint32_t qs = smem_u32(Qb + w * kTileBytes);
 #pragma unroll
               for (int ks = 0; ks < 8; ++ks)
-                umma_f16(tbase + 256 * w, kstep_desc(qs, ks, 128), kstep_desc(kts, ks, 128),
+                umma_f16(tbase + 256 * w, qstep_desc(qs, ks), kstep_desc(kts, ks, 128),
                          idesc_s, ks > 0);
               umma_commit(&s_ready[w]);
               ++kS[w];
@@ -668,9 +683,14 @@ extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const 
   CUtensorMap tk, tv, tq;
   if (!make_pool_map(&tk, k_pages, prow, false) || !make_pool_map(&tv, v_pages, prow, false))
     return MSA_ERR_CUDA;
-  // queries as [tokens * H_q, 128]; boxes of one token's G heads (G >= 8)
-  if (!make_pool_map(&tq, q, (int64_t)max_tokens_of(*cfg) * a.Hq, false, a.G >= 8 ? a.G : 8))
-    return MSA_ERR_CUDA;
+  // queries as [half (2)][row (tokens * H_q)][64 columns]: a box of 8 rows x
+  // both halves is one 2 KB group of the half-interleaved Q tile (G >= 8)
+  {
+    const int64_t dims[3] = {64, (int64_t)max_tokens_of(*cfg) * a.Hq, 2};
+    const int64_t str[2] = {(int64_t)kHeadDim * 2, 128};
+    const int box[3] = {64, 8, 2};
+    if (!make_bf16_map(&tq, q, 3, dims, str, box)) return MSA_ERR_CUDA;
+  }
   // fp16 partial rows [T * H_q * S, 128] (2-byte elements, copied as bits):
   // whole M-tiles and 8-row boxes
   const int64_t orows = (int64_t)max_tokens_of(*cfg) * a.Hq * a.S;

@@ -51,6 +51,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
          ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// As sdesc_sw128 with another stride between 8-row groups (a multiple of 16).
+__device__ __forceinline__ uint64_t sdesc_sw128_sbo(uint32_t saddr, uint32_t sbo_bytes) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) |
+         ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor of kind::f16 with fp32 accumulation, both operands
 // K-major.  fmt: 0 = fp16, 1 = bf16 (A and B must share it).
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t fmt, uint32_t M, uint32_t N) {
