@@ -290,12 +290,20 @@ def run_ours(args, rank, world, local_rank):
     launches_per_step = {"plan": 1, "index_score": 1, "topk_select": 1, "build_k2q_csr": 6,
                          "sparse_prefill": 1, "sparse_decode": 1, "combine": 1}
 
-    def step(evs=None):
+    dominant = "sparse_prefill" if sa.prefill else "index_score"
+    dom_i = names.index(dominant)
+
+    def step(evs=None, only=None):
+        """One step; events around every call (evs) or only around call `only`.
+        An event between two kernels keeps the second from launching early
+        (programmatic dependent launch), so the timed steps bracket only the
+        dominant kernel."""
         for i, (_, fn) in enumerate(calls):
-            if evs is not None:
+            timed = evs is not None and (only is None or i == only)
+            if timed:
                 evs[i][0].record(stream)
             fn()
-            if evs is not None:
+            if timed:
                 evs[i][1].record(stream)
 
     for _ in range(args.warmup):
@@ -313,13 +321,19 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         start.record(stream)
         for k in range(K):
-            step(evs[k])
+            step(evs[k], only=dom_i)
         stop.record(stream)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
     ms = start.elapsed_time(stop)
-    per_kernel = {n: sum(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(K)) / K
+    dom_ms = sum(evs[k][dom_i][0].elapsed_time(evs[k][dom_i][1]) for k in range(K)) / K
+    # per-kernel breakdown, after the timed region (every call bracketed)
+    Kb = min(K, 200)
+    for k in range(Kb):
+        step(evs[k])
+    torch.cuda.synchronize()
+    per_kernel = {n: sum(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(Kb)) / Kb
                   for i, n in enumerate(names)}
 
     # ---- e2e: host buffers in, result out, through the public API
@@ -380,6 +394,8 @@ def run_ours(args, rank, world, local_rank):
                    msa.ops.local_blocks_from_tokens(spec.local_tokens), spec.topk_blocks],
                    "pool_pages": spec.num_pages, "parallelism": f"replicas{world}"},
         "kernels_ms": per_kernel,
+        "kernels_ms_note": ("dominant kernel timed in the timed region; the others in "
+                            f"{Kb} further steps with every call bracketed by events"),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": sum(launches_per_step[n] for n in names) * K,
@@ -388,11 +404,12 @@ def run_ours(args, rank, world, local_rank):
     if sa.prefill:
         fl = prefill_flops(w, sa.selected)
         achieved = {n: fl[n] / (per_kernel[n] / 1e3) / 1e12 for n in ("index_score", "sparse_prefill")}
+        achieved["sparse_prefill"] = fl["sparse_prefill"] / (dom_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
         result["roofline"] = {
             "bound": "tensor", "kernel": "sparse_prefill", "achieved": achieved["sparse_prefill"],
             "peak": peak[0], "unit": "TFLOP/s", "frac": achieved["sparse_prefill"] / peak[0],
-            "peak_source": f"{peak[1]} bf16_tflops_sustained",
+            "peak_source": f"{peak[1]} bf16_tflops_sustained", "launch_ms": dom_ms,
             "traffic": NCU_TRAFFIC_BYTES.get((spec.name, "sparse_prefill"))}
         result["kernel_tflops"] = achieved
         result["flops_per_step"] = {k: fl[k] for k in ("index_score", "sparse_prefill")}
@@ -401,11 +418,11 @@ def run_ours(args, rank, world, local_rank):
         ab = algorithmic_bytes(w)
         db = decode_bytes(w, sa.selected, msa.num_splits(cfg))
         peak = peaks["hbm_gbs"]
-        idx_gbs = ab["index_score"] / (per_kernel["index_score"] / 1e3) / 1e9
+        idx_gbs = ab["index_score"] / (dom_ms / 1e3) / 1e9
         step_bytes = ab["index_score"] + db["decode"] + db["combine"]
         result["roofline"] = {"bound": "hbm", "kernel": "index_score", "achieved": idx_gbs,
                               "peak": peak[0], "unit": "GB/s", "frac": idx_gbs / peak[0],
-                              "peak_source": f"{peak[1]} hbm_gbs",
+                              "peak_source": f"{peak[1]} hbm_gbs", "launch_ms": dom_ms,
                               "traffic": NCU_TRAFFIC_BYTES.get((spec.name, "index_score"))}
         result["step_hbm"] = {"algorithmic_bytes": step_bytes,
                               "achieved_gbs": step_bytes / (ms / K / 1e3) / 1e9,
