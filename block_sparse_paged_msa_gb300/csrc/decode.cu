@@ -177,9 +177,16 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
     // -------------------------------------------------------- scheduler
     // Resolves each work item (token metadata -> selected slots -> pages) and
     // publishes it with the item's Q rows, up to kItems ahead of the others.
+    // Items are handed out dynamically (an atomic counter in the workspace
+    // header), so CTAs that drew cheap items take more of them.
     int islot = 0;
     uint32_t iphase = 0;
-    for (int idx = blockIdx.x; idx < a.n_items; idx += gridDim.x) {
+    auto grab = [&]() {
+      int i = 0;
+      if (lane == 0) i = atomicAdd(&ws.hdr->work_next, 1);
+      return __shfl_sync(0xffffffffu, i, 0);
+    };
+    for (int idx = grab(); idx < a.n_items; idx = grab()) {
       const Item it = item_of(ws, a, idx);
       if (!it.active) continue;
       const ItemBlocks bl = item_blocks(ws, a, it.t, it.h, it.s, it.r, it.pos, lane);
@@ -210,6 +217,12 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
       mbar_wait(&item_empty[islot], iphase ^ 1u, ws.hdr);
       meta[islot].t = -1;
       mbar_arrive(&item_full[islot]);
+      // the last CTA to stop taking items resets the counters for the next
+      // launch on this workspace
+      if (atomicAdd(&ws.hdr->work_done, 1) == (int)gridDim.x - 1) {
+        ws.hdr->work_next = 0;
+        ws.hdr->work_done = 0;
+      }
     }
     return;
   }

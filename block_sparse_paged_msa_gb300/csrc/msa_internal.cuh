@@ -26,6 +26,9 @@ struct WsHeader {
   int32_t num_tokens;     // T of the current plan
   int32_t total_blocks;   // sum over requests of ceil(seq_len / P)
   int32_t max_batch;      // number of plan_err words
+  int32_t work_next;      // msa_sparse_decode: next work item to hand out
+  int32_t work_done;      //   and CTAs done taking items (both zeroed by the plan
+                          //   and by the last CTA of each launch)
 };
 
 inline size_t align_up(size_t x, size_t a = 256) { return (x + a - 1) / a * a; }

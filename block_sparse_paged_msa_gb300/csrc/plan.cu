@@ -165,6 +165,8 @@ plan_kernel(WsView ws, int batch, int max_batch, int Hkv, int q_len, int max_blo
   if (r == 0 && tid == 0) {
     ws.hdr->err = 0;         // later kernels' bits; this kernel reports in plan_err
     ws.hdr->max_batch = max_batch;
+    ws.hdr->work_next = 0;
+    ws.hdr->work_done = 0;
   }
   if (r < batch) {
     ReqInfo ri = request_info(r, seq_lens, cu_q, q_len, max_blocks, max_tokens);
