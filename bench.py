@@ -287,7 +287,7 @@ def run_ours(args, rank, world, local_rank):
                                                               w.v_pages, sa.selected))]
     calls += [("combine", lambda: msa.combine(c, sa.ws, sa.out, sa.lse))]
     names = [n for n, _ in calls]
-    launches_per_step = {"plan": 1, "index_score": 1, "topk_select": 1, "build_k2q_csr": 6,
+    launches_per_step = {"plan": 1, "index_score": 1, "topk_select": 1, "build_k2q_csr": 7,
                          "sparse_prefill": 1, "sparse_decode": 1, "combine": 1}
 
     dominant = "sparse_prefill" if sa.prefill else "index_score"

@@ -169,7 +169,7 @@ constexpr int kTilesPerItem = 16;
 constexpr int kLoaderWarps = 3;          // Q loaders (TMA issue from one warp is slow)
 constexpr int kTcThreads = (9 + kLoaderWarps) * 32;   // 2 softmax warpgroups, MMA issuer
 constexpr int kTileBytes = kBlock * kHeadDim * 2;
-constexpr int kTcSmemBytes = 6 * kTileBytes + 1024;
+constexpr int kTcSmemBytes = 7 * kTileBytes + 1024;
 
 // Q tile layout ("half-interleaved", K-major, 128-byte swizzle): rows in
 // groups of 8; a group holds its rows' columns 0..63 (1 KB, one swizzle atom)
@@ -221,9 +221,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   uint8_t* Kt = smem;                          // K tile, bf16, K-major SW128 [key][d]
   uint8_t* VT = smem + kTileBytes;             // V^T, fp16, K-major SW128 [d][key]
   uint8_t* Pb = smem + 2 * kTileBytes;         // O staging tiles [2], fp16 [row][d]
-  uint8_t* Vst = Pb + kTileBytes;              // V staging (bf16 [key][d]) = P[1]
   uint8_t* Qb = Pb + 2 * kTileBytes;           // Q[2], bf16 [row][d]
-  __shared__ __align__(8) uint64_t kv_full, q_full[2], s_ready[2], p_ready[2], o_ready[2];
+  uint8_t* Vst = Qb + 2 * kTileBytes;          // V of the next row (bf16 [key][d])
+  __shared__ __align__(8) uint64_t k_full, v_full, k_free, vt_ready, q_full[2], s_ready[2],
+      p_ready[2], o_ready[2];
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool issuer = warp == 8, loader = warp >= 9;
@@ -231,7 +232,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   const int wg = warp >> 2;                    // softmax warpgroup (0, 1)
   const int wtid = tid & 127;                  // = this thread's row / TMEM lane
   if (tid == 0) {
-    mbar_init(&kv_full, 1);
+    mbar_init(&k_full, 1);
+    mbar_init(&v_full, 1);
+    mbar_init(&k_free, 1);
+    mbar_init(&vt_ready, 256);                 // the softmax warps, after the transpose
     for (int w = 0; w < 2; ++w) {
       mbar_init(&q_full[w], kLoaderWarps);
       mbar_init(&s_ready[w], 1);
@@ -256,18 +260,54 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   const int tok_per_item = kTilesPerItem * TPT;
   const int n_items = ws.sched[rows];
   const uint32_t idesc_s = idesc_f16(1, 128, 128), idesc_o = idesc_f16(0, 128, 128);
-  uint32_t kv_phase = 0;
+  uint32_t k_phase = 0, v_phase = 0, kf_phase = 0, vt_phase = 0;
+  int pf_row = -1;                             // issuer: row whose K / V are on the way
   int kS[2] = {0, 0}, kP[2] = {0, 0};          // issuer: S / PV issued per warpgroup
   int kL0 = 0, kL1 = 0;                        // loader: Q tiles loaded per warpgroup
   int kW = 0;                                  // warpgroup: tiles done
   int cur_row = -1;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    int lo = 0, hi = (int)rows - 1;            // row of this item
+  // CSR row of work item `it`: the last row whose first item is <= it
+  auto row_of = [&](int it) {
+    int lo = 0, hi = (int)rows - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (ws.sched[mid] <= item) lo = mid; else hi = mid - 1;
+      if (ws.sched[mid] <= it) lo = mid; else hi = mid - 1;
     }
-    const int row = lo, chunk = item - ws.sched[row];
+    return lo;
+  };
+  // K / V tiles of CSR row rw: K into the K tile, V into the V staging tile
+  auto load_k = [&](int rw) {
+    const int jj = rw % a.NB, rr = (rw / a.NB) % a.B, hh = rw / (a.NB * a.B);
+    const int pg = ws.block_table[(int64_t)rr * a.NB + jj];
+    const int y = ((pg < 0 ? 0 : pg) * a.Hkv + hh) * kBlock;
+    mbar_arrive_expect_tx(&k_full, kTileBytes);
+    tma_load_2d(Kt, &tmap_k, 0, y, &k_full);
+    tma_load_2d(Kt + kTileBytes / 2, &tmap_k, 64, y, &k_full);
+  };
+  auto load_v = [&](int rw) {
+    const int jj = rw % a.NB, rr = (rw / a.NB) % a.B, hh = rw / (a.NB * a.B);
+    const int pg = ws.block_table[(int64_t)rr * a.NB + jj];
+    const int y = ((pg < 0 ? 0 : pg) * a.Hkv + hh) * kBlock;
+    mbar_arrive_expect_tx(&v_full, kTileBytes);
+    tma_load_2d(Vst, &tmap_v, 0, y, &v_full);
+    tma_load_2d(Vst + kTileBytes / 2, &tmap_v, 64, y, &v_full);
+  };
+  // row of the next item of this CTA if it will be processed and needs other
+  // K / V than `rw`, else -1 (issuer only)
+  auto next_row = [&](int kk, int rw) {
+    if (kk + (int)gridDim.x >= n_items) return -1;
+    const int nit = ws.item_order[kk + gridDim.x];
+    const int nr = row_of(nit);
+    if (nr == rw) return -1;
+    const int nb_ = a.row_ptr[nr] + (nit - ws.sched[nr]) * tok_per_item;
+    const int ne_ = min(a.row_ptr[nr + 1], nb_ + tok_per_item);
+    const int nj = nr % a.NB, nrr = (nr / a.NB) % a.B;
+    if (ws.block_table[(int64_t)nrr * a.NB + nj] < 0 || nb_ >= ne_) return -1;
+    return nr;
+  };
+  for (int k = blockIdx.x; k < n_items; k += gridDim.x) {
+    const int item = ws.item_order[k];           // largest items first
+    const int row = row_of(item), chunk = item - ws.sched[row];
     const int j = row % a.NB, r = (row / a.NB) % a.B, h = row / (a.NB * a.B);
     const int beg = a.row_ptr[row] + chunk * tok_per_item;
     const int end = min(a.row_ptr[row + 1], beg + tok_per_item);
@@ -278,20 +318,21 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
 
     // the previous item's MMAs are done; a new row also overwrites P[1] (V
     // staging), so the output rows staged there must have been read
-    if (warp < 8 && row != cur_row) bulk_wait_read();
-    named_bar_sync(1, kTcThreads);
-    if (row != cur_row) {
-      if (issuer && lane == 0) {
-        const int y = (page * a.Hkv + h) * kBlock;
-        mbar_arrive_expect_tx(&kv_full, 2 * kTileBytes);
-        tma_load_2d(Kt, &tmap_k, 0, y, &kv_full);
-        tma_load_2d(Kt + kTileBytes / 2, &tmap_k, 64, y, &kv_full);
-        tma_load_2d(Vst, &tmap_v, 0, y, &kv_full);
-        tma_load_2d(Vst + kTileBytes / 2, &tmap_v, 64, y, &kv_full);
-      }
-      mbar_wait(&kv_full, kv_phase, ws.hdr);
-      kv_phase ^= 1u;
-      if (warp < 8) {
+    // The loaders run ahead across items (their Q buffers are tracked per
+    // tile); the others meet here once the previous item's MMAs are done.
+    if (!loader) named_bar_sync(1, kTcThreads - 32 * kLoaderWarps);
+    const bool new_row = row != cur_row;
+    // A new row's K and V were prefetched during the previous item (K once its
+    // last S had read the K tile); otherwise (first item, or the previous
+    // item did not know) they are requested now.
+    if (new_row && issuer && lane == 0 && pf_row != row) {
+      load_k(row);
+      load_v(row);
+    }
+    if (new_row && warp < 8) {
+      mbar_wait(&v_full, v_phase, ws.hdr);
+      v_phase ^= 1u;
+      {
         // V [key][d] bf16 -> V^T [d][key] fp16 (keys past the last visible
         // token become 0, whatever the page holds there)
         const uint32_t vs = smem_u32(Vst);
@@ -312,9 +353,12 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
         }
         fence_proxy_async_smem();
       }
-      named_bar_sync(1, kTcThreads);
-      cur_row = row;
+      // V^T is ready for the PV MMAs and the V staging tile is free; the
+      // issuer has meanwhile started the item's S MMAs
+      tc_fence_before();
+      mbar_arrive(&vt_ready);
     }
+    cur_row = row;
 
     if (loader) {
       // ------------------------------------------------------------ Q rows
@@ -378,11 +422,33 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     if (issuer) {
       if (lane == 0) {
         const uint32_t kts = smem_u32(Kt), vts = smem_u32(VT);
+        const int nrow = next_row(k, row);
+        if (new_row) {
+          mbar_wait(&k_full, k_phase, ws.hdr);
+          k_phase ^= 1u;
+        }
+        bool vt_ok = !new_row;                   // V^T of this row written
+        // same row as the last item: no transpose, the V staging tile is free
+        if (vt_ok && nrow >= 0) load_v(nrow);
+        pf_row = nrow;
+        bool k_done = nrow < 0;                  // the next row's K is requested
         int nS[2] = {0, 0}, nP[2] = {0, 0};      // this item's S / PV per warpgroup
         const int want[2] = {(ntiles + 1) / 2, ntiles / 2};
         uint32_t spins = 0;
         while (nP[0] < want[0] || nP[1] < want[1]) {
           bool did = false;
+          // once this item's S MMAs have all completed, the next row's K
+          if (!k_done && nS[0] == want[0] && nS[1] == want[1] &&
+              mbar_test_wait(&k_free, kf_phase)) {
+            load_k(nrow);
+            k_done = true;
+          }
+          if (!vt_ok && mbar_test_wait(&vt_ready, vt_phase)) {
+            vt_ok = true;
+            vt_phase ^= 1u;
+            tc_fence_after();
+            if (nrow >= 0) load_v(nrow);         // the V staging tile is free again
+          }
 #pragma unroll
           for (int w = 0; w < 2; ++w) {
             // S_k overwrites P_{k-1}: only once O_{k-1} = P_{k-1} V completed
@@ -398,9 +464,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
               umma_commit(&s_ready[w]);
               ++kS[w];
               ++nS[w];
+              if (nS[0] == want[0] && nS[1] == want[1]) umma_commit(&k_free);   // last S
               did = true;
             }
-            if (nP[w] < nS[w] && mbar_test_wait(&p_ready[w], (uint32_t)(kP[w] & 1))) {
+            if (vt_ok && nP[w] < nS[w] && mbar_test_wait(&p_ready[w], (uint32_t)(kP[w] & 1))) {
               tc_fence_after();
 #pragma unroll
               for (int ks = 0; ks < 8; ++ks)
@@ -418,6 +485,16 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
             atomicOr(&ws.hdr->err, MSA_DEVERR_TIMEOUT);
             break;
           }
+        }
+        // k_free completes once per item: consume it (and request K if the
+        // loop ended first)
+        mbar_wait(&k_free, kf_phase, ws.hdr);
+        kf_phase ^= 1u;
+        if (!k_done) load_k(nrow);
+        if (!vt_ok) {                            // only on a timeout above
+          mbar_wait(&vt_ready, vt_phase, ws.hdr);
+          vt_phase ^= 1u;
+          if (nrow >= 0) load_v(nrow);
         }
       }
       __syncwarp();
@@ -595,6 +672,41 @@ sched_count_kernel(const int32_t* __restrict__ row_ptr, int32_t* __restrict__ sc
   if (blockIdx.x == 0 && threadIdx.x == 0) sched[0] = 0;
 }
 
+// The work items ordered by their tile count, largest first (a counting sort
+// in one CTA), so that the CTAs' round-robin share of the items comes out even.
+__global__ void __launch_bounds__(1024)
+item_order_kernel(const int32_t* __restrict__ row_ptr, WsView ws, int64_t rows, int tok_per_item,
+                  int tpt) {
+  __shared__ int cnt[kTilesPerItem + 1], base[kTilesPerItem + 1];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int tid = threadIdx.x;
+  if (tid <= kTilesPerItem) cnt[tid] = 0;
+  __syncthreads();
+  auto items_of = [&](int64_t row, auto&& fn) {
+    const int n = row_ptr[row + 1] - row_ptr[row];
+    for (int k = 0; k * tok_per_item < n; ++k) {
+      const int m = min(tok_per_item, n - k * tok_per_item);
+      fn(k, (m + tpt - 1) / tpt);
+    }
+  };
+  for (int64_t row = tid; row < rows; row += 1024)
+    items_of(row, [&](int, int sz) { atomicAdd(&cnt[sz], 1); });
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int sz = kTilesPerItem; sz >= 0; --sz) {
+      base[sz] = run;
+      run += cnt[sz];
+    }
+  }
+  __syncthreads();
+  for (int64_t row = tid; row < rows; row += 1024) {
+    const int first = ws.sched[row];
+    items_of(row, [&](int k, int sz) { ws.item_order[atomicAdd(&base[sz], 1)] = first + k; });
+  }
+}
+
 template <typename K>
 msa_status set_smem(K kernel, size_t bytes) {
   static std::mutex mu;
@@ -658,7 +770,10 @@ extern "C" msa_status msa_build_k2q_csr(const msa_config* cfg, const void* ws,
   if ((st = launch_pdl(sched_count_kernel, dim3(sgrid), dim3(256), 0, s, (const int32_t*)row_ptr,
                        v.sched, rows, tok_per_item)) != MSA_OK)
     return st;
-  return launch_pdl(csr_scan_kernel, dim3(1), dim3(1024), 0, s, v.sched, rows);
+  if ((st = launch_pdl(csr_scan_kernel, dim3(1), dim3(1024), 0, s, v.sched, rows)) != MSA_OK)
+    return st;
+  return launch_pdl(item_order_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)row_ptr, v, rows,
+                    tok_per_item, kBlock / G);
 }
 
 extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const void* q,
