@@ -163,9 +163,10 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(int32_t* __restrict__ ro
 // ------------------------------------------------------------ attention
 // Work items: a CSR row's tokens in chunks of kTilesPerItem M-tiles of 128
 // rows (tokens x GQA heads); msa_build_k2q_csr writes the first item of every
-// row (ws.sched), so the huge rows of the init / local blocks are split
-// instead of dominating the tail.
-constexpr int kTilesPerItem = 16;
+// row (ws.sched) and the items ordered largest first (ws.item_order), so the
+// huge rows of the init / local blocks are split and the CTAs' round-robin
+// shares come out even.
+constexpr int kTilesPerItem = 32;
 constexpr int kLoaderWarps = 3;          // Q loaders (TMA issue from one warp is slow)
 constexpr int kTcThreads = (9 + kLoaderWarps) * 32;   // 2 softmax warpgroups, MMA issuer
 constexpr int kTileBytes = kBlock * kHeadDim * 2;
