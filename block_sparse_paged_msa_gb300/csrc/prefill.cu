@@ -193,22 +193,23 @@ struct PrefillArgs {
 };
 
 // Persistent: one CTA per SM walks the work items.  Per CSR row (KV head h,
-// request r, key block j) the K tile and the V tile arrive by TMA; V is
-// transposed once into an fp16 K-major tile (V^T), the B operand of O = P V.
-// M-tiles alternate between the two softmax warpgroups; warpgroup w's k-th
-// tile (counted over the whole kernel) goes through
+// request r, key block j) the K tile and the V tile arrive by TMA (the next
+// row's V during the current item, into the second V buffer; its K once the
+// current item's last S has read the K tile); V is converted to fp16 in
+// place and read by O = P V as an MN-major B operand.  M-tiles alternate
+// between the two softmax warpgroups; warpgroup w's k-th tile (counted over
+// the whole kernel) goes through
 //   loaders: Q_k rows -> Q[w] (TMA)  once S_{k-1} has read Q[w]      (q_full)
 //   issuer:  S_k = Q_k K^T (bf16) into TMEM region w, once Q_k landed and
 //            O_{k-1} = P_{k-1} V has finished reading P_{k-1}      (s_ready)
 //   WG:      S_k -> registers (thread = row), causal mask, softmax; P_k
 //            (fp16) written over S_k's first 64 TMEM columns      (p_ready)
 //   issuer:  O_k = P_k V (A operand from TMEM, fp16)                (o_ready)
-//   WG:      O_k -> normalised fp16 row -> P[w] staging tile (swizzled) ->
+//   WG:      O_k -> normalised fp16 row -> staging tile w (swizzled) ->
 //            TMA tile stores into the partials, LSE beside them.
 // TMEM: per warpgroup 128 columns of S / P and 128 of O (512 in all).  P
-// never touches shared memory, which the two SS MMAs of 128 x 128 tiles
-// otherwise keep close to saturated.  The issuer polls both warpgroups and
-// serves whichever is ready.
+// never touches shared memory.  The issuer polls both warpgroups and serves
+// whichever is ready; the loaders run ahead across items.
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
@@ -220,10 +221,12 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   // launch asks for 1 KB of slack)
   uint8_t* smem = tc_smem_raw + ((1024u - (smem_u32(tc_smem_raw) & 1023u)) & 1023u);
   uint8_t* Kt = smem;                          // K tile, bf16, K-major SW128 [key][d]
-  uint8_t* VT = smem + kTileBytes;             // V^T, fp16, K-major SW128 [d][key]
+  // V of the current row and of the next one, [key][d] as TMA lands it; the
+  // current one converted to fp16 in place is the MN-major B operand of P V
+  auto Vb = [&](int i) { return i ? smem + 6 * kTileBytes : smem + kTileBytes; };
   uint8_t* Pb = smem + 2 * kTileBytes;         // O staging tiles [2], fp16 [row][d]
   uint8_t* Qb = Pb + 2 * kTileBytes;           // Q[2], bf16 [row][d]
-  uint8_t* Vst = Qb + 2 * kTileBytes;          // V of the next row (bf16 [key][d])
+
   __shared__ __align__(8) uint64_t k_full, v_full, k_free, vt_ready, q_full[2], s_ready[2],
       p_ready[2], o_ready[2];
   __shared__ uint32_t tmem_base;
@@ -260,9 +263,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   const int lgG = __ffs(G) - 1;                // G divides 16
   const int tok_per_item = kTilesPerItem * TPT;
   const int n_items = ws.sched[rows];
-  const uint32_t idesc_s = idesc_f16(1, 128, 128), idesc_o = idesc_f16(0, 128, 128);
+  const uint32_t idesc_s = idesc_f16(1, 128, 128), idesc_o = idesc_f16_bmn(0, 128, 128);
   uint32_t k_phase = 0, v_phase = 0, kf_phase = 0, vt_phase = 0;
   int pf_row = -1;                             // issuer: row whose K / V are on the way
+  int vsel = 1;                                // buffer of the current row's V (flips per row)
   int kS[2] = {0, 0}, kP[2] = {0, 0};          // issuer: S / PV issued per warpgroup
   int kL0 = 0, kL1 = 0;                        // loader: Q tiles loaded per warpgroup
   int kW = 0;                                  // warpgroup: tiles done
@@ -285,7 +289,8 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     tma_load_2d(Kt, &tmap_k, 0, y, &k_full);
     tma_load_2d(Kt + kTileBytes / 2, &tmap_k, 64, y, &k_full);
   };
-  auto load_v = [&](int rw) {
+  auto load_v = [&](int rw, int buf) {
+    uint8_t* Vst = Vb(buf);
     const int jj = rw % a.NB, rr = (rw / a.NB) % a.B, hh = rw / (a.NB * a.B);
     const int pg = ws.block_table[(int64_t)rr * a.NB + jj];
     const int y = ((pg < 0 ? 0 : pg) * a.Hkv + hh) * kBlock;
@@ -326,36 +331,38 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     // A new row's K and V were prefetched during the previous item (K once its
     // last S had read the K tile); otherwise (first item, or the previous
     // item did not know) they are requested now.
+    if (new_row) vsel ^= 1;
     if (new_row && issuer && lane == 0 && pf_row != row) {
       load_k(row);
-      load_v(row);
+      load_v(row, vsel);
     }
     if (new_row && warp < 8) {
       mbar_wait(&v_full, v_phase, ws.hdr);
       v_phase ^= 1u;
       {
-        // V [key][d] bf16 -> V^T [d][key] fp16 (keys past the last visible
-        // token become 0, whatever the page holds there)
-        const uint32_t vs = smem_u32(Vst);
-        for (int b = warp * 8; b < warp * 8 + 8; ++b) {
-          const int kc = b >> 2, dc4 = (b & 3) * 4;
-          uint32_t m0, m1, m2, m3;
-          ldsm_x4_t(vs + swz_tma(kc * 8 + (lane & 7), dc4 + (lane >> 3)), m0, m1, m2, m3);
-          const uint32_t mm[4] = {m0, m1, m2, m3};
-          const int g = lane >> 2, tq = lane & 3;
-          const int key0 = kc * 8 + 2 * tq;
+        // V bf16 -> fp16 in place (16-byte chunks; a chunk lies in one key
+        // row, 128 bytes per row and 64-column half); keys past the last
+        // visible token become 0, whatever the page holds there
+        uint8_t* vb = Vb(vsel);
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            uint32_t hv = bf16x2_to_f16x2(mm[m]);
-            if (key0 >= ntok) hv &= 0xffff0000u;
-            if (key0 + 1 >= ntok) hv &= 0x0000ffffu;
-            *reinterpret_cast<uint32_t*>(VT + kmaj_off((dc4 + m) * 8 + g, kc, 128) + 4 * tq) = hv;
+        for (int i = 0; i < 8; ++i) {
+          const int off = (tid + 256 * i) * 16;
+          const int key = (off & (kTileBytes / 2 - 1)) >> 7;
+          uint4 x = *reinterpret_cast<const uint4*>(vb + off);
+          if (key >= ntok) {
+            x = make_uint4(0u, 0u, 0u, 0u);
+          } else {
+            x.x = bf16x2_to_f16x2(x.x);
+            x.y = bf16x2_to_f16x2(x.y);
+            x.z = bf16x2_to_f16x2(x.z);
+            x.w = bf16x2_to_f16x2(x.w);
           }
+          *reinterpret_cast<uint4*>(vb + off) = x;
         }
         fence_proxy_async_smem();
       }
-      // V^T is ready for the PV MMAs and the V staging tile is free; the
-      // issuer has meanwhile started the item's S MMAs
+      // V (fp16) is ready for the PV MMAs; the issuer has meanwhile started
+      // the item's S MMAs
       tc_fence_before();
       mbar_arrive(&vt_ready);
     }
@@ -422,15 +429,15 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
 
     if (issuer) {
       if (lane == 0) {
-        const uint32_t kts = smem_u32(Kt), vts = smem_u32(VT);
+        const uint32_t kts = smem_u32(Kt), vts = smem_u32(Vb(vsel));
         const int nrow = next_row(k, row);
         if (new_row) {
           mbar_wait(&k_full, k_phase, ws.hdr);
           k_phase ^= 1u;
         }
-        bool vt_ok = !new_row;                   // V^T of this row written
-        // same row as the last item: no transpose, the V staging tile is free
-        if (vt_ok && nrow >= 0) load_v(nrow);
+        bool vt_ok = !new_row;                   // V of this row converted
+        // the other V buffer held the previous row, whose PV MMAs are done
+        if (nrow >= 0) load_v(nrow, vsel ^ 1);
         pf_row = nrow;
         bool k_done = nrow < 0;                  // the next row's K is requested
         int nS[2] = {0, 0}, nP[2] = {0, 0};      // this item's S / PV per warpgroup
@@ -448,7 +455,6 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
             vt_ok = true;
             vt_phase ^= 1u;
             tc_fence_after();
-            if (nrow >= 0) load_v(nrow);         // the V staging tile is free again
           }
 #pragma unroll
           for (int w = 0; w < 2; ++w) {
@@ -473,7 +479,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
 #pragma unroll
               for (int ks = 0; ks < 8; ++ks)
                 umma_f16_ts(tbase + 256 * w + 128, tbase + 256 * w + 8 * ks,
-                            kstep_desc(vts, ks, 128), idesc_o, ks > 0);
+                            sdesc_sw128_mn(vts + ks * 2048, kTileBytes / 2), idesc_o, ks > 0);
               umma_commit(&o_ready[w]);
               ++kP[w];
               ++nP[w];
@@ -495,7 +501,6 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
         if (!vt_ok) {                            // only on a timeout above
           mbar_wait(&vt_ready, vt_phase, ws.hdr);
           vt_phase ^= 1u;
-          if (nrow >= 0) load_v(nrow);
         }
       }
       __syncwarp();

@@ -58,10 +58,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128_sbo(uint32_t saddr, uint32_t sbo
          ((uint64_t)2 << 61);
 }
 
+// Descriptor of an MN-major operand with 128-byte swizzle: 64-element (128 B)
+// rows of the MN dimension, 8 rows of K per 1 KB atom; lbo_bytes between the
+// 64-element MN blocks, 1 KB between 8-row K groups.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo_bytes) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor of kind::f16 with fp32 accumulation, both operands
 // K-major.  fmt: 0 = fp16, 1 = bf16 (A and B must share it).
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t fmt, uint32_t M, uint32_t N) {
   return (1u << 4) | (fmt << 7) | (fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+// As idesc_f16 with B MN-major (bit 16).
+__host__ __device__ constexpr uint32_t idesc_f16_bmn(uint32_t fmt, uint32_t M, uint32_t N) {
+  return idesc_f16(fmt, M, N) | (1u << 16);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T for one K step; issued by one thread.
