@@ -289,6 +289,10 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// As bulk_wait_read, leaving this thread's most recent bulk group in flight.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 
 // Named barrier over `count` threads (ids 1.. are free; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {

@@ -100,7 +100,7 @@ inline WsLayout layout_of(const msa_config& c) {
   L.tok_pos = o;     o = align_up(o + 4 * T);
   L.block_table = o; o = align_up(o + 4 * B * (size_t)c.max_blocks_per_req);
   L.sched = o;       o = align_up(o + (is_prefill(c) ? 4 * (size_t)(csr_rows_of(c) + 1) : 0));
-  L.item_order = o;  o = align_up(o + (is_prefill(c) ? 4 * (size_t)prefill_items_bound(c) : 0));
+  L.item_order = o;  o = align_up(o + (is_prefill(c) ? 16 * (size_t)prefill_items_bound(c) : 0));
   L.slot_entry = o;  o = align_up(o + (is_prefill(c) ? 4 * T * (size_t)c.num_kv_heads * width_of(c) : 0));
   L.csr_bits = o;    o = align_up(o + (is_prefill(c) ? 4 * csr_words_of(c) : 0));
   L.csr_wpre = o;    o = align_up(o + (is_prefill(c) ? 4 * csr_words_of(c) : 0));
@@ -122,7 +122,8 @@ struct WsView {
   int32_t* tok_pos;
   int32_t* block_table;   // [max_batch, max_blocks_per_req], -1 = invalid
   int32_t* sched;         // prefill: [csr rows + 1] first work item of each CSR row
-  int32_t* item_order;    // prefill: work items by size, largest first
+  int4* item_order;       // prefill: work items by size, largest first: (CSR row,
+                          // first entry, end entry, 0)
   int32_t* slot_entry;    // prefill: [T, H_kv, S] the CSR entry that holds (token, KV
                           // head, slot of the selected list)
   uint32_t* csr_bits;     // prefill: [H_kv, NB, words] token bitmaps of the CSR rows
@@ -149,7 +150,7 @@ inline WsView view_of(const msa_config& c, const void* ws) {
   v.tok_pos = (int32_t*)(b + L.tok_pos);
   v.block_table = (int32_t*)(b + L.block_table);
   v.sched = (int32_t*)(b + L.sched);
-  v.item_order = (int32_t*)(b + L.item_order);
+  v.item_order = (int4*)(b + L.item_order);
   v.slot_entry = (int32_t*)(b + L.slot_entry);
   v.csr_bits = (uint32_t*)(b + L.csr_bits);
   v.csr_wpre = (int32_t*)(b + L.csr_wpre);

@@ -163,9 +163,9 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(int32_t* __restrict__ ro
 // ------------------------------------------------------------ attention
 // Work items: a CSR row's tokens in chunks of kTilesPerItem M-tiles of 128
 // rows (tokens x GQA heads); msa_build_k2q_csr writes the first item of every
-// row (ws.sched) and the items ordered largest first (ws.item_order), so the
-// huge rows of the init / local blocks are split and the CTAs' round-robin
-// shares come out even.
+// row (ws.sched) and the items ordered largest first (ws.item_order: CSR row,
+// first and end entry of each), so the huge rows of the init / local blocks
+// are split and the CTAs' round-robin shares come out even.
 constexpr int kTilesPerItem = 32;
 constexpr int kLoaderWarps = 3;          // Q loaders (TMA issue from one warp is slow)
 constexpr int kTcThreads = (9 + kLoaderWarps) * 32;   // 2 softmax warpgroups, MMA issuer
@@ -261,7 +261,6 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
 
   const int G = a.G, TPT = kBlock / G;         // tokens per M-tile
   const int lgG = __ffs(G) - 1;                // G divides 16
-  const int tok_per_item = kTilesPerItem * TPT;
   const int n_items = ws.sched[rows];
   const uint32_t idesc_s = idesc_f16(1, 128, 128), idesc_o = idesc_f16_bmn(0, 128, 128);
   uint32_t k_phase = 0, v_phase = 0, kf_phase = 0, vt_phase = 0;
@@ -271,15 +270,6 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   int kL0 = 0, kL1 = 0;                        // loader: Q tiles loaded per warpgroup
   int kW = 0;                                  // warpgroup: tiles done
   int cur_row = -1;
-  // CSR row of work item `it`: the last row whose first item is <= it
-  auto row_of = [&](int it) {
-    int lo = 0, hi = (int)rows - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (ws.sched[mid] <= it) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-  };
   // K / V tiles of CSR row rw: K into the K tile, V into the V staging tile
   auto load_k = [&](int rw) {
     const int jj = rw % a.NB, rr = (rw / a.NB) % a.B, hh = rw / (a.NB * a.B);
@@ -302,21 +292,17 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   // K / V than `rw`, else -1 (issuer only)
   auto next_row = [&](int kk, int rw) {
     if (kk + (int)gridDim.x >= n_items) return -1;
-    const int nit = ws.item_order[kk + gridDim.x];
-    const int nr = row_of(nit);
+    const int4 nit = ws.item_order[kk + gridDim.x];
+    const int nr = nit.x;
     if (nr == rw) return -1;
-    const int nb_ = a.row_ptr[nr] + (nit - ws.sched[nr]) * tok_per_item;
-    const int ne_ = min(a.row_ptr[nr + 1], nb_ + tok_per_item);
     const int nj = nr % a.NB, nrr = (nr / a.NB) % a.B;
-    if (ws.block_table[(int64_t)nrr * a.NB + nj] < 0 || nb_ >= ne_) return -1;
+    if (ws.block_table[(int64_t)nrr * a.NB + nj] < 0 || nit.y >= nit.z) return -1;
     return nr;
   };
   for (int k = blockIdx.x; k < n_items; k += gridDim.x) {
-    const int item = ws.item_order[k];           // largest items first
-    const int row = row_of(item), chunk = item - ws.sched[row];
+    const int4 item = ws.item_order[k];          // largest items first
+    const int row = item.x, beg = item.y, end = item.z;
     const int j = row % a.NB, r = (row / a.NB) % a.B, h = row / (a.NB * a.B);
-    const int beg = a.row_ptr[row] + chunk * tok_per_item;
-    const int end = min(a.row_ptr[row + 1], beg + tok_per_item);
     const int page = ws.block_table[(int64_t)r * a.NB + j];
     if (page < 0 || beg >= end) continue;      // flagged by the plan (uniform)
     const int ntok = min(kBlock, ws.req_seq_len[r] - j * kBlock);
@@ -429,15 +415,29 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
 
     if (issuer) {
       if (lane == 0) {
-        const uint32_t kts = smem_u32(Kt), vts = smem_u32(Vb(vsel));
+        // descriptors of K step 0 (K tile, both Q buffers, this row's V);
+        // step ks only moves the start address in the low word
+        const uint64_t dk = kstep_desc(smem_u32(Kt), 0, 128);
+        const uint64_t dq0 = qstep_desc(smem_u32(Qb), 0);
+        const uint64_t dq1 = qstep_desc(smem_u32(Qb + kTileBytes), 0);
+        const uint64_t dv = sdesc_sw128_mn(smem_u32(Vb(vsel)), kTileBytes / 2);
+        const uint32_t vlo = (uint32_t)dv, vhi = (uint32_t)(dv >> 32);
+        const uint32_t klo = (uint32_t)dk, khi = (uint32_t)(dk >> 32);
         const int nrow = next_row(k, row);
         if (new_row) {
           mbar_wait(&k_full, k_phase, ws.hdr);
           k_phase ^= 1u;
         }
         bool vt_ok = !new_row;                   // V of this row converted
-        // the other V buffer held the previous row, whose PV MMAs are done
-        if (nrow >= 0) load_v(nrow, vsel ^ 1);
+        // The next row's V goes to the other V buffer (the previous row's,
+        // whose PV MMAs are done).  v_full counts one V load per phase, so it
+        // is requested only once the softmax warps have seen this row's V land
+        // (vt_ready): never two V loads in flight, never a phase they missed.
+        bool v_done = nrow < 0;
+        if (!v_done && vt_ok) {
+          load_v(nrow, vsel ^ 1);
+          v_done = true;
+        }
         pf_row = nrow;
         bool k_done = nrow < 0;                  // the next row's K is requested
         int nS[2] = {0, 0}, nP[2] = {0, 0};      // this item's S / PV per warpgroup
@@ -455,6 +455,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
             vt_ok = true;
             vt_phase ^= 1u;
             tc_fence_after();
+            if (!v_done) {
+              load_v(nrow, vsel ^ 1);
+              v_done = true;
+            }
           }
 #pragma unroll
           for (int w = 0; w < 2; ++w) {
@@ -463,11 +467,18 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
                 mbar_test_wait(&q_full[w], (uint32_t)(kS[w] & 1)) &&
                 (kS[w] == 0 || mbar_test_wait(&o_ready[w], (uint32_t)((kS[w] - 1) & 1)))) {
               tc_fence_after();
-              const uint32_t qs = smem_u32(Qb + w * kTileBytes);
-#pragma unroll
-              for (int ks = 0; ks < 8; ++ks)
-                umma_f16(tbase + 256 * w, qstep_desc(qs, ks), kstep_desc(kts, ks, 128),
-                         idesc_s, ks > 0);
+              const uint64_t dq = w ? dq1 : dq0;
+              const uint32_t qlo = (uint32_t)dq, qhi = (uint32_t)(dq >> 32);
+              const uint32_t dt = tbase + 256 * w;
+              // K step ks: Q at +(ks / 4) KB + (ks % 4) 32 B, K at +(ks / 4) 16 KB + (ks % 4) 32 B
+              umma_ss<false>(dt, qlo, qhi, klo, khi, idesc_s);
+              umma_ss<true>(dt, qlo + 2, qhi, klo + 2, khi, idesc_s);
+              umma_ss<true>(dt, qlo + 4, qhi, klo + 4, khi, idesc_s);
+              umma_ss<true>(dt, qlo + 6, qhi, klo + 6, khi, idesc_s);
+              umma_ss<true>(dt, qlo + 64, qhi, klo + 1024, khi, idesc_s);
+              umma_ss<true>(dt, qlo + 66, qhi, klo + 1026, khi, idesc_s);
+              umma_ss<true>(dt, qlo + 68, qhi, klo + 1028, khi, idesc_s);
+              umma_ss<true>(dt, qlo + 70, qhi, klo + 1030, khi, idesc_s);
               umma_commit(&s_ready[w]);
               ++kS[w];
               ++nS[w];
@@ -476,10 +487,12 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
             }
             if (vt_ok && nP[w] < nS[w] && mbar_test_wait(&p_ready[w], (uint32_t)(kP[w] & 1))) {
               tc_fence_after();
+              // K step ks: P columns +8 ks, V rows 16 ks (+2 KB)
+              const uint32_t ta = tbase + 256 * w, dt = ta + 128;
+              umma_ts<false>(dt, ta, vlo, vhi, idesc_o);
 #pragma unroll
-              for (int ks = 0; ks < 8; ++ks)
-                umma_f16_ts(tbase + 256 * w + 128, tbase + 256 * w + 8 * ks,
-                            sdesc_sw128_mn(vts + ks * 2048, kTileBytes / 2), idesc_o, ks > 0);
+              for (int ks = 1; ks < 8; ++ks)
+                umma_ts<true>(dt, ta + 8 * ks, vlo + 128 * ks, vhi, idesc_o);
               umma_commit(&o_ready[w]);
               ++kP[w];
               ++nP[w];
@@ -502,6 +515,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
           mbar_wait(&vt_ready, vt_phase, ws.hdr);
           vt_phase ^= 1u;
         }
+        if (!v_done) load_v(nrow, vsel ^ 1);
       }
       __syncwarp();
       continue;
@@ -657,6 +671,18 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     }
   }
   if (warp < 8) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  // Every MMA and copy has been waited for on the normal path.  After a wait
+  // timed out some may still run: the issuer waits for its MMAs (bounded, no
+  // early exit), and every thread gives in-flight TMA loads ~100 us to land,
+  // before the TMEM is freed and the shared memory released.
+  if (issuer && lane == 0) {
+    umma_commit(&k_free);
+    for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&k_free, kf_phase); ++i) {
+    }
+  }
+  if (*reinterpret_cast<volatile int*>(&ws.hdr->err) & MSA_DEVERR_TIMEOUT) {
+    for (int i = 0; i < 1000; ++i) __nanosleep(100);
+  }
   tc_fence_before();
   __syncthreads();
   if (issuer) {
@@ -708,8 +734,11 @@ item_order_kernel(const int32_t* __restrict__ row_ptr, WsView ws, int64_t rows, 
   }
   __syncthreads();
   for (int64_t row = tid; row < rows; row += 1024) {
-    const int first = ws.sched[row];
-    items_of(row, [&](int k, int sz) { ws.item_order[atomicAdd(&base[sz], 1)] = first + k; });
+    const int rb = row_ptr[row], re = row_ptr[row + 1];
+    items_of(row, [&](int k, int sz) {
+      const int b = rb + k * tok_per_item;
+      ws.item_order[atomicAdd(&base[sz], 1)] = make_int4((int)row, b, min(re, b + tok_per_item), 0);
+    });
   }
 }
 

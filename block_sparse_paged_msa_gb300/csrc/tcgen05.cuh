@@ -98,6 +98,31 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Lean forms for an issuing loop: a shared-memory descriptor passed as its two
+// 32-bit words, so that a K step (which only moves the 14-bit start-address
+// field in the low word; shared-window addresses stay below 2^18 bytes, so
+// the field never carries) costs one integer add; the accumulate flag is a
+// compile-time constant.
+template <bool kAcc>
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint32_t alo, uint32_t ahi,
+                                        uint32_t blo, uint32_t bhi, uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .b64 a, b;\n .reg .pred p;\n mov.b64 a, {%1, %2};\n mov.b64 b, {%3, %4};\n"
+      " setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n}" ::"r"(d_tmem),
+      "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "n"(kAcc ? 1 : 0)
+      : "memory");
+}
+template <bool kAcc>
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo,
+                                        uint32_t bhi, uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .b64 b;\n .reg .pred p;\n mov.b64 b, {%2, %3};\n setp.ne.b32 p, %5, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "n"(kAcc ? 1 : 0)
+      : "memory");
+}
+
 // Arrive once on `bar` when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
