@@ -56,6 +56,12 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// 2^x for both halves of an f16x2 (one special-function instruction).
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
 
 // Packed fp32 pairs (sm_100 family): two lanes of arithmetic per instruction.
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
@@ -288,10 +294,6 @@ __device__ __forceinline__ void bulk_commit() {
 // Wait until this thread's committed bulk stores have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// As bulk_wait_read, leaving this thread's most recent bulk group in flight.
-__device__ __forceinline__ void bulk_wait_read_1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 // Named barrier over `count` threads (ids 1.. are free; 0 is __syncthreads).

@@ -566,10 +566,12 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
       }
       const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float msc = m == -INFINITY ? 0.f : m * a.scale_log2;
-      // pass 2: probabilities (exp2 domain, scale folded into one FMA), fp16 P
-      // into TMEM over the S columns already read.  Pairs of columns go
-      // through packed fp32 FMA / add; masked columns (only outside the fast
-      // path) become -inf before the exponential.
+      // pass 2: probabilities (exp2 domain, scale folded into one packed FMA),
+      // fp16 P into TMEM over the S columns already read.  The exponent x <= 0
+      // is rounded to fp16 and 2^x taken for two columns per special-function
+      // instruction (fp16 is P's own precision); the row sum adds those same
+      // fp16 values in fp32 (two pairs at a time in fp16, each term <= 1).
+      // Masked columns (only outside the fast path) become -inf first.
       const uint64_t sc2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-msc, -msc);
       uint64_t ls2[4] = {0, 0, 0, 0};               // (+0.f, +0.f) pairs
 #pragma unroll 1
@@ -584,20 +586,16 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
         }
         uint32_t pk[32];
 #pragma unroll
-        for (int i2 = 0; i2 < 32; ++i2) {
-          float x0, x1;
+        for (int i2 = 0; i2 < 32; i2 += 2) {
+          float x0, x1, x2, x3;
           f2_split(fma_f2(f2u(rg[2 * i2], rg[2 * i2 + 1]), sc2, nm2), x0, x1);
-          // a quarter of the exponentials on the FMA pipe: the special-function
-          // unit alone takes 8 cycles per warp instruction
-          float p0, p1;
-          if ((i2 & 3) == 3) {
-            exp2_poly2(x0, x1, p0, p1);
-          } else {
-            p0 = ex2_approx(x0);
-            p1 = ex2_approx(x1);
-          }
-          ls2[i2 & 3] = add_f2(ls2[i2 & 3], f2(p0, p1));
-          pk[i2] = pack_f16(p0, p1);
+          f2_split(fma_f2(f2u(rg[2 * i2 + 2], rg[2 * i2 + 3]), sc2, nm2), x2, x3);
+          pk[i2] = ex2_f16x2(pack_f16(x0, x1));
+          pk[i2 + 1] = ex2_f16x2(pack_f16(x2, x3));
+          __half2 hs = __hadd2(*reinterpret_cast<const __half2*>(&pk[i2]),
+                               *reinterpret_cast<const __half2*>(&pk[i2 + 1]));
+          const float2 fs = __half22float2(hs);
+          ls2[(i2 >> 1) & 3] = add_f2(ls2[(i2 >> 1) & 3], f2(fs.x, fs.y));
         }
         tmem_st32(tlane + 32 * cb, pk);             // keys 64cb.. -> columns 32cb..
       }
