@@ -92,37 +92,6 @@ __device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-// 2^x for a pair x <= 0 (-inf allowed) on the FMA pipe instead of the
-// special-function unit.  Method: round x to the nearest integer n by adding
-// and subtracting 1.5 * 2^23, so f = x - n lies in [-1/2, 1/2]; 2^f by a cubic
-// (coefficients fitted here by least squares at Chebyshev nodes of [-1/2, 1/2],
-// reweighted to equalise the relative error: max relative error 7.5e-5); then
-// n is added to the exponent field -- the integer bits of x + 1.5 * 2^23,
-// shifted by 23, are n mod 2^9 times 2^23.  x is clamped at -126 so the
-// exponent cannot wrap; results there are below 2^-125 (zero once rounded to
-// fp16).
-constexpr float kExp2C0 = 0.9999280571937561f;
-constexpr float kExp2C1 = 0.6932609677314758f;
-constexpr float kExp2C2 = 0.2426111251115799f;
-constexpr float kExp2C3 = 0.0551716648042202f;
-__device__ __forceinline__ void exp2_poly2(float x0, float x1, float& y0, float& y1) {
-  constexpr float kShift = 12582912.f;   // 1.5 * 2^23
-  x0 = fmaxf(x0, -126.f);
-  x1 = fmaxf(x1, -126.f);
-  const uint64_t x2 = f2(x0, x1);
-  const uint64_t t2 = add_f2(x2, f2(kShift, kShift));
-  const uint64_t n2 = add_f2(t2, f2(-kShift, -kShift));
-  const uint64_t fr = fma_f2(n2, f2(-1.f, -1.f), x2);
-  uint64_t p = fma_f2(f2(kExp2C3, kExp2C3), fr, f2(kExp2C2, kExp2C2));
-  p = fma_f2(p, fr, f2(kExp2C1, kExp2C1));
-  p = fma_f2(p, fr, f2(kExp2C0, kExp2C0));
-  float p0, p1, tt0, tt1;
-  f2_split(p, p0, p1);
-  f2_split(t2, tt0, tt1);
-  y0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(tt0) << 23));
-  y1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(tt1) << 23));
-}
-
 // max(a, b, c) in one instruction (sm_100 family)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
