@@ -247,6 +247,23 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, con
                : "memory");
 }
 
+// L2 policy for data written once and not read again soon (streamed results):
+// evicted first, so it does not push reused operands out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// As tma_store_2d, with an L2 cache policy for the written lines.
+__device__ __forceinline__ void tma_store_2d_hint(const void* tmap, int x, int y, const void* src,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], "
+      "%4;" ::"l"(tmap),
+      "r"(x), "r"(y), "r"(smem_u32(src)), "l"(policy)
+      : "memory");
+}
+
 // 1-D bulk copy (TMA engine) of `bytes` (multiple of 16, both addresses 16-byte
 // aligned) into shared memory, completion counted on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,

@@ -523,6 +523,9 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
 
     // ---------------------------------------------------- softmax warpgroups
     uint8_t* prow = Pb + wg * kTileBytes;
+    // the partials are read back only by the combine: evict them from L2
+    // first, so they do not push out the queries that later items reuse
+    const uint64_t pol_out = l2_evict_first_policy();
     const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + 256 * wg;
     const bool leader = wtid == 0;                  // issues the warpgroup's output stores
     // this thread's row of tile t: its token (< 0 past the end of the item)
@@ -652,8 +655,8 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
       named_bar_sync(2 + wg, 128);
       if (leader) {
         if (nrows == kBlock) {
-          tma_store_2d(&tmap_o, 0, e0 * G, prow);
-          tma_store_2d(&tmap_o, 64, e0 * G, prow + kTileBytes / 2);
+          tma_store_2d_hint(&tmap_o, 0, e0 * G, prow, pol_out);
+          tma_store_2d_hint(&tmap_o, 64, e0 * G, prow + kTileBytes / 2, pol_out);
         } else {
           for (int b8 = 0; b8 < (nrows >> 3); ++b8) {
             tma_store_2d(&tmap_o8, 0, e0 * G + 8 * b8, prow + 1024 * b8);
