@@ -276,8 +276,9 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     const int pg = ws.block_table[(int64_t)rr * a.NB + jj];
     const int y = ((pg < 0 ? 0 : pg) * a.Hkv + hh) * kBlock;
     mbar_arrive_expect_tx(&k_full, kTileBytes);
-    tma_load_2d(Kt, &tmap_k, 0, y, &k_full);
-    tma_load_2d(Kt + kTileBytes / 2, &tmap_k, 64, y, &k_full);
+    const uint64_t pol = l2_evict_first_policy();   // one item's use, then gone
+    tma_load_2d_hint(Kt, &tmap_k, 0, y, &k_full, pol);
+    tma_load_2d_hint(Kt + kTileBytes / 2, &tmap_k, 64, y, &k_full, pol);
   };
   auto load_v = [&](int rw, int buf) {
     uint8_t* Vst = Vb(buf);
@@ -285,8 +286,9 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     const int pg = ws.block_table[(int64_t)rr * a.NB + jj];
     const int y = ((pg < 0 ? 0 : pg) * a.Hkv + hh) * kBlock;
     mbar_arrive_expect_tx(&v_full, kTileBytes);
-    tma_load_2d(Vst, &tmap_v, 0, y, &v_full);
-    tma_load_2d(Vst + kTileBytes / 2, &tmap_v, 64, y, &v_full);
+    const uint64_t pol = l2_evict_first_policy();
+    tma_load_2d_hint(Vst, &tmap_v, 0, y, &v_full, pol);
+    tma_load_2d_hint(Vst + kTileBytes / 2, &tmap_v, 64, y, &v_full, pol);
   };
   // row of the next item of this CTA if it will be processed and needs other
   // K / V than `rw`, else -1 (issuer only)
@@ -363,6 +365,9 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
       // softmax masks.  G < 8: 16-byte cp.async copies, 2 rows per instruction.
       // The loader warps share each tile's copies (box / instruction k goes to
       // warp k % kLoaderWarps) and each arrives on q_full[w] once.
+      // each token's queries are read once per selected block (~20 times):
+      // kept in L2 ahead of the K / V tiles and the streamed partials
+      const uint64_t pol_q = l2_evict_last_policy();
       for (int t = 0; t < ntiles; ++t) {
         const int w = t & 1;
         const int n = w ? kL1 : kL0;
@@ -382,7 +387,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
           if (b < nt * gpt) {
             const int tk = b / gpt, sub = b - tk * gpt;
             const int y = a.q_idx[e0 + tk] * a.Hq + h * G + 8 * sub;
-            tma_load_3d(Qb + w * kTileBytes + b * 2048, &tmap_q, 0, y, 0, &q_full[w]);
+            tma_load_3d_hint(Qb + w * kTileBytes + b * 2048, &tmap_q, 0, y, 0, &q_full[w], pol_q);
           }
           continue;
         }
