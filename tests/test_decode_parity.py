@@ -4,8 +4,10 @@ Selections and block scores are compared bit-exactly (integer-valued index
 vectors make every dot product exact in fp32 and fp64); out and LSE within the
 bounds in gpu_util.  Small cases span several blocks and ragged last pages and
 are compared on every element; the full-size medium decode (batch 32, seq_lens
-8k..32k, 64/8 heads) runs in the launch configuration the bench times and is
-compared on sampled (token, KV head) pairs."""
+8k..32k, 64/8 heads), long decode (batch 128, seq_lens 64k..128k, a 114 688-page
+pool: 90 GB of K, V and index keys), fp8 decode and verify run in the launch
+configuration the bench times and are compared on sampled (token, KV head)
+pairs."""
 import numpy as np
 import pytest
 import torch
@@ -92,3 +94,17 @@ def test_verify_full_size_sampled():
     assert msa.check_device_error(sa.ws) == 0
     samples = [(0, 0), (1, 3), (2, 7), (3, 5), (255, 7), (128, 2)]
     print(compare_sampled(w, sa, samples))
+
+
+@pytest.mark.parametrize("name,samples", [
+    ("long_decode", [(0, 0), (127, 7), (37, 3), (64, 5), (100, 1), (5, 6)]),
+    ("fp8_decode", [(0, 0), (31, 7), (9, 3), (17, 5), (25, 1), (4, 6)]),
+])
+def test_full_size_sampled(name, samples):
+    spec = wl.WORKLOADS[name]
+    w = wl.make_workload(spec, device="cuda")
+    sa = run_gpu(w)
+    assert msa.check_device_error(sa.ws) == 0
+    print(name, compare_sampled(w, sa, samples))
+    del w, sa
+    torch.cuda.empty_cache()
