@@ -15,15 +15,16 @@
 //    per-(KV head, key block) token bitmaps, so every row lists its tokens
 //    ascending and the structure is deterministic.
 //  * prefill_tc_kernel (msa_sparse_prefill): fifth-generation tensor cores.
-//    A persistent CTA per SM walks work items of up to 16 M-tiles of one CSR
-//    row; per row the K and V tiles arrive by TMA and V is transposed once to
-//    fp16.  M-tiles of 128 rows (tokens x GQA heads) alternate between two
-//    softmax warpgroups: one thread issues tcgen05.mma for S = Q K^T (bf16)
-//    and O = P V (fp16, P from TMEM) with fp32 accumulators in TMEM; each
-//    warpgroup thread owns one row (tcgen05.ld), applies the causal mask and
-//    the softmax; the normalised fp16 partial rows of a tile, contiguous in
-//    CSR-entry order, leave by TMA tile stores with their LSE beside them.
-//    msa_combine merges each token's slots.
+//    A persistent CTA per SM walks work items of up to 32 M-tiles of one CSR
+//    row; per row the K and V tiles arrive by TMA and V is converted to fp16
+//    in place (read by P V as an MN-major operand).  M-tiles of 128 rows
+//    (tokens x GQA heads) alternate between two softmax warpgroups: one
+//    thread issues tcgen05.mma for S = Q K^T (bf16) and O = P V (fp16, P from
+//    TMEM) with fp32 accumulators in TMEM; each warpgroup thread owns one row
+//    (tcgen05.ld), applies the causal mask and the softmax; the normalised
+//    fp16 partial rows of a tile, contiguous in CSR-entry order, leave by TMA
+//    tile stores with their LSE beside them.  msa_combine merges each token's
+//    slots.
 #include <algorithm>
 #include <mutex>
 
@@ -239,7 +240,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     mbar_init(&k_full, 1);
     mbar_init(&v_full, 1);
     mbar_init(&k_free, 1);
-    mbar_init(&vt_ready, 256);                 // the softmax warps, after the transpose
+    mbar_init(&vt_ready, 256);                 // the softmax warps, after the V conversion
     for (int w = 0; w < 2; ++w) {
       mbar_init(&q_full[w], kLoaderWarps);
       mbar_init(&s_ready[w], 1);
@@ -270,7 +271,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   int kL0 = 0, kL1 = 0;                        // loader: Q tiles loaded per warpgroup
   int kW = 0;                                  // warpgroup: tiles done
   int cur_row = -1;
-  // K / V tiles of CSR row rw: K into the K tile, V into the V staging tile
+  // K / V tiles of CSR row rw: K into the K tile, V into V buffer `buf`
   auto load_k = [&](int rw) {
     const int jj = rw % a.NB, rr = (rw / a.NB) % a.B, hh = rw / (a.NB * a.B);
     const int pg = ws.block_table[(int64_t)rr * a.NB + jj];
@@ -310,8 +311,6 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     const int ntok = min(kBlock, ws.req_seq_len[r] - j * kBlock);
     const int ntiles = (end - beg + TPT - 1) / TPT;
 
-    // the previous item's MMAs are done; a new row also overwrites P[1] (V
-    // staging), so the output rows staged there must have been read
     // The loaders run ahead across items (their Q buffers are tracked per
     // tile); the others meet here once the previous item's MMAs are done.
     if (!loader) named_bar_sync(1, kTcThreads - 32 * kLoaderWarps);

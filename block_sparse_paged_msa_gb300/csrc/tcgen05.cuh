@@ -86,18 +86,6 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
-// As umma_f16 with the A operand in TMEM: M rows = TMEM lanes, each 32-bit
-// column holding two consecutive K elements (lower half first); one K step of
-// 16 elements spans 8 columns from a_tmem.
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Lean forms for an issuing loop: a shared-memory descriptor passed as its two
 // 32-bit words, so that a K step (which only moves the 14-bit start-address
 // field in the low word; shared-window addresses stay below 2^18 bytes, so
@@ -113,6 +101,9 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint32_t alo, uint32_t 
       "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "n"(kAcc ? 1 : 0)
       : "memory");
 }
+// A operand in TMEM: M rows = TMEM lanes, each 32-bit column holding two
+// consecutive K elements (lower half first); one K step of 16 elements spans
+// 8 columns from a_tmem.
 template <bool kAcc>
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo,
                                         uint32_t bhi, uint32_t idesc) {
