@@ -726,6 +726,34 @@ extern "C" msa_status msa_sparse_decode(const msa_config* cfg, void* ws, const v
   return fp8 ? launch_decode<true>(v, a, tk, tv, s) : launch_decode<false>(v, a, tk, tv, s);
 }
 
+namespace msa {
+namespace {
+// One CTA waits on an mbarrier that no thread ever arrives on, with a short
+// poll limit: the bounded wait must give up, record MSA_DEVERR_TIMEOUT and
+// return, leaving the context usable.
+__global__ void __launch_bounds__(32) selftest_wait_kernel(WsView ws) {
+  __shared__ __align__(8) uint64_t never;
+  if (threadIdx.x == 0) {
+    mbar_init(&never, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  griddep_launch_dependents();
+  griddep_wait();
+  mbar_wait<1u << 14>(&never, 0, ws.hdr);
+}
+}  // namespace
+}  // namespace msa
+
+extern "C" msa_status msa_selftest_wait_timeout(const msa_config* cfg, void* ws,
+                                                msa_stream_t stream) {
+  msa_status st = check_config(cfg);
+  if (st != MSA_OK) return st;
+  if (!ws) return MSA_ERR_INVALID_ARG;
+  return launch_pdl(selftest_wait_kernel, dim3(1), dim3(32), 0, (cudaStream_t)stream,
+                    view_of(*cfg, ws));
+}
+
 extern "C" msa_status msa_combine(const msa_config* cfg, const void* ws, void* out, float* lse,
                                   msa_stream_t stream) {
   msa_status st = check_config(cfg);

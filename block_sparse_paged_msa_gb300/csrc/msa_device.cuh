@@ -202,11 +202,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of `bar` with the given parity; false on timeout.
-// Once any waiter has timed out (the error word says so), every other wait
-// gives up within a few hundred polls instead of running to its own limit.
+// Wait for the phase of `bar` with the given parity; false on timeout (after
+// kLimit polls, recorded as MSA_DEVERR_TIMEOUT in the error word).  Once any
+// waiter has timed out (the error word says so), every other wait gives up
+// within a few hundred polls instead of running to its own limit.
+template <uint32_t kLimit = kWaitLimit>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WsHeader* hdr) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+  for (uint32_t i = 0; i < kLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 255u &&
         (*reinterpret_cast<volatile int*>(&hdr->err) & MSA_DEVERR_TIMEOUT))

@@ -65,6 +65,7 @@ _SIGNATURES = {
     "msa_sparse_decode": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "msa_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "msa_check_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+    "msa_selftest_wait_timeout": (ctypes.c_int, [_CFG, _P, _P]),
     "msa_sparse_decode_noalloc": (ctypes.c_int, [_CFG, ctypes.c_int32, _P, _P, ctypes.c_int32,
                                                  _P, _P, _P, _P, _P, _P, _P]),
     "msa_decode_step": (ctypes.c_int, [_CFG, _P, ctypes.c_int32, _P, _P, ctypes.c_int32, _P, _P,
@@ -315,6 +316,13 @@ def check_device_error(ws, stream=None) -> int:
     if st not in (0, 4):
         _check("msa_check_device_error", st)
     return flags.value
+
+
+def selftest_wait_timeout(cfg: MsaConfig, ws, stream=None):
+    """Run the library's bounded wait on a barrier nothing completes (see
+    msa_selftest_wait_timeout); the error word then holds MSA_DEVERR_TIMEOUT."""
+    _check("msa_selftest_wait_timeout",
+           lib().msa_selftest_wait_timeout(ctypes.byref(cfg), _ptr(ws), _stream(stream)))
 
 
 # ---------------------------------------------------------------- the step

@@ -318,6 +318,17 @@ msa_status msa_decode_step(const msa_config* cfg, void* ws, int32_t batch,
  */
 msa_status msa_check_device_error(const void* ws, int32_t* flags, msa_stream_t stream);
 
+/*
+ * msa_selftest_wait_timeout -- checks the failure path of the pipeline waits.
+ * Launches one CTA that waits on an mbarrier nothing ever completes, through
+ * the same bounded wait every warp-specialised kernel uses, with a short limit
+ * (2^14 polls).  The wait gives up and sets MSA_DEVERR_TIMEOUT in the
+ * workspace's error word, which msa_check_device_error then reports; no
+ * device fault, and the context stays usable (msa_plan clears the word).
+ * ws: a workspace of msa_workspace_bytes(cfg) bytes.  Asynchronous on `stream`.
+ */
+msa_status msa_selftest_wait_timeout(const msa_config* cfg, void* ws, msa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

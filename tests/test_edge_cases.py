@@ -1,5 +1,6 @@
 """Boundary conventions of the C ABI on the GPU: idle requests, empty batches,
-bad page ids flagged without a fault, CUDA-graph replay equal to eager."""
+bad page ids flagged without a fault, CUDA-graph replay equal to eager, and a
+pipeline wait that runs out reported as a status (no fault, context usable)."""
 import numpy as np
 import pytest
 import torch
@@ -146,3 +147,20 @@ def test_graph_replay_equals_eager(name):
         T = w2.num_tokens
         assert torch.equal(g_sel[:T], eager.selected[:T])
         assert torch.equal(g_out[:T], eager.out[:T]) and torch.equal(g_lse[:T], eager.lse[:T])
+
+
+def test_bounded_wait_times_out_without_fault():
+    # A wait on a barrier that nothing completes gives up after its limit and
+    # reports MSA_DEVERR_TIMEOUT; the next plan clears the word and the same
+    # step gives the same results as before.
+    spec = wl.WORKLOADS["tiny_decode"]
+    w = wl.make_workload(spec, device="cuda")
+    sa = run_gpu(w)
+    assert msa.check_device_error(sa.ws) == 0
+    out0, lse0 = sa.out.clone(), sa.lse.clone()
+    msa.ops.selftest_wait_timeout(sa.cfg, sa.ws)
+    assert msa.check_device_error(sa.ws) & 8          # MSA_DEVERR_TIMEOUT
+    sa.run(w.seq_lens, w.block_table, w.idx_q, w.idx_k_pages, w.q, w.k_pages, w.v_pages)
+    torch.cuda.synchronize()
+    assert msa.check_device_error(sa.ws) == 0
+    assert torch.equal(sa.out, out0) and torch.equal(sa.lse, lse0)
