@@ -177,20 +177,37 @@ topk_warp_kernel(WsView ws, int Hkv, int max_blocks, int init, int local, int to
   const int nc = c1 - c0;
   const int K = min(topk, nc);
   uint32_t key[CPL];
+  uint32_t kmax = 0u;                           // over this lane's candidates
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
     const int c = i * 32 + lane;
     key[i] = c < nc ? order_key(sc[c0 + c]) : 0u;
+    kmax = max(kmax, key[i]);
   }
   uint32_t thr = 0xffffffffu;   // keys > thr win outright
   int ktie = 0;                 // this many keys == thr win, lowest index first
   if (K == nc) {
     thr = 0u;                   // every candidate (real keys are >= 1)
   } else if (K > 0) {
-    uint32_t prefix = 0u, mask = 0u;
+    // Only the bytes where the candidates' keys differ need a pass: diff = the
+    // OR over candidates of (key ^ largest key).  Above its highest byte every
+    // key matches the largest one, below its lowest every key carries the same
+    // bits (integer-valued scores share their top byte and their low mantissa
+    // bytes, so one pass is typical).
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    uint32_t dl = 0u;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i)
+      if (i * 32 + lane < nc) dl |= key[i] ^ kmax;
+    const uint32_t diff = __reduce_or_sync(0xffffffffu, dl);
+    // all keys equal: the K lowest indices win (diff = 0 -> no pass)
+    const int top = diff ? (31 - __clz(diff)) >> 3 << 3 : -8;   // first shift
+    const int bot = diff ? (__ffs(diff) - 1) >> 3 << 3 : 0;     // last shift
+    uint32_t mask = top >= 24 ? 0u : 0xffffffffu << (top + 8);
+    uint32_t prefix = kmax & mask;
     int krem = K;
 #pragma unroll 1
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int shift = top; shift >= bot; shift -= 8) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) hist[lane * 8 + e] = 0;
       __syncwarp();
@@ -233,7 +250,7 @@ topk_warp_kernel(WsView ws, int Hkv, int max_blocks, int init, int local, int to
       mask |= 0xffu << shift;
       __syncwarp();
     }
-    thr = prefix;
+    thr = prefix | (kmax & ~mask);   // the bits below the last pass are shared
     ktie = krem;
   }
   for (int i = lane; i < c0; i += 32) out[i] = i;
