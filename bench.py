@@ -37,6 +37,22 @@ sys.path.insert(0, ROOT)
 from block_sparse_paged_msa_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "sparse-decode query-tokens/s"
+
+
+def max_over_ranks(values, world, device):
+    """Each timing's maximum over the ranks (the slowest replica sets the job
+    time); a collective on timings only, none on the data path."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def replica_throughput(units_per_step, world, steps, ms):
+    """Whole-job throughput of `world` independent replicas, each processing
+    units_per_step per step, over `steps` steps taking `ms` (the slowest rank's)."""
+    return units_per_step * world * steps / (ms / 1e3)
+
 UNIT = "q-tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -404,12 +420,9 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- accounting
     T = w.num_tokens
-    t_max = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
-    ms, e2e_ms = float(t_max[0]), float(t_max[1])
-    value = T * world * K / (ms / 1e3)
-    e2e_value = T * world * Ke / (e2e_ms / 1e3)
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, dev)
+    value = replica_throughput(T, world, K, ms)
+    e2e_value = replica_throughput(T, world, Ke, e2e_ms)
     peaks = measured_peaks()
     result = {
         "metric": METRIC if not sa.prefill else "sparse-prefill query-tokens/s",
