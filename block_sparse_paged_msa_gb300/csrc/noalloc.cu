@@ -69,3 +69,13 @@ extern "C" msa_status msa_sparse_decode_noalloc(const msa_config* cfg, int32_t b
     return st;
   return msa_combine(cfg, scratch, out, lse, stream);
 }
+
+extern "C" msa_status msa_noalloc_check_device_error(int32_t* flags, msa_stream_t stream) {
+  if (flags == nullptr) return MSA_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  msa_status st = scratch_address(&scratch);
+  if (st != MSA_OK) return st;
+  // The scratch starts with the same header and per-request plan words as a
+  // workspace (zero before the first call: no error).
+  return msa_check_device_error(scratch, flags, stream);
+}

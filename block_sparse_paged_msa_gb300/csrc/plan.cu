@@ -308,6 +308,16 @@ const char* msa_status_string(msa_status s) {
 
 msa_status msa_validate_config(const msa_config* cfg) { return check_config(cfg); }
 
+int32_t msa_init_blocks_from_tokens(int32_t tokens, int32_t block_size) {
+  if (tokens < 0 || block_size <= 0) return -1;
+  return (int32_t)(((int64_t)tokens + block_size - 1) / block_size);
+}
+
+int32_t msa_local_blocks_from_tokens(int32_t tokens, int32_t block_size) {
+  if (tokens < 0 || block_size <= 0) return -1;
+  return (int32_t)(((int64_t)tokens + block_size - 1) / block_size + 1);
+}
+
 int32_t msa_selected_width(const msa_config* cfg) {
   return check_config(cfg) == MSA_OK ? width_of(*cfg) : 0;
 }

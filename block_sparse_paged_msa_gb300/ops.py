@@ -53,6 +53,9 @@ _P = ctypes.c_void_p
 _CFG = ctypes.POINTER(MsaConfig)
 _SIGNATURES = {
     "msa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "msa_init_blocks_from_tokens": (ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32]),
+    "msa_local_blocks_from_tokens": (ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32]),
+    "msa_noalloc_check_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _P]),
     "msa_validate_config": (ctypes.c_int, [_CFG]),
     "msa_selected_width": (ctypes.c_int32, [_CFG]),
     "msa_num_splits": (ctypes.c_int32, [_CFG]),
@@ -111,7 +114,9 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else t.data_ptr()
 
 
-def _need(t: torch.Tensor, name: str, dtype=None, dim=None):
+def _need(t: torch.Tensor, name: str, dtype=None, dim=None, rows=None, tail=None):
+    """dtype / rank / contiguity, at least `rows` entries on dim 0, and the
+    trailing dims equal to `tail` (None entries are not checked)."""
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
@@ -120,17 +125,65 @@ def _need(t: torch.Tensor, name: str, dtype=None, dim=None):
         raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
     if dim is not None and t.dim() != dim:
         raise ValueError(f"{name} must have {dim} dims, has {t.dim()}")
+    if rows is not None and t.shape[0] < rows:
+        raise ValueError(f"{name} has {t.shape[0]} rows on dim 0, the config needs {rows}")
+    if tail is not None:
+        got = tuple(t.shape[t.dim() - len(tail):])
+        if any(w is not None and g != w for g, w in zip(got, tail)):
+            raise ValueError(f"{name} has trailing dims {got}, the config needs {tuple(tail)}")
+
+
+def _kv_dtypes(cfg):
+    return (torch.bfloat16,) if cfg.kv_dtype == MSA_KV_BF16 else (torch.float8_e4m3fn, torch.uint8)
+
+
+def max_tokens(cfg) -> int:
+    """Largest number of query tokens a step of `cfg` may hold."""
+    return cfg.max_q_tokens or cfg.max_batch * cfg.q_len
+
+
+def _need_pools(cfg, k_pages=None, v_pages=None, idx_k_pages=None):
+    """The pools must hold cfg.num_pages pages of [H_kv, 128, D | d]: the
+    kernels' TMA maps and page checks are built from cfg.num_pages."""
+    shape = (cfg.num_kv_heads, cfg.block_size, cfg.head_dim)
+    if k_pages is not None:
+        _need(k_pages, "k_pages", _kv_dtypes(cfg), 4, cfg.num_pages, shape)
+    if v_pages is not None:
+        _need(v_pages, "v_pages", _kv_dtypes(cfg), 4, cfg.num_pages, shape)
+    if idx_k_pages is not None:
+        _need(idx_k_pages, "idx_k_pages", torch.bfloat16, 4, cfg.num_pages,
+              (cfg.num_kv_heads, cfg.block_size, cfg.index_dim))
+
+
+def _need_batch(cfg, seq_lens, block_table=None, cu_seqlens_q=None):
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B = seq_lens.shape[0]
+    if B > cfg.max_batch:
+        raise ValueError(f"batch {B} exceeds max_batch {cfg.max_batch}")
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, 2, B, (cfg.max_blocks_per_req,))
+    if cu_seqlens_q is not None:
+        _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1, B + 1)
+    return B
 
 
 # ---------------------------------------------------------------- config
 def local_blocks_from_tokens(local_tokens: int, block_size: int = 128) -> int:
-    """sglang MiniMaxSparseAttnBackend.__init__: sparse_local_tokens -> blocks,
-    ceil(tokens / block) + 1 (the query's own partial block on top)."""
-    return (local_tokens + block_size - 1) // block_size + 1
+    """sglang MiniMaxSparseAttnBackend.__init__: sparse_local_tokens -> blocks
+    (resolved by libmsa, msa_local_blocks_from_tokens)."""
+    n = lib().msa_local_blocks_from_tokens(local_tokens, block_size)
+    if n < 0:
+        raise ValueError(f"local_tokens {local_tokens}, block_size {block_size}")
+    return n
 
 
 def init_blocks_from_tokens(init_tokens: int, block_size: int = 128) -> int:
-    return (init_tokens + block_size - 1) // block_size
+    """sglang MiniMaxSparseAttnBackend.__init__: sparse_init_tokens -> blocks
+    (resolved by libmsa, msa_init_blocks_from_tokens)."""
+    n = lib().msa_init_blocks_from_tokens(init_tokens, block_size)
+    if n < 0:
+        raise ValueError(f"init_tokens {init_tokens}, block_size {block_size}")
+    return n
 
 
 def make_config(*, num_q_heads, num_kv_heads, init_blocks, local_blocks, topk_blocks,
@@ -195,13 +248,60 @@ def status_string(status: int) -> str:
 
 
 # ---------------------------------------------------------------- calls
-def plan(cfg, seq_lens, block_table, ws, cu_seqlens_q=None, stream=None):
-    _need(seq_lens, "seq_lens", torch.int32, 1)
-    _need(block_table, "block_table", torch.int32, 2)
+# Every wrapper checks the tensors against the config before the C ABI sees a
+# pointer: dtypes, contiguity, trailing dims, and enough rows for what the
+# kernels may touch.  Calls that take the step's batch check against that
+# batch; calls that only take the workspace (whose plan may describe any step
+# up to the config's maxima) check against max_tokens(cfg).
+_SIZES = {}
+
+
+def _sizes(cfg):
+    """(workspace bytes, selected width, CSR rows, CSR capacity) of a config,
+    asked of the library once per distinct config."""
+    key = bytes(cfg)
+    v = _SIZES.get(key)
+    if v is None:
+        v = (workspace_bytes(cfg), selected_width(cfg), k2q_rows(cfg), k2q_capacity(cfg))
+        _SIZES[key] = v
+    return v
+
+
+def _need_ws(cfg, ws):
     _need(ws, "ws", torch.uint8)
-    if cu_seqlens_q is not None:
-        _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
-    B = seq_lens.shape[0]
+    n = _sizes(cfg)[0]
+    if ws.numel() < n:
+        raise ValueError(f"ws has {ws.numel()} bytes, the config needs {n}")
+
+
+def _need_block_table(cfg, block_table, B):
+    _need(block_table, "block_table", torch.int32, 2, B)
+    if block_table.shape[1] < cfg.max_blocks_per_req:
+        raise ValueError(f"block_table has {block_table.shape[1]} columns, the config needs "
+                         f"{cfg.max_blocks_per_req}")
+
+
+def _need_tokens(cfg, T, *, q=None, idx_q=None, block_scores=None, selected=None, out=None,
+                 lse=None):
+    if q is not None:
+        _need(q, "q", torch.bfloat16, 3, T, (cfg.num_q_heads, cfg.head_dim))
+    if idx_q is not None:
+        _need(idx_q, "idx_q", torch.bfloat16, 3, T, (cfg.num_kv_heads, cfg.index_dim))
+    if block_scores is not None:
+        _need(block_scores, "block_scores", torch.float32, 3, T,
+              (cfg.num_kv_heads, cfg.max_blocks_per_req))
+    if selected is not None:
+        _need(selected, "selected", torch.int32, 3, T, (cfg.num_kv_heads, _sizes(cfg)[1]))
+    if out is not None:
+        _need(out, "out", torch.bfloat16, 3, T, (cfg.num_q_heads, cfg.head_dim))
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2, T, (cfg.num_q_heads,))
+
+
+def plan(cfg, seq_lens, block_table, ws, cu_seqlens_q=None, stream=None):
+    B = _need_batch(cfg, seq_lens, cu_seqlens_q=cu_seqlens_q)
+    _need_block_table(cfg, block_table, B)
+    _need_ws(cfg, ws)
     _check("msa_plan", lib().msa_plan(ctypes.byref(cfg), B, _ptr(seq_lens), _ptr(cu_seqlens_q),
                                       _ptr(block_table), block_table.shape[1], _ptr(ws),
                                       _stream(stream)))
@@ -209,22 +309,23 @@ def plan(cfg, seq_lens, block_table, ws, cu_seqlens_q=None, stream=None):
 
 def plan_from_req_to_token(cfg, seq_lens, req_to_token, req_pool_indices, ws,
                            cu_seqlens_q=None, stream=None):
-    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B = _need_batch(cfg, seq_lens, cu_seqlens_q=cu_seqlens_q)
     _need(req_to_token, "req_to_token", torch.int32, 2)
-    _need(req_pool_indices, "req_pool_indices", torch.int64, 1)
-    _need(ws, "ws", torch.uint8)
-    if cu_seqlens_q is not None:
-        _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    if req_to_token.shape[1] < cfg.max_blocks_per_req * cfg.block_size:
+        raise ValueError("req_to_token rows are shorter than max_blocks_per_req * block_size")
+    _need(req_pool_indices, "req_pool_indices", torch.int64, 1, B)
+    _need_ws(cfg, ws)
     _check("msa_plan_from_req_to_token", lib().msa_plan_from_req_to_token(
-        ctypes.byref(cfg), seq_lens.shape[0], _ptr(seq_lens), _ptr(cu_seqlens_q),
+        ctypes.byref(cfg), B, _ptr(seq_lens), _ptr(cu_seqlens_q),
         _ptr(req_to_token), req_to_token.shape[1], _ptr(req_pool_indices), _ptr(ws),
         _stream(stream)))
 
 
 def index_score(cfg, ws, idx_q, idx_k_pages, block_scores, stream=None):
-    _need(idx_q, "idx_q", torch.bfloat16, 3)
-    _need(idx_k_pages, "idx_k_pages", torch.bfloat16, 4)
-    _need(block_scores, "block_scores", torch.float32, 3)
+    _need_ws(cfg, ws)
+    T = max_tokens(cfg)
+    _need_tokens(cfg, T, idx_q=idx_q, block_scores=block_scores)
+    _need_pools(cfg, idx_k_pages=idx_k_pages)
     _check("msa_index_score", lib().msa_index_score(
         ctypes.byref(cfg), _ptr(ws), _ptr(idx_q), _ptr(idx_k_pages), _ptr(block_scores),
         _stream(stream)))
@@ -234,46 +335,39 @@ def decode_step(cfg, ws, seq_lens, block_table, idx_q, idx_k_pages, q, k_pages, 
                 block_scores, selected, out, lse, stream=None):
     """One decode / verify step in one call (plan, index score, top-k,
     split-K decode, combine)."""
-    _need(seq_lens, "seq_lens", torch.int32, 1)
-    _need(block_table, "block_table", torch.int32, 2)
-    _need(idx_q, "idx_q", torch.bfloat16, 3)
-    _need(idx_k_pages, "idx_k_pages", torch.bfloat16, 4)
-    _need(q, "q", torch.bfloat16, 3)
-    kv = (torch.bfloat16,) if cfg.kv_dtype == MSA_KV_BF16 else (torch.float8_e4m3fn, torch.uint8)
-    _need(k_pages, "k_pages", kv, 4)
-    _need(v_pages, "v_pages", kv, 4)
-    _need(block_scores, "block_scores", torch.float32, 3)
-    _need(selected, "selected", torch.int32, 3)
-    _need(out, "out", torch.bfloat16, 3)
-    _need(lse, "lse", torch.float32, 2)
+    B = _need_batch(cfg, seq_lens)
+    _need_block_table(cfg, block_table, B)
+    _need_ws(cfg, ws)
+    T = B * cfg.q_len
+    _need_tokens(cfg, T, q=q, idx_q=idx_q, block_scores=block_scores, selected=selected,
+                 out=out, lse=lse)
+    _need_pools(cfg, k_pages, v_pages, idx_k_pages)
     _check("msa_decode_step", lib().msa_decode_step(
-        ctypes.byref(cfg), _ptr(ws), seq_lens.shape[0], _ptr(seq_lens), _ptr(block_table),
+        ctypes.byref(cfg), _ptr(ws), B, _ptr(seq_lens), _ptr(block_table),
         block_table.shape[1], _ptr(idx_q), _ptr(idx_k_pages), _ptr(q), _ptr(k_pages),
         _ptr(v_pages), _ptr(block_scores), _ptr(selected), _ptr(out), _ptr(lse),
         _stream(stream)))
 
 
 def topk_select(cfg, ws, block_scores, selected, stream=None):
-    _need(block_scores, "block_scores", torch.float32, 3)
-    _need(selected, "selected", torch.int32, 3)
+    _need_ws(cfg, ws)
+    _need_tokens(cfg, max_tokens(cfg), block_scores=block_scores, selected=selected)
     _check("msa_topk_select", lib().msa_topk_select(
         ctypes.byref(cfg), _ptr(ws), _ptr(block_scores), _ptr(selected), _stream(stream)))
 
 
 def sparse_decode(cfg, ws, q, k_pages, v_pages, selected, stream=None):
-    _need(q, "q", torch.bfloat16, 3)
-    kv = (torch.bfloat16,) if cfg.kv_dtype == MSA_KV_BF16 else (torch.float8_e4m3fn, torch.uint8)
-    _need(k_pages, "k_pages", kv, 4)
-    _need(v_pages, "v_pages", kv, 4)
-    _need(selected, "selected", torch.int32, 3)
+    _need_ws(cfg, ws)
+    _need_tokens(cfg, max_tokens(cfg), q=q, selected=selected)
+    _need_pools(cfg, k_pages, v_pages)
     _check("msa_sparse_decode", lib().msa_sparse_decode(
         ctypes.byref(cfg), _ptr(ws), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(selected),
         _stream(stream)))
 
 
 def combine(cfg, ws, out, lse, stream=None):
-    _need(out, "out", torch.bfloat16, 3)
-    _need(lse, "lse", torch.float32, 2)
+    _need_ws(cfg, ws)
+    _need_tokens(cfg, max_tokens(cfg), out=out, lse=lse)
     _check("msa_combine", lib().msa_combine(ctypes.byref(cfg), _ptr(ws), _ptr(out), _ptr(lse),
                                             _stream(stream)))
 
@@ -287,23 +381,21 @@ def k2q_capacity(cfg) -> int:
 
 
 def build_k2q_csr(cfg, ws, selected, row_ptr, q_indices, stream=None):
-    _need(selected, "selected", torch.int32, 3)
-    _need(row_ptr, "row_ptr", torch.int32, 1)
-    _need(q_indices, "q_indices", torch.int32, 1)
-    if row_ptr.numel() < k2q_rows(cfg) + 1 or q_indices.numel() < k2q_capacity(cfg):
-        raise ValueError("row_ptr / q_indices smaller than msa_k2q_rows + 1 / msa_k2q_capacity")
+    _need_ws(cfg, ws)
+    _need_tokens(cfg, max_tokens(cfg), selected=selected)
+    _need(row_ptr, "row_ptr", torch.int32, 1, _sizes(cfg)[2] + 1)
+    _need(q_indices, "q_indices", torch.int32, 1, _sizes(cfg)[3])
     _check("msa_build_k2q_csr", lib().msa_build_k2q_csr(
         ctypes.byref(cfg), _ptr(ws), _ptr(selected), _ptr(row_ptr), _ptr(q_indices),
         _stream(stream)))
 
 
 def sparse_prefill(cfg, ws, q, k_pages, v_pages, selected, row_ptr, q_indices, stream=None):
-    _need(q, "q", torch.bfloat16, 3)
-    _need(k_pages, "k_pages", torch.bfloat16, 4)
-    _need(v_pages, "v_pages", torch.bfloat16, 4)
-    _need(selected, "selected", torch.int32, 3)
-    _need(row_ptr, "row_ptr", torch.int32, 1)
-    _need(q_indices, "q_indices", torch.int32, 1)
+    _need_ws(cfg, ws)
+    _need_tokens(cfg, max_tokens(cfg), q=q, selected=selected)
+    _need_pools(cfg, k_pages, v_pages)
+    _need(row_ptr, "row_ptr", torch.int32, 1, _sizes(cfg)[2] + 1)
+    _need(q_indices, "q_indices", torch.int32, 1, _sizes(cfg)[3])
     _check("msa_sparse_prefill", lib().msa_sparse_prefill(
         ctypes.byref(cfg), _ptr(ws), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(selected),
         _ptr(row_ptr), _ptr(q_indices), _stream(stream)))
@@ -321,6 +413,7 @@ def check_device_error(ws, stream=None) -> int:
 def selftest_wait_timeout(cfg: MsaConfig, ws, stream=None):
     """Run the library's bounded wait on a barrier nothing completes (see
     msa_selftest_wait_timeout); the error word then holds MSA_DEVERR_TIMEOUT."""
+    _need_ws(cfg, ws)
     _check("msa_selftest_wait_timeout",
            lib().msa_selftest_wait_timeout(ctypes.byref(cfg), _ptr(ws), _stream(stream)))
 
@@ -380,18 +473,24 @@ def sparse_decode_noalloc(cfg, seq_lens, block_table, q, k_pages, v_pages, selec
     where cudaMalloc is not acceptable).  Scratch is a fixed 16 MiB device
     array inside libmsa; steps that need more raise MsaError (UNSUPPORTED).
     The first call on a device must come before any stream capture; calls
-    that overlap on the GPU share that scratch and race."""
-    _need(seq_lens, "seq_lens", torch.int32, 1)
-    _need(block_table, "block_table", torch.int32, 2)
-    _need(q, "q", torch.bfloat16, 3)
-    kv = (torch.bfloat16,) if cfg.kv_dtype == MSA_KV_BF16 else (torch.float8_e4m3fn, torch.uint8)
-    _need(k_pages, "k_pages", kv, 4)
-    _need(v_pages, "v_pages", kv, 4)
-    _need(selected, "selected", torch.int32, 3)
-    _need(out, "out", torch.bfloat16, 3)
-    _need(lse, "lse", torch.float32, 2)
+    that overlap on the GPU share that scratch and race.  Device-side data
+    errors of the last call: noalloc_check_device_error()."""
+    B = _need_batch(cfg, seq_lens)
+    _need_block_table(cfg, block_table, B)
+    _need_tokens(cfg, B * cfg.q_len, q=q, selected=selected, out=out, lse=lse)
+    _need_pools(cfg, k_pages, v_pages)
     _check("msa_sparse_decode_noalloc", lib().msa_sparse_decode_noalloc(
-        ctypes.byref(cfg), seq_lens.shape[0], _ptr(seq_lens), _ptr(block_table),
+        ctypes.byref(cfg), B, _ptr(seq_lens), _ptr(block_table),
         block_table.shape[1], _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(selected), _ptr(out),
         _ptr(lse), _stream(stream)),
         "(the step may need more than the 16 MiB scratch: see msa_workspace_bytes)")
+
+
+def noalloc_check_device_error(stream=None) -> int:
+    """Synchronises the stream; returns the device error bits the last
+    sparse_decode_noalloc call on the current device recorded (0 = none)."""
+    flags = ctypes.c_int32(0)
+    st = lib().msa_noalloc_check_device_error(ctypes.byref(flags), _stream(stream))
+    if st not in (0, 4):
+        _check("msa_noalloc_check_device_error", st)
+    return flags.value

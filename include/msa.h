@@ -125,6 +125,19 @@ typedef struct msa_config {
 /* Human-readable name of a status (static string). */
 const char* msa_status_string(msa_status status);
 
+/*
+ * Block counts from token counts, as sglang MiniMaxSparseAttnBackend.__init__
+ * resolves a layer's sparse configuration when it gives tokens instead of
+ * blocks:
+ *   msa_init_blocks_from_tokens(n, P)  = ceil(n / P)      (sparse_init_tokens)
+ *   msa_local_blocks_from_tokens(n, P) = ceil(n / P) + 1  (sparse_local_tokens;
+ *                                        the query's own, partly filled block
+ *                                        comes on top of the window)
+ * Host-only, no GPU needed.  Return -1 if n < 0 or P <= 0.
+ */
+int32_t msa_init_blocks_from_tokens(int32_t tokens, int32_t block_size);
+int32_t msa_local_blocks_from_tokens(int32_t tokens, int32_t block_size);
+
 /* MSA_OK if the kernels implement cfg, else INVALID_ARG / UNSUPPORTED.  Every
  * entry point below runs this check first. */
 msa_status msa_validate_config(const msa_config* cfg);
@@ -284,10 +297,15 @@ msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const void* q,
  * than that (msa_workspace_bytes(cfg) > MSA_NOALLOC_SCRATCH_BYTES).
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  All calls share the one array: calls whose work overlaps on the
- * GPU (other streams, other threads) race and must be serialised by the
- * caller.  Each call rewrites every part of the scratch it reads, so earlier
- * contents never leak into a result.
+ * capture.  The cached address belongs to the device's primary context: do
+ * not keep using the library on a device after cudaDeviceReset of it.  All
+ * calls share the one array: calls whose work overlaps on the GPU (other
+ * streams, other threads) race and must be serialised by the caller.  Each
+ * call rewrites every part of the scratch it reads, so earlier contents never
+ * leak into a result.  Data problems found on the device (bad page ids, a
+ * seq_len out of range, a pipeline wait that gave up) are recorded in the
+ * array's error words as for a workspace; msa_noalloc_check_device_error
+ * reads them.
  */
 #define MSA_NOALLOC_SCRATCH_BYTES (16u << 20)
 msa_status msa_sparse_decode_noalloc(const msa_config* cfg, int32_t batch,
@@ -295,6 +313,15 @@ msa_status msa_sparse_decode_noalloc(const msa_config* cfg, int32_t batch,
                                      int32_t bt_stride, const void* q, const void* k_pages,
                                      const void* v_pages, const int32_t* selected, void* out,
                                      float* lse, msa_stream_t stream);
+
+/*
+ * msa_noalloc_check_device_error -- msa_check_device_error for the scratch
+ * array of msa_sparse_decode_noalloc on the current device: synchronises
+ * `stream`, writes the OR of the error bits of the last no-alloc call into
+ * *flags (host) and returns MSA_ERR_DEVICE_FLAG if any is set.  Allocates
+ * nothing; never call it inside stream capture.
+ */
+msa_status msa_noalloc_check_device_error(int32_t* flags, msa_stream_t stream);
 
 /*
  * msa_decode_step -- one decode / verify step (decode mode): msa_plan (with

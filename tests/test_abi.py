@@ -35,6 +35,28 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) <= set(ops._SIGNATURES), set(names) - set(ops._SIGNATURES)
 
 
+def test_block_counts_from_tokens(lib):
+    """The library resolves sglang's token counts into block counts
+    (MiniMaxSparseAttnBackend.__init__); values at the golden file's cases."""
+    import json
+    gold = json.load(open(os.path.join(os.path.dirname(HEADER), "..", "tests", "golden",
+                                       "config_resolution.json")))
+    P = gold["block_size"]
+    for tokens, blocks in gold["local"]:
+        assert lib.msa_local_blocks_from_tokens(tokens, P) == blocks, tokens
+        assert ops.local_blocks_from_tokens(tokens, P) == blocks, tokens
+    for tokens, blocks in gold["init"]:
+        assert lib.msa_init_blocks_from_tokens(tokens, P) == blocks, tokens
+        assert ops.init_blocks_from_tokens(tokens, P) == blocks, tokens
+    assert lib.msa_local_blocks_from_tokens(-1, P) == -1
+    assert lib.msa_init_blocks_from_tokens(5, 0) == -1
+    with pytest.raises(ValueError):
+        ops.local_blocks_from_tokens(-1, P)
+    # config_for takes the library's resolution
+    spec = wl.WORKLOADS["long_decode"]
+    assert ops.config_for(spec).local_blocks == 5
+
+
 def test_status_strings(lib):
     for s, name in ops.STATUS.items():
         assert ops.status_string(s).startswith(name)
@@ -88,6 +110,7 @@ def test_host_side_errors_need_no_gpu(lib):
     bad = _cfg(head_dim=64)
     assert lib.msa_topk_select(ctypes.byref(bad), P(256), P(16), P(16), None) == 2
     assert lib.msa_check_device_error(None, None, None) == 1
+    assert lib.msa_noalloc_check_device_error(None, None) == 1
 
 
 def test_missing_library_raises(monkeypatch, tmp_path):

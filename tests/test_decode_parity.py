@@ -108,3 +108,20 @@ def test_full_size_sampled(name, samples):
     print(name, compare_sampled(w, sa, samples))
     del w, sa
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("q_len,seq_lens", [(1, (140000, 131300)), (4, (139001, 133004))])
+def test_requests_beyond_1024_blocks_every_element(q_len, seq_lens):
+    """Requests longer than 1 024 blocks (131 072 tokens) take the CTA-wide
+    radix select of msa_topk_select instead of the warp one; with 1 KV head
+    and 8 query heads the oracle checks every selection, every block score and
+    every output element.  Integer-valued index vectors make tied block scores
+    common among the ~1 000 candidates, so the tie rule is exercised."""
+    spec = wl.WORKLOADS["medium_decode"].replace(
+        name="beyond_1024_blocks", batch=2, seq_lens=seq_lens, seq_len_range=None,
+        q_len=q_len, num_q_heads=8, num_kv_heads=1, num_pages=2200, seed=1101 + q_len)
+    assert spec.max_blocks > 1024
+    w = wl.make_workload(spec, device="cuda")
+    sa = run_gpu(w)
+    assert msa.check_device_error(sa.ws) == 0
+    print(compare(w, sa, run_oracle(w.to("cpu"))))

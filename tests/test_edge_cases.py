@@ -164,3 +164,32 @@ def test_bounded_wait_times_out_without_fault():
     torch.cuda.synchronize()
     assert msa.check_device_error(sa.ws) == 0
     assert torch.equal(sa.out, out0) and torch.equal(sa.lse, lse0)
+
+
+def test_binding_rejects_tensors_smaller_than_the_config():
+    """The binding compares every tensor with the config before the C ABI sees
+    a pointer: a pool with fewer pages than cfg.num_pages, a selected list of
+    the wrong width, too few output rows, or a short block table raise
+    ValueError and launch nothing."""
+    spec = wl.small("medium_decode", batch=3)
+    w = wl.make_workload(spec, device="cuda")
+    cfg = msa.config_for(spec)
+    sa = msa.SparseAttention(cfg)
+    sa.out.fill_(3)
+    args = dict(seq_lens=w.seq_lens, block_table=w.block_table, idx_q=w.idx_q,
+                idx_k_pages=w.idx_k_pages, q=w.q, k_pages=w.k_pages, v_pages=w.v_pages,
+                block_scores=sa.block_scores, selected=sa.selected, out=sa.out, lse=sa.lse)
+    bad = [("k_pages", w.k_pages[:-1]), ("v_pages", w.v_pages[:, :, :64].contiguous()),
+           ("idx_k_pages", w.idx_k_pages[:2]), ("selected", sa.selected[..., :-1].contiguous()),
+           ("out", sa.out[:1]), ("lse", sa.lse[:, :8].contiguous()),
+           ("q", w.q[:, :32].contiguous()), ("block_table", w.block_table[:, :2].contiguous()),
+           ("block_scores", sa.block_scores[:, :, :3].contiguous())]
+    for name, t in bad:
+        with pytest.raises(ValueError, match=name):
+            msa.ops.decode_step(cfg, sa.ws, **{**args, name: t})
+    with pytest.raises(ValueError, match="k_pages"):
+        msa.sparse_decode(cfg, sa.ws, w.q, w.k_pages[:1], w.v_pages, sa.selected)
+    with pytest.raises(ValueError, match="ws"):
+        msa.plan(cfg, w.seq_lens, w.block_table, sa.ws[:256])
+    torch.cuda.synchronize()
+    assert bool((sa.out == 3).all())
