@@ -1,18 +1,23 @@
 """Benchmark: block-sparse paged MSA decode on GB300.
 
-One step = the whole decode path for one batch (plan -> index score -> top-k
-select -> sparse decode -> combine) on the medium decode workload: batch 32,
-seq_lens uniform in [8192, 32768], 64 query / 8 KV heads, head dim 128, block
-128, init 1 + local 3 + top-16 blocks, index dim 128, 16384-page pool.  Inputs
-are resident in HBM (1.7 GB touched per step, well above the 129 MB L2, so no
-flush is needed).  Prints one JSON line (rank 0).
+Headline: one step = the whole decode path for one batch (plan -> index score
+-> top-k select -> sparse decode -> combine) on the medium decode workload:
+batch 32, seq_lens uniform in [8192, 32768], 64 query / 8 KV heads, head dim
+128, block 128, init 1 + local 3 + top-16 blocks, index dim 128, 16384-page
+pool.  Inputs are resident in HBM (1.6 GB touched per step, well above the
+129 MB L2, so no flush is needed).  The same run then measures every other
+configuration (chunked prefill, fp8 KV decode, speculative verify, long-context
+decode) under the "workloads" key, and times the fp64 oracle on the host cores
+(all of them, and one alone) as the CPU baseline.  Prints one JSON line
+(rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload medium_decode|long_decode|fp8_decode|verify|tiny_decode]
+                  [--workload medium_decode|long_decode|fp8_decode|verify|prefill|tiny_decode]
+                  [--others LIST|none] [--no-cpu-baseline]
 
 N > 1 runs N independent replicas (one per GPU, launched by torchrun); the
 path needs no exchange between GPUs.  ``--impl reference`` times the fp64 CPU
-oracle on the host cores instead (a bounded sample per step).
+oracle on every host core instead (one (token, KV head) pair per core per step).
 """
 from __future__ import annotations
 
@@ -221,11 +226,11 @@ def _oracle_problems(w: wl.Workload, seed: int = 0):
             return x.view(torch.uint8).numpy() if x.dtype == torch.float8_e4m3fn \
                 else x.float().numpy()
         yield dict(
-            seq_lens=[L], q_lens=[nq], block_table=np.arange(nb)[None],
+            seq_lens=np.array([L]), q_lens=np.array([nq]), block_table=np.arange(nb)[None],
             idx_q=w.idx_q[q0:q0 + nq, h:h + 1].float().cpu().numpy(),
             idx_k_pages=host(w.idx_k_pages),
             q=w.q[q0:q0 + nq, h * G:(h + 1) * G].float().cpu().numpy(),
-            k_pages=host(w.k_pages), v_pages=host(w.v_pages), token=t - q0)
+            k_pages=host(w.k_pages), v_pages=host(w.v_pages), token=np.array([t - q0]))
 
 
 def _run_oracle_problem(oracle, s: wl.WorkloadSpec, pr):
@@ -236,55 +241,111 @@ def _run_oracle_problem(oracle, s: wl.WorkloadSpec, pr):
         init_blocks=s.init_blocks,
         local_blocks=oracle.local_blocks_from_tokens(s.local_tokens, s.block_size),
         topk_blocks=s.topk_blocks, softmax_scale=s.softmax_scale, k_scale=s.kv_scale,
-        v_scale=s.kv_scale, kv_is_e4m3=s.kv_dtype == "fp8_e4m3", tokens=[pr["token"]])
+        v_scale=s.kv_scale, kv_is_e4m3=s.kv_dtype == "fp8_e4m3", tokens=[int(pr["token"][0])])
 
 
-def cpu_baseline(w: wl.Workload, budget_s: float = 15.0):
-    """The oracle as it stands, on the host, over a bounded sample of
-    (token, KV head) pairs drawn until about budget_s seconds of oracle time;
-    q-tokens/s = pairs / H_kv / oracle seconds (problem set-up not timed)."""
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_worker(shm_name, layout, spec, first, warmup, steps, budget_s, barrier, results):
+    """One host core: attach the shared problems, wait for every worker, run
+    `warmup` problems untimed, then `steps` problems (or, with steps = 0, as
+    many as fit in budget_s) and report (count, seconds)."""
+    from multiprocessing import shared_memory
     import oracle
+    shm = shared_memory.SharedMemory(name=shm_name)
+    try:
+        probs = [{k: np.ndarray(shape, np.dtype(dt), buffer=shm.buf, offset=off)
+                  for k, (off, shape, dt) in lay.items()} for lay in layout]
+        i = first
+        for _ in range(warmup):
+            _run_oracle_problem(oracle, spec, probs[i % len(probs)])
+            i += 1
+        barrier.wait()
+        n, t0 = 0, time.perf_counter()
+        while (steps and n < steps) or (not steps and time.perf_counter() - t0 < budget_s):
+            _run_oracle_problem(oracle, spec, probs[i % len(probs)])
+            i += 1
+            n += 1
+        results.put((n, time.perf_counter() - t0))
+        del probs
+    finally:
+        shm.close()
+
+
+def run_oracle_pool(w: wl.Workload, workers: int, n_problems: int, *, warmup=1, steps=0,
+                    budget_s=10.0, seed=0):
+    """The oracle, as it stands, on `workers` host processes at once (spawned,
+    so no CUDA state is inherited), single-threaded BLAS in each.  They share
+    n_problems (token, KV head) problems of the workload through shared
+    memory, worker i starting at problem i.  Returns (pairs done, seconds of
+    the slowest worker)."""
+    import multiprocessing as mp
+    from multiprocessing import shared_memory
+    gen = _oracle_problems(w, seed=seed)
+    probs = [next(gen) for _ in range(n_problems)]
+    layout, off = [], 0
+    for pr in probs:
+        lay = {}
+        for k, v in pr.items():
+            v = np.ascontiguousarray(v)
+            lay[k] = (off, v.shape, v.dtype.str)
+            off += (v.nbytes + 63) // 64 * 64
+        layout.append(lay)
+    shm = shared_memory.SharedMemory(create=True, size=max(off, 64))
+    try:
+        for pr, lay in zip(probs, layout):
+            for k, (o, shape, dt) in lay.items():
+                np.ndarray(shape, np.dtype(dt), buffer=shm.buf, offset=o)[...] = pr[k]
+        del probs
+        ctx = mp.get_context("spawn")
+        barrier, results = ctx.Barrier(workers), ctx.Queue()
+        procs = [ctx.Process(target=_oracle_worker,
+                             args=(shm.name, layout, w.spec, i, warmup, steps, budget_s,
+                                   barrier, results)) for i in range(workers)]
+        for p in procs:
+            p.start()
+        got = [results.get(timeout=600) for _ in procs]
+        for p in procs:
+            p.join(timeout=60)
+    finally:
+        shm.close()
+        shm.unlink()
+    return sum(n for n, _ in got), max(t for _, t in got)
+
+
+def cpu_baseline(w: wl.Workload, budget_s: float = 10.0):
+    """The oracle as it stands on the host: all host cores at once (one process
+    per core) and one core alone, each over a bounded sample of (token, KV
+    head) pairs for about budget_s seconds; q-tokens/s = pairs / H_kv / s."""
     s = w.spec
-    spent, done = 0.0, 0
-    for pr in _oracle_problems(w):
-        t0 = time.perf_counter()
-        _run_oracle_problem(oracle, s, pr)
-        spent += time.perf_counter() - t0
-        done += 1
-        if spent > budget_s:
-            break
-    return {"value": done / s.num_kv_heads / spent, "unit": UNIT,
-            "cores": _blas_threads(), "kind": "oracle",
-            "sample": f"{done} random (token, KV head) pairs of {s.name} (one request's "
-                      f"pages each), fp64 numpy, {spent:.1f} s of oracle time"}
-
-
-def _blas_threads():
-    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
-        if os.environ.get(k, "").isdigit():
-            return int(os.environ[k])
-    return 1
+    cores = host_cores()
+    n_all, t_all = run_oracle_pool(w, cores, min(16, cores), budget_s=budget_s)
+    n_one, t_one = run_oracle_pool(w, 1, 4, budget_s=budget_s, seed=1)
+    return {"value": n_all / s.num_kv_heads / t_all, "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "one_core": {"value": n_one / s.num_kv_heads / t_one, "cores": 1},
+            "sample": f"random (token, KV head) pairs of {s.name} (one request's pages each), "
+                      f"fp64 numpy, single-threaded BLAS per process: {n_all} pairs on "
+                      f"{cores} processes in {t_all:.1f} s, {n_one} pairs on one in "
+                      f"{t_one:.1f} s"}
 
 
 # ----------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local_rank):
-    import block_sparse_paged_msa_gb300 as msa
-    from block_sparse_paged_msa_gb300 import build as msa_build
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    if rank == 0 or not os.path.exists(msa.ops.lib_path()):
-        msa_build.build()
-    if world > 1:
-        torch.distributed.barrier()
-    spec = workload_spec(args).replace(seed=workload_spec(args).seed + rank)
-    w = wl.make_workload(spec, device=dev)
-    cfg = msa.config_for(spec)
-    sa = msa.SparseAttention(cfg, device=dev)
-    stream = torch.cuda.current_stream()
-    cu = w.cu_seqlens_q if sa.prefill else None
+LAUNCHES_PER_CALL = {"plan": 1, "index_score": 1, "topk_select": 1, "build_k2q_csr": 7,
+                     "sparse_prefill": 1, "sparse_decode": 1, "combine": 1}
+
+
+def _step_calls(msa, sa, w):
+    """The step's calls, as msa_decode_step chains them (decode / verify) or
+    SparseAttention.run does (prefill)."""
     c = sa.cfg
-    # the step's calls, as msa_decode_step chains them (decode) or
-    # SparseAttention.run does (prefill)
+    cu = w.cu_seqlens_q if sa.prefill else None
     calls = [
         ("plan", lambda: msa.plan(c, w.seq_lens, w.block_table, sa.ws, cu)),
         ("index_score", lambda: msa.index_score(c, sa.ws, w.idx_q, w.idx_k_pages,
@@ -302,62 +363,17 @@ def run_ours(args, rank, world, local_rank):
         calls += [("sparse_decode", lambda: msa.sparse_decode(c, sa.ws, w.q, w.k_pages,
                                                               w.v_pages, sa.selected))]
     calls += [("combine", lambda: msa.combine(c, sa.ws, sa.out, sa.lse))]
-    names = [n for n, _ in calls]
-    launches_per_step = {"plan": 1, "index_score": 1, "topk_select": 1, "build_k2q_csr": 7,
-                         "sparse_prefill": 1, "sparse_decode": 1, "combine": 1}
+    return calls
 
-    dominant = "sparse_prefill" if sa.prefill else "index_score"
-    dom_i = names.index(dominant)
 
-    def step(evs=None, only=None):
-        """One step; events around every call (evs) or only around call `only`.
-        An event between two kernels keeps the second from launching early
-        (programmatic dependent launch), so the timed steps bracket only the
-        dominant kernel."""
-        for i, (_, fn) in enumerate(calls):
-            timed = evs is not None and (only is None or i == only)
-            if timed:
-                evs[i][0].record(stream)
-            fn()
-            if timed:
-                evs[i][1].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    assert msa.check_device_error(sa.ws) == 0
-
-    K = args.steps
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in names] for _ in range(K)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clk:
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        start.record(stream)
-        for k in range(K):
-            step(evs[k], only=dom_i)
-        stop.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-    ms = start.elapsed_time(stop)
-    dom_ms = sum(evs[k][dom_i][0].elapsed_time(evs[k][dom_i][1]) for k in range(K)) / K
-    # per-kernel breakdown, after the timed region (every call bracketed)
-    Kb = min(K, 200)
-    for k in range(Kb):
-        step(evs[k])
-    torch.cuda.synchronize()
-    per_kernel = {n: sum(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(Kb)) / Kb
-                  for i, n in enumerate(names)}
-
-    # ---- e2e: host buffers in, result out, through the public API.  Pipelined
-    # as a serving loop would run it: step i+1's inputs go host -> device on a
-    # copy stream while step i computes, and step i's result comes back on a
-    # second copy stream while step i+1 computes (two SparseAttention
-    # instances and two input buffers alternate).  Every step still moves its
-    # own inputs in and its own result out inside the timed region.
+def _e2e(msa, sa, w, cfg, dev, stream, K, warmup, world):
+    """Throughput through the public API with host buffers: SparseAttention.run
+    per step, each step's inputs copied from pinned host memory and its result
+    read back inside the timed region.  Pipelined as a serving loop would run
+    it: step i+1's inputs go host -> device on a copy stream while step i
+    computes, and step i's result comes back on a second copy stream while step
+    i+1 computes (two SparseAttention instances and two input buffers
+    alternate)."""
     step_inputs = ("seq_lens", "block_table", "idx_q", "q") + (("cu_seqlens_q",) if sa.prefill
                                                                else ())
     pin = {k: getattr(w, k).cpu().pin_memory() for k in step_inputs}
@@ -404,7 +420,7 @@ def run_ours(args, rank, world, local_rank):
         for b in range(2):
             stream.wait_event(ev["out_free"][b])
 
-    e2e_steps(max(3, args.warmup // 4))
+    e2e_steps(max(3, warmup // 4))
     torch.cuda.synchronize()
     Ke = max(10, K // 2)
     if world > 1:
@@ -417,70 +433,177 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     assert all(msa.check_device_error(x.ws) == 0 for x in sas)
+    del sas[1]
+    return Ke, e2e_ms, h2d, d2h
 
-    # ---- accounting
+
+def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False):
+    """Times `steps` steps of one workload after `warmup` untimed ones, the
+    dominant kernel bracketed by CUDA events in the timed region, then a
+    per-kernel breakdown from further steps.  Returns the bench fields."""
+    import block_sparse_paged_msa_gb300 as msa
+    w = wl.make_workload(spec, device=dev)
+    cfg = msa.config_for(spec)
+    sa = msa.SparseAttention(cfg, device=dev)
+    stream = torch.cuda.current_stream()
+    calls = _step_calls(msa, sa, w)
+    names = [n for n, _ in calls]
+    dominant = "sparse_prefill" if sa.prefill else "index_score"
+    dom_i = names.index(dominant)
+
+    def step(evs=None, only=None):
+        """One step; events around every call (evs) or only around call `only`.
+        An event between two kernels keeps the second from launching early
+        (programmatic dependent launch), so the timed steps bracket only the
+        dominant kernel."""
+        for i, (_, fn) in enumerate(calls):
+            timed = evs is not None and (only is None or i == only)
+            if timed:
+                evs[i][0].record(stream)
+            fn()
+            if timed:
+                evs[i][1].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    assert msa.check_device_error(sa.ws) == 0
+
+    K = steps
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in names] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(clock_gpu) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for k in range(K):
+            step(evs[k], only=dom_i)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+    ms = start.elapsed_time(stop)
+    dom_ms = sum(evs[k][dom_i][0].elapsed_time(evs[k][dom_i][1]) for k in range(K)) / K
+    # per-kernel breakdown, after the timed region (every call bracketed)
+    Kb = min(K, 200)
+    for k in range(Kb):
+        step(evs[k])
+    torch.cuda.synchronize()
+    assert msa.check_device_error(sa.ws) == 0
+    per_kernel = {n: sum(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(Kb)) / Kb
+                  for i, n in enumerate(names)}
+    e2e_res = _e2e(msa, sa, w, cfg, dev, stream, K, warmup, world) if e2e else None
+
     T = w.num_tokens
-    ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, dev)
-    value = replica_throughput(T, world, K, ms)
-    e2e_value = replica_throughput(T, world, Ke, e2e_ms)
+    times = [ms, dom_ms] + ([e2e_res[1]] if e2e_res else [])
+    times = max_over_ranks(times, world, dev)
+    ms, dom_ms = times[0], times[1]
     peaks = measured_peaks()
-    result = {
+    r = {
         "metric": METRIC if not sa.prefill else "sparse-prefill query-tokens/s",
-        "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
+        "value": replica_throughput(T, world, K, ms), "unit": UNIT, "steps": K,
+        "warmup": warmup, "ms_per_step": ms / K,
         "dtype": "bf16" if spec.kv_dtype == "bf16" else "fp8_e4m3",
-        "data": "synthetic (seeded; integer-valued bf16 index vectors, N(0,1) bf16 q/k/v)",
         "config": {"workload": spec.name, "batch": spec.batch,
                    "seq_lens": list(spec.seq_len_range or spec.seq_lens[:1]),
                    "q_per_request": spec.q_len,
                    "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads,
                    "head_dim": spec.head_dim, "index_dim": spec.index_dim,
                    "block": spec.block_size, "init_local_topk": [spec.init_blocks,
-                   msa.ops.local_blocks_from_tokens(spec.local_tokens), spec.topk_blocks],
+                   cfg.local_blocks, spec.topk_blocks],
                    "pool_pages": spec.num_pages, "parallelism": f"replicas{world}"},
         "kernels_ms": per_kernel,
         "kernels_ms_note": ("dominant kernel timed in the timed region; the others in "
                             f"{Kb} further steps with every call bracketed by events"),
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "how": "SparseAttention.run per step; inputs of step i+1 uploaded and the "
-                       "result of step i read back on copy streams while step i+1 computes"},
-        "gpu_launches": sum(launches_per_step[n] for n in names) * K,
+        "gpu_launches": sum(LAUNCHES_PER_CALL[n] for n in names) * K,
         "clocks": clk.summary(),
     }
+    if e2e_res is not None:
+        Ke, e2e_ms, h2d, d2h = e2e_res
+        r["e2e"] = {"value": replica_throughput(T, world, Ke, times[2]), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "how": "SparseAttention.run per step; inputs of step i+1 uploaded and the "
+                           "result of step i read back on copy streams while step i+1 "
+                           "computes"}
     if sa.prefill:
         fl = prefill_flops(w, sa.selected)
-        achieved = {n: fl[n] / (per_kernel[n] / 1e3) / 1e12 for n in ("index_score", "sparse_prefill")}
+        achieved = {n: fl[n] / (per_kernel[n] / 1e3) / 1e12
+                    for n in ("index_score", "sparse_prefill")}
         achieved["sparse_prefill"] = fl["sparse_prefill"] / (dom_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
-        result["roofline"] = {
+        r["roofline"] = {
             "bound": "tensor", "kernel": "sparse_prefill", "achieved": achieved["sparse_prefill"],
             "peak": peak[0], "unit": "TFLOP/s", "frac": achieved["sparse_prefill"] / peak[0],
             "peak_source": f"{peak[1]} bf16_tflops_sustained", "launch_ms": dom_ms,
             "traffic": NCU_TRAFFIC_BYTES.get((spec.name, "sparse_prefill"))}
-        result["kernel_tflops"] = achieved
-        result["flops_per_step"] = {k: fl[k] for k in ("index_score", "sparse_prefill")}
-        result["config"]["l2"] = "no flush: K/V + index pools 0.9 GB and 2.7 GB of partials > L2"
+        r["kernel_tflops"] = achieved
+        r["flops_per_step"] = {k: fl[k] for k in ("index_score", "sparse_prefill")}
+        r["config"]["l2"] = "no flush: K/V + index pools 0.9 GB and 2.7 GB of partials > L2"
     else:
         ab = algorithmic_bytes(w)
         db = decode_bytes(w, sa.selected, msa.num_splits(cfg))
         peak = peaks["hbm_gbs"]
         idx_gbs = ab["index_score"] / (dom_ms / 1e3) / 1e9
         step_bytes = ab["index_score"] + db["decode"] + db["combine"]
-        result["roofline"] = {"bound": "hbm", "kernel": "index_score", "achieved": idx_gbs,
-                              "peak": peak[0], "unit": "GB/s", "frac": idx_gbs / peak[0],
-                              "peak_source": f"{peak[1]} hbm_gbs", "launch_ms": dom_ms,
-                              "traffic": NCU_TRAFFIC_BYTES.get((spec.name, "index_score"))}
-        result["step_hbm"] = {"algorithmic_bytes": step_bytes,
-                              "achieved_gbs": step_bytes / (ms / K / 1e3) / 1e9,
-                              "frac": step_bytes / (ms / K / 1e3) / 1e9 / peak[0]}
-        result["kernel_gbs"] = {
+        r["roofline"] = {"bound": "hbm", "kernel": "index_score", "achieved": idx_gbs,
+                         "peak": peak[0], "unit": "GB/s", "frac": idx_gbs / peak[0],
+                         "peak_source": f"{peak[1]} hbm_gbs", "launch_ms": dom_ms,
+                         "traffic": NCU_TRAFFIC_BYTES.get((spec.name, "index_score"))}
+        r["step_hbm"] = {"algorithmic_bytes": step_bytes,
+                         "achieved_gbs": step_bytes / (ms / K / 1e3) / 1e9,
+                         "frac": step_bytes / (ms / K / 1e3) / 1e9 / peak[0]}
+        r["kernel_gbs"] = {
             "index_score": idx_gbs,
             "sparse_decode": db["decode"] / (per_kernel["sparse_decode"] / 1e3) / 1e9,
             "combine": db["combine"] / (per_kernel["combine"] / 1e3) / 1e9}
-        result["config"]["l2"] = (f"no flush: {step_bytes / 1e9:.2f} GB touched per step "
-                                  f"> 129 MB L2")
+        r["kv_bytes_per_step"] = db["kv"]
+        r["config"]["l2"] = (f"no flush: {step_bytes / 1e9:.2f} GB touched per step "
+                             f"> 129 MB L2")
+    del sa
+    return r, w
+
+
+# The other configurations the default run measures beside the headline, with
+# their timed / warm-up steps (each a few dozen milliseconds of GPU time; most
+# of their cost is drawing the inputs, 90 GB for the long decode).
+OTHER_WORKLOADS = {"prefill": (40, 5), "fp8_decode": (200, 10), "verify": (100, 5),
+                   "long_decode": (40, 5)}
+
+
+def run_ours(args, rank, world, local_rank):
+    import block_sparse_paged_msa_gb300 as msa
+    from block_sparse_paged_msa_gb300 import build as msa_build
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if rank == 0 or not os.path.exists(msa.ops.lib_path()):
+        msa_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    clock_gpu = local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0
+    base = workload_spec(args)
+    spec = base.replace(seed=base.seed + rank)
+    result, w = measure(spec, args.steps, args.warmup, dev, world, clock_gpu, e2e=True)
+    result.update({"n_gpus": world, "higher_is_better": True, "scaling": "weak",
+                   "vs_baseline": None,
+                   "data": "synthetic (seeded; integer-valued bf16 index vectors, N(0,1) bf16 "
+                           "q/k/v)"})
+    others = [n for n in args.others.split(",") if n and n != "none" and n != spec.name]
+    if others:
+        # the headline's inputs are kept (the CPU baseline samples them)
+        torch.cuda.empty_cache()
+        result["workloads"] = {}
+        for name in others:
+            K, W = OTHER_WORKLOADS.get(name, (40, 5))
+            o = wl.WORKLOADS[name]
+            r, wo = measure(o.replace(seed=o.seed + rank), K, W, dev, world, clock_gpu)
+            keep = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "dtype",
+                    "roofline", "kernels_ms", "kernel_gbs", "kernel_tflops", "step_hbm",
+                    "clocks", "gpu_launches", "config")
+            result["workloads"][name] = {k: r[k] for k in keep if k in r}
+            del wo
+            torch.cuda.empty_cache()
     return result, w
 
 
@@ -497,29 +620,25 @@ def workload_spec(args) -> wl.WorkloadSpec:
 
 
 def run_reference(args):
-    """The fp64 oracle on the host cores: each step one (token, KV head) pair."""
-    import oracle
+    """The fp64 oracle on every host core: each step is one (token, KV head)
+    pair per core, all cores at once; the timed steps end when the slowest
+    core finishes its share."""
     spec = workload_spec(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     w = wl.make_workload(spec, device=dev)
-    gen = _oracle_problems(w, seed=1)
-    probs = [next(gen) for _ in range(16)]
-    for i in range(args.warmup):
-        _run_oracle_problem(oracle, spec, probs[i % len(probs)])
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        _run_oracle_problem(oracle, spec, probs[i % len(probs)])
-    dt = time.perf_counter() - t0
-    value = args.steps / spec.num_kv_heads / dt
-    cores = _blas_threads()
+    cores = host_cores()
+    n, dt = run_oracle_pool(w, cores, min(16, cores), warmup=args.warmup, steps=args.steps,
+                            seed=1)
+    value = n / spec.num_kv_heads / dt
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)", "config": {"workload": spec.name},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"each step one (token, KV head) pair of {spec.name} "
-                                   f"(one request's pages), fp64 numpy"},
+                         "sample": f"each step one (token, KV head) pair of {spec.name} per "
+                                   f"core (one request's pages), {cores} processes, fp64 "
+                                   f"numpy, single-threaded BLAS per process"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -532,6 +651,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="medium_decode", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--others", default=None,
+                    help="comma-separated workloads measured beside the headline (default: "
+                         "every other configuration when the headline is medium_decode at "
+                         "its full size; 'none' to skip)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller profiling captures)")
     ap.add_argument("--pool-pages", type=int, default=None,
@@ -539,6 +662,10 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.others is None:
+        default = args.workload == "medium_decode" and args.batch is None \
+            and args.pool_pages is None
+        args.others = ",".join(OTHER_WORKLOADS) if default else "none"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
