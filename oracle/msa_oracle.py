@@ -39,7 +39,8 @@ import numpy as np
 __all__ = [
     "init_blocks_from_tokens", "local_blocks_from_tokens", "e4m3_to_float",
     "query_positions", "gather_sequence", "block_scores", "select_blocks",
-    "attention", "combine", "sparse_attention", "build_k2q_csr",
+    "attention", "combine", "sparse_attention", "build_k2q_csr", "e4m3_encode",
+    "cache_slots", "cache_write",
 ]
 
 
@@ -82,6 +83,31 @@ _E4M3_TABLE = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
 def e4m3_to_float(codes: np.ndarray) -> np.ndarray:
     """Decode uint8 e4m3 codes to float64."""
     return _E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+_E4M3_FINITE = _E4M3_TABLE[:0x7F]   # codes 0x00 .. 0x7E: 0 .. 448, ascending
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """Float values -> e4m3fn codes (uint8), from the format's definition: the
+    nearest representable value, ties to the code whose last mantissa bit is 0;
+    magnitudes beyond the largest finite value (448) saturate to it, as the
+    quantise-on-write of an fp8 KV cache clamps instead of making NaN; NaN ->
+    0x7F.  The sign bit is kept (a negative value that rounds to zero is 0x80)."""
+    x = np.asarray(x, dtype=np.float64)
+    mag = np.abs(x)
+    n = len(_E4M3_FINITE)
+    hi = np.clip(np.searchsorted(_E4M3_FINITE, np.nan_to_num(mag, nan=0.0, posinf=1e9)), 0, n - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = mag - _E4M3_FINITE[lo]
+    d_hi = _E4M3_FINITE[hi] - mag
+    code = np.where(d_lo < d_hi, lo, hi)
+    tie = d_lo == d_hi
+    code = np.where(tie, np.where(lo % 2 == 0, lo, hi), code)
+    code = np.where(mag >= _E4M3_FINITE[-1], n - 1, code)          # saturate
+    code = code | np.where(np.signbit(x), 0x80, 0)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
 
 
 # --------------------------------------------------------------------------
@@ -261,6 +287,47 @@ def sparse_attention(*, seq_lens, q_lens, block_table, idx_q, idx_k_pages, q,
             out[t, h * G:(h + 1) * G] = o
             lse[t, h * G:(h + 1) * G] = ls
     return {"scores": scores, "selected": selected, "out": out, "lse": lse}
+
+
+# --------------------------------------------------------------------------
+# Cache write before attention (sglang forward_decode / forward_extend call
+# ``set_fused_kv_index_buffer(layer, out_cache_loc, k, v, idx_k, idx_v)``
+# before the sparse op, which is why seq_lens already counts the new tokens).
+# --------------------------------------------------------------------------
+def cache_slots(seq_lens: Sequence[int], q_lens: Sequence[int], block_table,
+                block_size: int) -> List[int]:
+    """Token slot (page * P + row) of every new query token, token-major: token
+    i of request r sits at position p = seq_len - q_len + i, in page
+    block_table[r][p // P] at row p % P.  Tokens of idle requests: -1."""
+    slots = []
+    for r, p in query_positions(seq_lens, q_lens):
+        if p < 0:
+            slots.append(-1)
+            continue
+        page = int(block_table[r][p // block_size])
+        slots.append(page * block_size + p % block_size)
+    return slots
+
+
+def cache_write(pool: np.ndarray, slots: Sequence[int], rows: np.ndarray,
+                e4m3_scale=None) -> np.ndarray:
+    """A copy of ``pool`` [num_pages, H, P, X] with ``rows[t, h]`` ([T, H, X])
+    stored at page slot // P, head h, row slot % P for every token whose slot
+    is >= 0.  ``e4m3_scale`` None: stored as given (bf16 values); otherwise the
+    pool holds e4m3 codes and each value is stored as the code of
+    float32(x) / float32(scale) (one IEEE fp32 division, then round to e4m3)."""
+    out = pool.copy()
+    P = pool.shape[2]
+    for t, slot in enumerate(slots):
+        if slot < 0:
+            continue
+        page, row = slot // P, slot % P
+        if e4m3_scale is None:
+            out[page, :, row, :] = rows[t]
+        else:
+            q = np.asarray(rows[t], dtype=np.float32) / np.float32(e4m3_scale)
+            out[page, :, row, :] = e4m3_encode(q)
+    return out
 
 
 # --------------------------------------------------------------------------

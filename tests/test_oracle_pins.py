@@ -359,6 +359,64 @@ def test_k2q_csr_round_trip():
             assert sorted(back.get((t, h), [])) == [j for j in sel[t, h] if j >= 0]
 
 
+# ---------------------------------------------------------------- cache write
+def test_e4m3_encode_round_trips_every_finite_code():
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_to_float(codes)), codes)
+
+
+def test_e4m3_encode_matches_torch_on_every_bf16_value_in_range():
+    """Every finite bf16 value (all 2^16 bit patterns) whose magnitude is at most
+    464 (beyond it torch returns NaN where the cache write saturates) encodes
+    to torch's own float8_e4m3fn code: round to nearest, ties to even."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    x = bits.float()
+    keep = torch.isfinite(x) & (x.abs() <= 464)
+    x = x[keep]
+    want = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.e4m3_encode(x.numpy())
+    assert np.array_equal(got, want)
+    # and scaled by 2^-5, the fp8 workloads' scale, as the cache write divides
+    y = (x / 2.0 ** -5)
+    ok = y.abs() <= 464
+    assert np.array_equal(oracle.e4m3_encode(y[ok].numpy()),
+                          y[ok].to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+
+
+def test_e4m3_encode_saturates_and_keeps_nan():
+    x = np.array([448.0, 464.0, 465.0, 1e6, np.inf, -500.0, -np.inf, np.nan, 2.0 ** -10,
+                  3 * 2.0 ** -11, -1e-9])
+    want = [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE, 0x7F, 0x00, 0x01, 0x80]
+    assert oracle.e4m3_encode(x).tolist() == want
+
+
+def test_cache_slots_hand_computed():
+    # request 0: 300 tokens, 1 new -> position 299 = block 2 row 43;
+    # request 1: idle; request 2: 130 tokens, 3 new -> positions 127, 128, 129
+    bt = [[7, 3, 9], [0, 0, 0], [5, 2, 0]]
+    slots = oracle.cache_slots([300, 0, 130], [1, 2, 3], bt, 128)
+    assert slots == [9 * 128 + 43, -1, -1, 5 * 128 + 127, 2 * 128 + 0, 2 * 128 + 1]
+
+
+def test_cache_write_places_rows_and_leaves_the_rest():
+    P, H, X = 4, 2, 3
+    pool = np.zeros((5, H, P, X))
+    rows = np.arange(3 * H * X, dtype=np.float64).reshape(3, H, X) + 1
+    out = oracle.cache_write(pool, [2 * P + 3, -1, 0 * P + 1], rows)
+    want = np.zeros_like(pool)
+    want[2, :, 3, :] = rows[0]
+    want[0, :, 1, :] = rows[2]
+    assert np.array_equal(out, want) and not pool.any()
+    # e4m3: the stored codes are those of float32(x) / float32(scale)
+    codes = np.zeros((5, H, P, X), dtype=np.uint8)
+    x = np.array([[[0.3, -1.7, 9.0], [100.0, -0.01, 1e4]]])
+    out8 = oracle.cache_write(codes, [4 * P], x, e4m3_scale=0.5)
+    want8 = torch.tensor(x[0] / 0.5, dtype=torch.float32).clamp(-448, 448).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(out8[4, :, 0, :], want8)
+    assert out8.sum() == want8.astype(np.int64).sum()
+
+
 # ---------------------------------------------------------------- mutations
 def _mutants():
     """Plausible mistakes, each planted in a copy of one oracle function."""
@@ -396,7 +454,18 @@ def _mutants():
         out, _ = real_combine(o, l)
         return out, float(np.max(l))
 
-    return [("block_scores", scores_sum), ("block_scores", scores_no_causal),
+    real_encode, real_slots = oracle.e4m3_encode, oracle.cache_slots
+
+    def encode_ties_away(x):             # round half away from zero
+        x = np.asarray(x, dtype=np.float64)
+        nudged = np.nextafter(np.abs(x), np.inf) * np.sign(x)
+        return real_encode(np.where(np.isnan(x), x, nudged))
+
+    def slots_one_late(seq_lens, q_lens, bt, P):   # position seq_len - q_len + i + 1
+        return real_slots([L + (L > 0) for L in seq_lens], q_lens, bt, P)
+
+    return [("e4m3_encode", encode_ties_away), ("cache_slots", slots_one_late),
+            ("block_scores", scores_sum), ("block_scores", scores_no_causal),
             ("select_blocks", select_high_tie), ("select_blocks", select_local_off_by_one),
             ("attention", attn_no_scale), ("attention", attn_transposed_v),
             ("combine", combine_lse_is_max)]
@@ -411,6 +480,11 @@ _PINS = [
     test_combine_equals_unsplit,
     test_dense_when_topk_covers_every_block,
     test_sparse_equals_dense_over_selected_tokens,
+    test_e4m3_encode_round_trips_every_finite_code,
+    test_e4m3_encode_matches_torch_on_every_bf16_value_in_range,
+    test_e4m3_encode_saturates_and_keeps_nan,
+    test_cache_slots_hand_computed,
+    test_cache_write_places_rows_and_leaves_the_rest,
 ]
 
 
