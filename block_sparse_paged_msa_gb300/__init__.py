@@ -6,7 +6,8 @@ synthetic inputs.  The library is loaded on first use and every op raises if it
 is missing: there is no CPU fallback.
 """
 from . import workloads  # noqa: F401
-from .ops import (MsaConfig, MsaError, SparseAttention, check_device_error,  # noqa: F401
+from .ops import (MsaConfig, MsaError, SparseAttention, cache_write,  # noqa: F401
+                  check_device_error,
                   combine, config_for, index_score, make_config, num_splits, plan,
                   plan_from_req_to_token, selected_width, sparse_decode, topk_select,
                   workspace_bytes)

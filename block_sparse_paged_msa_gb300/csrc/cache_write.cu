@@ -1,0 +1,116 @@
+// msa_cache_write: the fused K / V / index-key cache write that precedes
+// attention.
+//
+// sglang minimax_sparse_backend.py (MiniMaxSparseAttnBackend.forward_decode and
+// forward_extend) calls set_fused_kv_index_buffer(layer, out_cache_loc, k, v,
+// idx_k, idx_v) before the sparse op: every new token's key, value and index
+// key land in the paged pools first, which is why seq_lens already counts the
+// new tokens when the index scores and the attention run.  Here the slot of a
+// token is either given (out_cache_loc, sglang's page * P + row slot ids) or
+// derived from the step's plan: token i of request r sits at position
+// seq_len - q_len + i, i.e. row pos % P of the page the validated block table
+// maps block pos / P to.
+//
+// Design: byte movement only.  One warp per (token, KV head): lanes 0-15 carry
+// the K row and lanes 16-31 the V row (16 bytes of bf16 each), then the index
+// key row; bf16 pools take the bytes as they are, e4m3 pools store
+// round-to-nearest-even(x / scale) codes, saturated to +-448 (NaN stays NaN),
+// computed with one IEEE fp32 division and the hardware conversion.  A slot
+// outside the pool is skipped and flagged (MSA_DEVERR_PAGE_RANGE), never
+// written.
+#include <cuda_fp8.h>
+
+#include "msa_device.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ uint4 ld_nc(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Two bf16 (one 32-bit word) -> two e4m3 codes of x / scale (low value in the
+// low byte).
+__device__ __forceinline__ uint32_t bf16x2_to_e4m3x2(uint32_t w, float scale) {
+  const float2 f = make_float2(__fdiv_rn(bf16lo(w), scale), __fdiv_rn(bf16hi(w), scale));
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+cache_write_kernel(WsView ws, int Hkv, int max_blocks, int64_t pool_slots, int idx_lanes,
+                   bool fp8, float k_scale, float v_scale, const int64_t* __restrict__ loc,
+                   const uint4* __restrict__ k, const uint4* __restrict__ v,
+                   const uint4* __restrict__ idx_k, uint8_t* __restrict__ k_pages,
+                   uint8_t* __restrict__ v_pages, uint4* __restrict__ idx_pages) {
+  const int lane = threadIdx.x & 31;
+  const int64_t item = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);   // (token, head)
+  griddep_launch_dependents();
+  griddep_wait();            // the plan of this step, and readers of the last one
+  if (item >= (int64_t)ws.hdr->num_tokens * Hkv) return;
+  const int t = (int)(item / Hkv), h = (int)(item % Hkv);
+  const int r = ws.tok_req[t];
+  if (r < 0) return;         // idle request: nothing to store
+  int64_t slot;
+  if (loc != nullptr) {
+    slot = loc[t];
+  } else {
+    const int pos = ws.tok_pos[t];
+    const int page = ws.block_table[(int64_t)r * max_blocks + pos / kBlock];
+    slot = page < 0 ? -1 : (int64_t)page * kBlock + pos % kBlock;
+  }
+  if (slot < 0 || slot >= pool_slots) {
+    if (lane == 0) set_error(ws.hdr, MSA_DEVERR_PAGE_RANGE);
+    return;
+  }
+  // destination row in the [pages * H_kv * P] view of a pool
+  const int64_t row = (slot / kBlock * Hkv + h) * kBlock + slot % kBlock;
+  const int half = lane >> 4, c = lane & 15;
+  const uint4 x = ld_nc((half ? v : k) + item * 16 + c);
+  uint8_t* pool = half ? v_pages : k_pages;
+  if (!fp8) {
+    reinterpret_cast<uint4*>(pool)[row * 16 + c] = x;
+  } else {
+    const float s = half ? v_scale : k_scale;
+    const uint32_t lo = bf16x2_to_e4m3x2(x.x, s) | bf16x2_to_e4m3x2(x.y, s) << 16;
+    const uint32_t hi = bf16x2_to_e4m3x2(x.z, s) | bf16x2_to_e4m3x2(x.w, s) << 16;
+    reinterpret_cast<uint2*>(pool)[row * 16 + c] = make_uint2(lo, hi);
+  }
+  if (idx_k != nullptr && lane < idx_lanes)
+    idx_pages[row * idx_lanes + lane] = ld_nc(idx_k + item * idx_lanes + lane);
+}
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" msa_status msa_cache_write(const msa_config* cfg, void* ws,
+                                      const int64_t* out_cache_loc, const void* k,
+                                      const void* v, const void* idx_k, void* k_pages,
+                                      void* v_pages, void* idx_k_pages, msa_stream_t stream) {
+  msa_status st = check_config(cfg);
+  if (st != MSA_OK) return st;
+  if (!ws || !k || !v || !k_pages || !v_pages || (idx_k != nullptr && idx_k_pages == nullptr))
+    return MSA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_pages) || !aligned16(v_pages) ||
+      (idx_k && (!aligned16(idx_k) || !aligned16(idx_k_pages))))
+    return MSA_ERR_INVALID_ARG;
+  const int64_t items = (int64_t)max_tokens_of(*cfg) * cfg->num_kv_heads;
+  if (items <= 0) return MSA_OK;
+  const int64_t grid = (items + kWarps - 1) / kWarps;
+  if (grid > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
+  const bool fp8 = cfg->kv_dtype == MSA_KV_FP8_E4M3;
+  return launch_pdl(cache_write_kernel, dim3((unsigned)grid), dim3(kWarps * 32), 0,
+                    (cudaStream_t)stream, view_of(*cfg, ws), cfg->num_kv_heads,
+                    cfg->max_blocks_per_req, (int64_t)cfg->num_pages * kBlock,
+                    cfg->index_dim / 8, fp8, fp8 ? cfg->k_scale : 1.f,
+                    fp8 ? cfg->v_scale : 1.f, out_cache_loc, (const uint4*)k, (const uint4*)v,
+                    (const uint4*)idx_k, (uint8_t*)k_pages, (uint8_t*)v_pages,
+                    (uint4*)idx_k_pages);
+}

@@ -64,6 +64,7 @@ _SIGNATURES = {
     "msa_plan_from_req_to_token": (ctypes.c_int, [_CFG, ctypes.c_int32, _P, _P, _P,
                                                   ctypes.c_int32, _P, _P, _P]),
     "msa_index_score": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
+    "msa_cache_write": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "msa_topk_select": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "msa_sparse_decode": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "msa_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
@@ -321,6 +322,27 @@ def plan_from_req_to_token(cfg, seq_lens, req_to_token, req_pool_indices, ws,
         _stream(stream)))
 
 
+def cache_write(cfg, ws, k, v, idx_k, k_pages, v_pages, idx_k_pages, out_cache_loc=None,
+                stream=None):
+    """Store the step's new K / V / index-K rows ([T, H_kv, D | d] bf16) into
+    the pools, after plan() and before index_score() (msa_cache_write).
+    out_cache_loc: [T] int64 slots (page * 128 + row), or None to take each
+    token's slot from the plan's block table and position.  idx_k may be None."""
+    _need_ws(cfg, ws)
+    T = max_tokens(cfg)
+    kv_shape = (cfg.num_kv_heads, cfg.head_dim)
+    _need(k, "k", torch.bfloat16, 3, T, kv_shape)
+    _need(v, "v", torch.bfloat16, 3, T, kv_shape)
+    if idx_k is not None:
+        _need(idx_k, "idx_k", torch.bfloat16, 3, T, (cfg.num_kv_heads, cfg.index_dim))
+    _need_pools(cfg, k_pages, v_pages, idx_k_pages)
+    if out_cache_loc is not None:
+        _need(out_cache_loc, "out_cache_loc", torch.int64, 1, T)
+    _check("msa_cache_write", lib().msa_cache_write(
+        ctypes.byref(cfg), _ptr(ws), _ptr(out_cache_loc), _ptr(k), _ptr(v), _ptr(idx_k),
+        _ptr(k_pages), _ptr(v_pages), _ptr(idx_k_pages), _stream(stream)))
+
+
 def index_score(cfg, ws, idx_q, idx_k_pages, block_scores, stream=None):
     _need_ws(cfg, ws)
     T = max_tokens(cfg)
@@ -443,16 +465,21 @@ class SparseAttention:
             self.q_indices = torch.empty(k2q_capacity(cfg), dtype=torch.int32, device=device)
 
     def run(self, seq_lens, block_table, idx_q, idx_k_pages, q, k_pages, v_pages,
-            cu_seqlens_q=None, stream=None):
+            cu_seqlens_q=None, stream=None, new_kv=None, out_cache_loc=None):
         """Decode / verify: msa_decode_step (plan, index score, top-k,
         split-K decode, combine).  Prefill (cu_seqlens_q required): plan, index
-        score, top-k, CSR, sparse prefill tiles, combine."""
+        score, top-k, CSR, sparse prefill tiles, combine.  new_kv = (k, v,
+        idx_k) first stores the step's new rows into the pools (cache_write,
+        right after the plan; slots from out_cache_loc or from the plan)."""
         c = self.cfg
-        if not self.prefill and cu_seqlens_q is None:
+        if not self.prefill and cu_seqlens_q is None and new_kv is None:
             decode_step(c, self.ws, seq_lens, block_table, idx_q, idx_k_pages, q, k_pages,
                         v_pages, self.block_scores, self.selected, self.out, self.lse, stream)
             return self.out, self.lse
         plan(c, seq_lens, block_table, self.ws, cu_seqlens_q, stream)
+        if new_kv is not None:
+            cache_write(c, self.ws, *new_kv, k_pages, v_pages, idx_k_pages, out_cache_loc,
+                        stream)
         index_score(c, self.ws, idx_q, idx_k_pages, self.block_scores, stream)
         topk_select(c, self.ws, self.block_scores, self.selected, stream)
         if self.prefill:

@@ -231,3 +231,17 @@ def make_workload(spec: WorkloadSpec, device="cpu", kv_pool=True) -> Workload:
         q = torch.empty((T, spec.num_q_heads, D), dtype=torch.bfloat16, device=device)
         k = v = torch.empty((0, Hkv, P, D), dtype=torch.bfloat16, device=device)
     return Workload(spec, seq_lens, q_lens, cu, block_table, idx_q, idx_k, q, k, v)
+
+
+def new_token_rows(spec: WorkloadSpec, num_tokens: int, seed: int, device="cpu"):
+    """The new tokens' key, value and index-key rows a step writes into the
+    cache before attention: k, v [T, H_kv, D] bf16 N(0, 1) and idx_k [T, H_kv,
+    d] integers in [-r, r] as bf16, drawn in that order from `seed`."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    shape = (num_tokens, spec.num_kv_heads, spec.head_dim)
+    k = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    idx_k = _randint_bf16((num_tokens, spec.num_kv_heads, spec.index_dim), spec.index_range,
+                          gen, device)
+    return k, v, idx_k

@@ -189,6 +189,30 @@ msa_status msa_plan_from_req_to_token(const msa_config* cfg, int32_t batch,
                                       msa_stream_t stream);
 
 /*
+ * msa_cache_write -- stores the step's new keys, values and index keys into
+ * the paged pools before attention (sglang MiniMaxSparseAttnBackend
+ * forward_decode / forward_extend call set_fused_kv_index_buffer(layer,
+ * out_cache_loc, k, v, idx_k, idx_v) first; that is why seq_lens counts the
+ * new tokens).  Run it after msa_plan and before msa_index_score of the same
+ * step, on the same workspace.
+ *   out_cache_loc  [T] int64 token slots, slot = page * P + row, or NULL: the
+ *                  slot comes from the plan -- token i of request r (position
+ *                  seq_len - n + i) goes to row pos % P of the page the block
+ *                  table maps block pos / P to
+ *   k, v           [T, H_kv, D] bf16;  idx_k [T, H_kv, d] bf16 or NULL (no
+ *                  index-key write)
+ *   k_pages, v_pages, idx_k_pages: the pools (layouts above)
+ * bf16 pools store the values as they are.  e4m3 pools store, per value, the
+ * e4m3fn code nearest to x / scale (cfg->k_scale or v_scale; one IEEE fp32
+ * division), ties to even, magnitudes beyond 448 saturated to +-448, NaN kept.
+ * Tokens of idle requests are skipped.  A slot outside [0, num_pages * P) is
+ * skipped and sets MSA_DEVERR_PAGE_RANGE.  All pointers 16-byte aligned.
+ */
+msa_status msa_cache_write(const msa_config* cfg, void* ws, const int64_t* out_cache_loc,
+                           const void* k, const void* v, const void* idx_k, void* k_pages,
+                           void* v_pages, void* idx_k_pages, msa_stream_t stream);
+
+/*
  * msa_index_score -- block scores from the index query/key
  * (sglang MiniMaxSparseAttnBackend.__init__ reads the index head dim and
  * score_type; forward_decode passes idx_q and the index-K cache to the sparse
