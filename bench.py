@@ -437,6 +437,34 @@ def _e2e(msa, sa, w, cfg, dev, stream, K, warmup, world):
     return Ke, e2e_ms, h2d, d2h
 
 
+def _cache_write_cost(msa, sa, w, spec, stream, n):
+    """The K / V / index-key cache write that precedes a step (msa_cache_write,
+    slots from the plan), timed alone over n calls after the step's plan: it is
+    not part of the timed step.  Algorithmic bytes: the new rows read (bf16)
+    and written (bf16 or e4m3 K / V, bf16 index keys)."""
+    c = sa.cfg
+    T = w.num_tokens
+    k, v, idx_k = wl.new_token_rows(spec, msa.ops.max_tokens(c), seed=spec.seed + 500,
+                                    device=w.q.device)
+    elem = 1 if spec.kv_dtype == "fp8_e4m3" else 2
+    per = spec.num_kv_heads * (2 * spec.head_dim * (2 + elem) + 2 * spec.index_dim * 2)
+    msa.plan(c, w.seq_lens, w.block_table, sa.ws, w.cu_seqlens_q if sa.prefill else None)
+    call = lambda: msa.cache_write(c, sa.ws, k, v, idx_k, w.k_pages, w.v_pages,  # noqa: E731
+                                   w.idx_k_pages)
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert msa.check_device_error(sa.ws) == 0
+    ms = e0.elapsed_time(e1) / n
+    return {"ms": ms, "bytes": T * per, "gbs": T * per / (ms / 1e3) / 1e9,
+            "note": "msa_cache_write before the step, timed alone (not in the timed step)"}
+
+
 def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False):
     """Times `steps` steps of one workload after `warmup` untimed ones, the
     dominant kernel bracketed by CUDA events in the timed region, then a
@@ -495,6 +523,7 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False):
     per_kernel = {n: sum(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(Kb)) / Kb
                   for i, n in enumerate(names)}
     e2e_res = _e2e(msa, sa, w, cfg, dev, stream, K, warmup, world) if e2e else None
+    cw = _cache_write_cost(msa, sa, w, spec, stream, Kb)
 
     T = w.num_tokens
     times = [ms, dom_ms] + ([e2e_res[1]] if e2e_res else [])
@@ -519,6 +548,7 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False):
                             f"{Kb} further steps with every call bracketed by events"),
         "gpu_launches": sum(LAUNCHES_PER_CALL[n] for n in names) * K,
         "clocks": clk.summary(),
+        "cache_write": cw,
     }
     if e2e_res is not None:
         Ke, e2e_ms, h2d, d2h = e2e_res
@@ -600,7 +630,7 @@ def run_ours(args, rank, world, local_rank):
             r, wo = measure(o.replace(seed=o.seed + rank), K, W, dev, world, clock_gpu)
             keep = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "dtype",
                     "roofline", "kernels_ms", "kernel_gbs", "kernel_tflops", "step_hbm",
-                    "clocks", "gpu_launches", "config")
+                    "clocks", "gpu_launches", "config", "cache_write")
             result["workloads"][name] = {k: r[k] for k in keep if k in r}
             del wo
             torch.cuda.empty_cache()

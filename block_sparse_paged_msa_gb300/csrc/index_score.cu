@@ -217,5 +217,8 @@ extern "C" msa_status msa_index_score(const msa_config* cfg, const void* ws, con
   const WsView v = view_of(*cfg, ws);
   cudaStream_t s = (cudaStream_t)stream;
   if (is_prefill(*cfg)) return prefill_index_score(*cfg, v, idx_q, idx_k_pages, block_scores, s);
+  // Several new tokens per request (speculative verify) share every key tile:
+  // the tensor-core kernel, whose tile stream does not depend on registers.
+  if (cfg->q_len > 1) return decode_index_score_tc(*cfg, v, idx_q, idx_k_pages, block_scores, s);
   return dispatch(*cfg, v, idx_q, idx_k_pages, block_scores, s);
 }

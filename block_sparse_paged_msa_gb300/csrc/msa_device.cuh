@@ -218,6 +218,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WsHead
   return false;
 }
 
+// Bounded wait used only when a kernel retires after a timeout: waits for the
+// phase of `bar` with the given parity (the completion of copies this CTA
+// issued) without giving up early on the error word, so that no copy is still
+// writing this CTA's shared memory when it exits; false if even that runs out.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
 // 2-D tiled TMA load of box (x, y) into shared memory, completion counted on
 // `bar` in bytes.  x * element size must be a multiple of 16 bytes.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,

@@ -172,6 +172,10 @@ bool make_bf16_map(CUtensorMap* m, const void* base, int rank, const int64_t* di
 // Index scores of a prefill chunk (tensor-core tiles; prefill.cu).
 msa_status prefill_index_score(const msa_config& c, const WsView& v, const void* idx_q,
                                const void* idx_k, float* scores, cudaStream_t s);
+// Index scores of a decode / verify step on the tensor cores (TMA-fed tiles;
+// index_score_tc.cu).
+msa_status decode_index_score_tc(const msa_config& c, const WsView& v, const void* idx_q,
+                                 const void* idx_k, float* scores, cudaStream_t s);
 int sm_count();  // SMs of the current device (cached per device)
 
 // Launch-status helper: any launch error becomes MSA_ERR_CUDA.

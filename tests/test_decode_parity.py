@@ -125,3 +125,28 @@ def test_requests_beyond_1024_blocks_every_element(q_len, seq_lens):
     sa = run_gpu(w)
     assert msa.check_device_error(sa.ws) == 0
     print(compare(w, sa, run_oracle(w.to("cpu"))))
+
+
+@pytest.mark.parametrize("q_len", [2, 3, 4])
+@pytest.mark.parametrize("index_dim", [64, 128])
+def test_verify_q_len_and_index_dim_every_element(q_len, index_dim):
+    """Speculative verify with 2, 3 or 4 new tokens per request: the index
+    scores run on the tensor-core kernel (keys as M = 128, the request's query
+    rows as N); block scores and selections bit-exact, every output element
+    within the bounds.  Draft positions straddle block boundaries (ragged
+    lengths), so the per-token causal limits inside the last block differ."""
+    spec = wl.small("verify", q_len=q_len, index_dim=index_dim,
+                    seq_lens=(1500, 127 + q_len, 2600, 3001, 256 + 1), batch=5, num_pages=128,
+                    seed=1200 + 10 * q_len + index_dim // 64)
+    _full_case(spec)
+
+
+def test_verify_bad_page_flagged_and_scored_minus_inf():
+    spec = wl.small("verify", batch=4)
+    w = wl.make_workload(spec, device="cuda")
+    w.block_table[2, 3] = spec.num_pages + 9
+    sa = run_gpu(w)
+    assert msa.check_device_error(sa.ws) & 1
+    # the other requests are exact
+    ref = run_oracle(w.to("cpu"), tokens=list(range(0, 8)) + list(range(12, 16)))
+    compare(w, sa, ref, tokens=list(range(0, 8)) + list(range(12, 16)))
