@@ -451,18 +451,29 @@ def _cache_write_cost(msa, sa, w, spec, stream, n):
     msa.plan(c, w.seq_lens, w.block_table, sa.ws, w.cu_seqlens_q if sa.prefill else None)
     call = lambda: msa.cache_write(c, sa.ws, k, v, idx_k, w.k_pages, w.v_pages,  # noqa: E731
                                    w.idx_k_pages)
-    for _ in range(3):
-        call()
+    call()
+    torch.cuda.synchronize()
+    # a launch this small is paced by the host: time n launches captured in a
+    # CUDA graph, replayed back to back
+    graph, side = torch.cuda.CUDAGraph(), torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(n):
+                call()
+    stream.wait_stream(side)
+    graph.replay()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(n):
-        call()
+    for _ in range(3):
+        graph.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     assert msa.check_device_error(sa.ws) == 0
-    ms = e0.elapsed_time(e1) / n
+    ms = e0.elapsed_time(e1) / (3 * n)
     return {"ms": ms, "bytes": T * per, "gbs": T * per / (ms / 1e3) / 1e9,
-            "note": "msa_cache_write before the step, timed alone (not in the timed step)"}
+            "note": "msa_cache_write before the step (not in the timed step), timed alone "
+                    f"from a CUDA graph of {n} launches"}
 
 
 def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False):
