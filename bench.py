@@ -97,7 +97,7 @@ def algorithmic_bytes(w: wl.Workload):
 def decode_bytes(w: wl.Workload, selected: torch.Tensor, nsplit: int) -> dict:
     s = w.spec
     P, D = s.block_size, s.head_dim
-    elem = 1 if s.kv_dtype == "fp8_e4m3" else 2
+    row = {"bf16": 2 * D, "fp8_e4m3": D, "nvfp4": D // 2 + D // 16}[s.kv_dtype]
     T = w.num_tokens
     sel = selected[:T].long()                                   # [T, Hkv, S]
     q_lens = w.q_lens.long()
@@ -106,7 +106,7 @@ def decode_bytes(w: wl.Workload, selected: torch.Tensor, nsplit: int) -> dict:
            + torch.cat([torch.arange(int(n), device=q_lens.device) for n in q_lens.tolist()]))
     vis = (pos[:, None, None] + 1 - sel * P).clamp(0, P)
     vis = torch.where(sel >= 0, vis, torch.zeros_like(vis))
-    kv = int(vis.sum()) * D * elem * 2
+    kv = int(vis.sum()) * row * 2
     partial = T * s.num_q_heads * nsplit * (D + 1) * 4
     q = T * s.num_q_heads * D * 2
     out = T * s.num_q_heads * (D * 2 + 4)
@@ -221,14 +221,16 @@ def _oracle_problems(w: wl.Workload, seed: int = 0):
         pages = w.block_table[r, :nb].long()
         q0, nq = int(cu[r]), int(w.q_lens[r])
 
-        def host(x):
-            x = x[pages][:, h:h + 1].cpu()
+        hs = slice(2 * h, 2 * h + 2) if s.kv_dtype == "nvfp4" else slice(h, h + 1)
+
+        def host(x, hs=hs):
+            x = x[pages][:, hs].cpu()
             return x.view(torch.uint8).numpy() if x.dtype == torch.float8_e4m3fn \
                 else x.float().numpy()
         yield dict(
             seq_lens=np.array([L]), q_lens=np.array([nq]), block_table=np.arange(nb)[None],
             idx_q=w.idx_q[q0:q0 + nq, h:h + 1].float().cpu().numpy(),
-            idx_k_pages=host(w.idx_k_pages),
+            idx_k_pages=host(w.idx_k_pages, slice(h, h + 1)),
             q=w.q[q0:q0 + nq, h * G:(h + 1) * G].float().cpu().numpy(),
             k_pages=host(w.k_pages), v_pages=host(w.v_pages), token=np.array([t - q0]))
 
@@ -241,7 +243,8 @@ def _run_oracle_problem(oracle, s: wl.WorkloadSpec, pr):
         init_blocks=s.init_blocks,
         local_blocks=oracle.local_blocks_from_tokens(s.local_tokens, s.block_size),
         topk_blocks=s.topk_blocks, softmax_scale=s.softmax_scale, k_scale=s.kv_scale,
-        v_scale=s.kv_scale, kv_is_e4m3=s.kv_dtype == "fp8_e4m3", tokens=[int(pr["token"][0])])
+        v_scale=s.kv_scale, kv_is_e4m3=s.kv_dtype == "fp8_e4m3",
+        kv_is_nvfp4=s.kv_dtype == "nvfp4", tokens=[int(pr["token"][0])])
 
 
 def host_cores() -> int:
@@ -444,6 +447,8 @@ def _cache_write_cost(msa, sa, w, spec, stream, n):
     and written (bf16 or e4m3 K / V, bf16 index keys)."""
     c = sa.cfg
     T = w.num_tokens
+    if spec.kv_dtype == "nvfp4":
+        return None                  # the cache write has no NVFP4 form
     k, v, idx_k = wl.new_token_rows(spec, msa.ops.max_tokens(c), seed=spec.seed + 500,
                                     device=w.q.device)
     elem = 1 if spec.kv_dtype == "fp8_e4m3" else 2
@@ -545,7 +550,7 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False):
         "metric": METRIC if not sa.prefill else "sparse-prefill query-tokens/s",
         "value": replica_throughput(T, world, K, ms), "unit": UNIT, "steps": K,
         "warmup": warmup, "ms_per_step": ms / K,
-        "dtype": "bf16" if spec.kv_dtype == "bf16" else "fp8_e4m3",
+        "dtype": spec.kv_dtype,
         "config": {"workload": spec.name, "batch": spec.batch,
                    "seq_lens": list(spec.seq_len_range or spec.seq_lens[:1]),
                    "q_per_request": spec.q_len,
@@ -609,8 +614,8 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False):
 # The other configurations the default run measures beside the headline, with
 # their timed / warm-up steps (each a few dozen milliseconds of GPU time; most
 # of their cost is drawing the inputs, 90 GB for the long decode).
-OTHER_WORKLOADS = {"prefill": (40, 5), "fp8_decode": (200, 10), "verify": (100, 5),
-                   "long_decode": (40, 5)}
+OTHER_WORKLOADS = {"prefill": (40, 5), "fp8_decode": (200, 10), "nvfp4_decode": (200, 10),
+                   "verify": (100, 5), "long_decode": (40, 5)}
 
 
 def run_ours(args, rank, world, local_rank):

@@ -16,12 +16,19 @@ the MiniMax-M3 sparse-attention backends are built for (sglang
 * ``seq_lens[r]``: the KV length of request r *including* its new query tokens
   (the cache write precedes attention in ``forward_decode``); query i of a
   request with ``n_q`` new tokens sits at position ``seq_lens[r] - n_q + i``;
-* queries ``q: [T, H_q, D]`` and index queries ``idx_q: [T, H_kv, d]``, token-major.
+* queries ``q: [T, H_q, D]`` and index queries ``idx_q: [T, H_kv, d]``, token-major;
+* an NVFP4 KV pool is one uint8 tensor ``[num_pages, 2 * H_kv, P, D/2 + D/16]``
+  (slot 2h: keys of KV head h, slot 2h + 1: its values), passed as both
+  ``k_pages`` and ``v_pages``: each 72-byte row is 64 bytes of packed FP4 codes
+  followed by 8 E4M3 block scales.
 
 Draw order (fixed, so a seed names one input set): seq_lens, page permutation,
 idx_q, idx_k, q, k, v.  Index values are integers in [-4, 4] stored as bf16, so
 every index dot product is exact in fp32.  Q/K/V are bf16 N(0, 1).  An fp8 KV
-pool stores round-to-nearest-even e4m3 codes of N(0, 1)/scale.
+pool stores round-to-nearest-even e4m3 codes of N(0, 1)/scale.  An NVFP4 pool
+holds uniformly random FP4 codes (all 16, both signs) with block-scale codes
+uniform over the e4m3 codes of [0.25, 1] (0x28 .. 0x38), so dequantised values
+reach +-6 with the tensor scale on top.
 """
 from __future__ import annotations
 
@@ -52,8 +59,8 @@ class WorkloadSpec:
     seq_lens: Optional[tuple] = None          # explicit KV lengths, or
     seq_len_range: Optional[tuple] = None     # inclusive uniform integer range
     q_len: int = 1                            # new query tokens per request
-    kv_dtype: str = "bf16"                    # "bf16" | "fp8_e4m3"
-    kv_scale: float = 1.0                     # per-tensor fp8 scale (k and v)
+    kv_dtype: str = "bf16"                    # "bf16" | "fp8_e4m3" | "nvfp4"
+    kv_scale: float = 1.0                     # per-tensor fp8 / nvfp4 scale (k and v)
     block_size: int = BLOCK
     index_range: int = 4                      # index values uniform in [-r, r]
 
@@ -101,6 +108,12 @@ WORKLOADS = {
         num_q_heads=64, num_kv_heads=8, head_dim=128, index_dim=128,
         init_blocks=1, local_tokens=256, topk_blocks=8, num_pages=16384,
         kv_dtype="fp8_e4m3", kv_scale=2.0 ** -5, seed=1004),
+    # NVFP4 KV cache with the medium decode shapes
+    "nvfp4_decode": WorkloadSpec(
+        name="nvfp4_decode", batch=32, seq_len_range=(8192, 32768),
+        num_q_heads=64, num_kv_heads=8, head_dim=128, index_dim=128,
+        init_blocks=1, local_tokens=256, topk_blocks=16, num_pages=16384,
+        kv_dtype="nvfp4", kv_scale=0.75, seed=1007),
     # chunked prefill: 4 requests, 16384 cached tokens + a 2048-token chunk each
     "prefill": WorkloadSpec(
         name="prefill", batch=4, seq_lens=(18432,) * 4, q_len=2048,
@@ -124,6 +137,7 @@ def small(name: str, **kw) -> WorkloadSpec:
     defaults = {
         "medium_decode": dict(batch=4, seq_len_range=(700, 3000), num_pages=160),
         "fp8_decode": dict(batch=4, seq_len_range=(700, 3000), num_pages=160),
+        "nvfp4_decode": dict(batch=4, seq_len_range=(700, 3000), num_pages=160),
         "long_decode": dict(batch=3, seq_len_range=(3000, 6000), num_pages=200),
         "tiny_decode": dict(),
         "verify": dict(batch=4, seq_lens=(1500, 2000, 2600, 3001), num_pages=128),
@@ -166,6 +180,23 @@ def _randn_kv(shape, spec: WorkloadSpec, gen, device, chunk_rows=4096) -> torch.
             flat[s:e] = x.to(torch.bfloat16)
         else:
             flat[s:e] = (x / spec.kv_scale).to(torch.float8_e4m3fn)
+    return out
+
+
+def _nvfp4_pool(spec: WorkloadSpec, gen, device, chunk_rows=256) -> torch.Tensor:
+    """[num_pages, 2 H_kv, P, D/2 + D/16] uint8: random FP4 code bytes, then
+    block-scale codes uniform over 0x28 .. 0x38 (e4m3 0.25 .. 1.0)."""
+    D = spec.head_dim
+    shape = (spec.num_pages, 2 * spec.num_kv_heads, spec.block_size, D // 2 + D // 16)
+    out = torch.empty(shape, dtype=torch.uint8, device=device)
+    flat = out.view(shape[0], -1, shape[-1])
+    for s in range(0, shape[0], chunk_rows):
+        e = min(shape[0], s + chunk_rows)
+        n = flat.shape[1]
+        flat[s:e, :, :D // 2] = torch.randint(0, 256, (e - s, n, D // 2), generator=gen,
+                                              device=device, dtype=torch.int32).to(torch.uint8)
+        flat[s:e, :, D // 2:] = torch.randint(0x28, 0x39, (e - s, n, D // 16), generator=gen,
+                                              device=device, dtype=torch.int32).to(torch.uint8)
     return out
 
 
@@ -225,8 +256,11 @@ def make_workload(spec: WorkloadSpec, device="cpu", kv_pool=True) -> Workload:
     if kv_pool:
         q = torch.randn((T, spec.num_q_heads, D), generator=gen, device=device,
                         dtype=torch.float32).to(torch.bfloat16)
-        k = _randn_kv((spec.num_pages, Hkv, P, D), spec, gen, device, chunk_rows=256)
-        v = _randn_kv((spec.num_pages, Hkv, P, D), spec, gen, device, chunk_rows=256)
+        if spec.kv_dtype == "nvfp4":
+            k = v = _nvfp4_pool(spec, gen, device)     # one pool: K and V slots per head
+        else:
+            k = _randn_kv((spec.num_pages, Hkv, P, D), spec, gen, device, chunk_rows=256)
+            v = _randn_kv((spec.num_pages, Hkv, P, D), spec, gen, device, chunk_rows=256)
     else:
         q = torch.empty((T, spec.num_q_heads, D), dtype=torch.bfloat16, device=device)
         k = v = torch.empty((0, Hkv, P, D), dtype=torch.bfloat16, device=device)

@@ -40,7 +40,8 @@ __all__ = [
     "init_blocks_from_tokens", "local_blocks_from_tokens", "e4m3_to_float",
     "query_positions", "gather_sequence", "block_scores", "select_blocks",
     "attention", "combine", "sparse_attention", "build_k2q_csr", "e4m3_encode",
-    "cache_slots", "cache_write",
+    "cache_slots", "cache_write", "e2m1_to_float", "nvfp4_dequant", "nvfp4_row_bytes",
+    "NVFP4_BLOCK",
 ]
 
 
@@ -108,6 +109,51 @@ def e4m3_encode(x: np.ndarray) -> np.ndarray:
     code = code | np.where(np.signbit(x), 0x80, 0)
     code = np.where(np.isnan(x), 0x7F, code)
     return code.astype(np.uint8)
+
+
+# --------------------------------------------------------------------------
+# NVFP4 KV pages (vLLM sparse_attention_msa.py, MiniMaxM3SparseMSANvfp4Backend:
+# HND pages in which every KV head has two slots, its keys and its values, each
+# token row holding packed FP4 data plus block scales; per-layer k / v scales).
+# The format, from its definition: an element is FP4 E2M1 (1 sign bit, 2
+# exponent bits with bias 1, 1 mantissa bit; exponent 0 is subnormal m * 0.5),
+# two per byte, the even element in the low nibble; every 16 consecutive
+# elements share one E4M3 scale.  A D = 128 row is 64 data bytes followed by
+# 8 scale bytes (72 bytes).  Value = e2m1(code) * e4m3(scale) * tensor scale.
+# --------------------------------------------------------------------------
+def _e2m1_value(code: int) -> float:
+    sign = -1.0 if code & 0x8 else 1.0
+    exp = (code >> 1) & 0x3
+    man = code & 0x1
+    if exp == 0:
+        return sign * man * 0.5
+    return sign * (1.0 + man / 2.0) * 2.0 ** (exp - 1)
+
+
+_E2M1_TABLE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+NVFP4_BLOCK = 16
+
+
+def e2m1_to_float(codes: np.ndarray) -> np.ndarray:
+    """Decode 4-bit e2m1 codes (0..15) to float64."""
+    return _E2M1_TABLE[np.asarray(codes, dtype=np.uint8) & 0xF]
+
+
+def nvfp4_row_bytes(head_dim: int) -> int:
+    """Bytes of one token row of an NVFP4 slot: head_dim / 2 data + head_dim / 16 scales."""
+    return head_dim // 2 + head_dim // NVFP4_BLOCK
+
+
+def nvfp4_dequant(rows: np.ndarray, head_dim: int) -> np.ndarray:
+    """[..., row_bytes] uint8 NVFP4 rows -> [..., head_dim] float64 (block scales
+    applied, the tensor scale not)."""
+    rows = np.asarray(rows, dtype=np.uint8)
+    data = rows[..., :head_dim // 2]
+    scales = rows[..., head_dim // 2:head_dim // 2 + head_dim // NVFP4_BLOCK]
+    vals = np.empty(rows.shape[:-1] + (head_dim,), dtype=np.float64)
+    vals[..., 0::2] = e2m1_to_float(data & 0xF)
+    vals[..., 1::2] = e2m1_to_float(data >> 4)
+    return vals * np.repeat(e4m3_to_float(scales), NVFP4_BLOCK, axis=-1)
 
 
 # --------------------------------------------------------------------------
@@ -235,13 +281,16 @@ def sparse_attention(*, seq_lens, q_lens, block_table, idx_q, idx_k_pages, q,
                      k_pages, v_pages, num_kv_heads: int, block_size: int,
                      init_blocks: int, local_blocks: int, topk_blocks: int,
                      softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
-                     kv_is_e4m3: bool = False, tokens=None,
+                     kv_is_e4m3: bool = False, kv_is_nvfp4: bool = False, tokens=None,
                      kv_heads=None) -> Dict[str, object]:
     """Index score -> block selection -> attention over the selected blocks.
 
     Arrays are numpy: ``idx_q [T, H_kv, d]``, ``idx_k_pages [pages, H_kv, P, d]``,
     ``q [T, H_q, D]``, ``k_pages / v_pages [pages, H_kv, P, D]`` (float, or uint8
     e4m3 codes when ``kv_is_e4m3``; dequantised value = decoded code * scale).
+    ``kv_is_nvfp4``: ``k_pages`` and ``v_pages`` are NVFP4 pools [pages, 2 H_kv,
+    P, row bytes] whose slot 2h holds the keys and slot 2h + 1 the values of KV
+    head h; value = nvfp4_dequant(row) * k_scale (keys) or * v_scale (values).
     ``tokens`` / ``kv_heads`` restrict the work to a sample (default: all).
 
     Returns dict with, per computed (t, h): ``scores[(t, h)]`` [nb],
@@ -262,8 +311,14 @@ def sparse_attention(*, seq_lens, q_lens, block_table, idx_q, idx_k_pages, q,
         if r not in seq_cache:
             L = int(seq_lens[r])
             ik = gather_sequence(idx_k_pages, block_table[r], L, block_size)
-            kk = gather_sequence(k_pages, block_table[r], L, block_size)
-            vv = gather_sequence(v_pages, block_table[r], L, block_size)
+            if kv_is_nvfp4:
+                kk = gather_sequence(k_pages[:, 0::2], block_table[r], L, block_size)
+                vv = gather_sequence(v_pages[:, 1::2], block_table[r], L, block_size)
+                kk = nvfp4_dequant(kk.astype(np.uint8), q.shape[2]) * k_scale
+                vv = nvfp4_dequant(vv.astype(np.uint8), q.shape[2]) * v_scale
+            else:
+                kk = gather_sequence(k_pages, block_table[r], L, block_size)
+                vv = gather_sequence(v_pages, block_table[r], L, block_size)
             if kv_is_e4m3:
                 kk = e4m3_to_float(kk.astype(np.uint8)) * k_scale
                 vv = e4m3_to_float(vv.astype(np.uint8)) * v_scale

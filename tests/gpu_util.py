@@ -71,14 +71,15 @@ def sub_problem(w: wl.Workload, t: int, h: int) -> wl.Workload:
     sub_spec = spec.replace(batch=1, num_kv_heads=1, num_q_heads=G, num_pages=nb,
                             seq_lens=(L,), seq_len_range=None, q_len=nq)
     hs = slice(h, h + 1)
+    kvs = slice(2 * h, 2 * h + 2) if spec.kv_dtype == "nvfp4" else hs   # NVFP4: K and V slots
     return wl.Workload(
         spec=sub_spec,
         seq_lens=w.seq_lens[r:r + 1].cpu(), q_lens=w.q_lens[r:r + 1].cpu(),
         cu_seqlens_q=torch.tensor([0, nq], dtype=torch.int32),
         block_table=torch.arange(nb, dtype=torch.int32)[None],
         idx_q=w.idx_q[q0:q0 + nq, hs].cpu(), idx_k_pages=w.idx_k_pages[pages][:, hs].cpu(),
-        q=w.q[q0:q0 + nq, h * G:(h + 1) * G].cpu(), k_pages=w.k_pages[pages][:, hs].cpu(),
-        v_pages=w.v_pages[pages][:, hs].cpu()), r, q0
+        q=w.q[q0:q0 + nq, h * G:(h + 1) * G].cpu(), k_pages=w.k_pages[pages][:, kvs].cpu(),
+        v_pages=w.v_pages[pages][:, kvs].cpu()), r, q0
 
 
 def compare_sampled(w: wl.Workload, sa, samples):

@@ -33,7 +33,8 @@ def run_oracle(w: Workload, tokens=None, kv_heads=None, scale=None):
         local_blocks=oracle_local_blocks(w), topk_blocks=s.topk_blocks,
         softmax_scale=s.softmax_scale if scale is None else scale,
         k_scale=s.kv_scale, v_scale=s.kv_scale,
-        kv_is_e4m3=(s.kv_dtype == "fp8_e4m3"), tokens=tokens, kv_heads=kv_heads)
+        kv_is_e4m3=(s.kv_dtype == "fp8_e4m3"), kv_is_nvfp4=(s.kv_dtype == "nvfp4"),
+        tokens=tokens, kv_heads=kv_heads)
 
 
 def selected_array(res, T, H, S) -> np.ndarray:

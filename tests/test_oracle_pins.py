@@ -417,6 +417,58 @@ def test_cache_write_places_rows_and_leaves_the_rest():
     assert out8.sum() == want8.astype(np.int64).sum()
 
 
+# ---------------------------------------------------------------- NVFP4
+def test_e2m1_codes_are_the_published_value_set():
+    """FP4 E2M1 from the format's definition: the eight magnitudes are
+    0, 0.5, 1, 1.5, 2, 3, 4, 6 in code order, the sign bit negates."""
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert oracle.e2m1_to_float(np.arange(8)).tolist() == mags
+    neg = oracle.e2m1_to_float(np.arange(8, 16))
+    assert neg.tolist() == [-m for m in mags] and np.signbit(neg).all()
+
+
+def test_nvfp4_row_hand_decoded():
+    """One 72-byte row built by hand: nibble order (even element low), block
+    scale indexing (elements 16b .. 16b + 15 use scale byte b) and the scale
+    values (e4m3 codes)."""
+    D = 128
+    assert oracle.nvfp4_row_bytes(D) == 72
+    row = np.zeros(72, dtype=np.uint8)
+    row[0] = 0x3 | (0xA << 4)           # element 0: code 3 = 1.5, element 1: code 10 = -1.0
+    row[8] = 0x7                         # element 16: 6.0 (block 1), element 17: 0
+    row[63] = 0xF << 4                   # element 127: -6.0 (block 7)
+    row[64] = 0x38                       # block 0 scale: 1.0
+    row[65] = 0x30                       # block 1 scale: 0.5
+    row[71] = 0x01                       # block 7 scale: the smallest subnormal, 2^-9
+    got = oracle.nvfp4_dequant(row, D)
+    want = np.zeros(D)
+    want[0], want[1], want[16], want[127] = 1.5, -1.0, 3.0, -6.0 * 2.0 ** -9
+    assert np.array_equal(got, want)
+
+
+def test_nvfp4_path_uses_dequantised_values():
+    """Attention over an NVFP4 pool equals attention over the float pools that
+    hold its dequantised values times the tensor scales (K from slot 2h, V from
+    slot 2h + 1)."""
+    spec = wl.small("nvfp4_decode", batch=2, seq_len_range=(300, 700), num_pages=16,
+                    num_q_heads=8, num_kv_heads=2)
+    w = wl.make_workload(spec)
+    res = run_oracle(w)
+    pool = to_np(w.k_pages)
+    P, D = spec.block_size, spec.head_dim
+    kf = oracle.nvfp4_dequant(pool[:, 0::2].astype(np.uint8), D) * 0.75
+    vf = oracle.nvfp4_dequant(pool[:, 1::2].astype(np.uint8), D) * 0.75
+    plain = oracle.sparse_attention(
+        seq_lens=to_np(w.seq_lens), q_lens=to_np(w.q_lens), block_table=to_np(w.block_table),
+        idx_q=to_np(w.idx_q), idx_k_pages=to_np(w.idx_k_pages), q=to_np(w.q), k_pages=kf,
+        v_pages=vf, num_kv_heads=spec.num_kv_heads, block_size=P, init_blocks=1,
+        local_blocks=oracle_local_blocks(w), topk_blocks=spec.topk_blocks,
+        softmax_scale=spec.softmax_scale)
+    assert spec.kv_scale == 0.75
+    assert np.array_equal(res["out"], plain["out"]) and np.array_equal(res["lse"], plain["lse"])
+    assert kf.max() <= 6 * 1.0 * 0.75 and np.abs(vf).max() > 0
+
+
 # ---------------------------------------------------------------- mutations
 def _mutants():
     """Plausible mistakes, each planted in a copy of one oracle function."""
@@ -464,7 +516,22 @@ def _mutants():
     def slots_one_late(seq_lens, q_lens, bt, P):   # position seq_len - q_len + i + 1
         return real_slots([L + (L > 0) for L in seq_lens], q_lens, bt, P)
 
-    return [("e4m3_encode", encode_ties_away), ("cache_slots", slots_one_late),
+    real_e2m1 = oracle.e2m1_to_float
+    real_nvfp4 = oracle.nvfp4_dequant
+
+    def e2m1_no_subnormal(codes):        # exponent 0 read as a normal number
+        c = np.asarray(codes, dtype=np.uint8) & 0xF
+        v = real_e2m1(c)
+        sub = ((c >> 1) & 3) == 0
+        return np.where(sub & ((c & 1) == 1), np.where(c & 8, -1.5, 1.5), v)
+
+    def nvfp4_nibbles_swapped(rows, D):  # odd element in the low nibble
+        rows = np.asarray(rows, dtype=np.uint8).copy()
+        rows[..., :D // 2] = (rows[..., :D // 2] >> 4) | ((rows[..., :D // 2] & 0xF) << 4)
+        return real_nvfp4(rows, D)
+
+    return [("e2m1_to_float", e2m1_no_subnormal), ("nvfp4_dequant", nvfp4_nibbles_swapped),
+            ("e4m3_encode", encode_ties_away), ("cache_slots", slots_one_late),
             ("block_scores", scores_sum), ("block_scores", scores_no_causal),
             ("select_blocks", select_high_tie), ("select_blocks", select_local_off_by_one),
             ("attention", attn_no_scale), ("attention", attn_transposed_v),
@@ -485,6 +552,8 @@ _PINS = [
     test_e4m3_encode_saturates_and_keeps_nan,
     test_cache_slots_hand_computed,
     test_cache_write_places_rows_and_leaves_the_rest,
+    test_e2m1_codes_are_the_published_value_set,
+    test_nvfp4_row_hand_decoded,
 ]
 
 
