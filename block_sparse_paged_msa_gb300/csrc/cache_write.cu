@@ -96,6 +96,7 @@ extern "C" msa_status msa_cache_write(const msa_config* cfg, void* ws,
                                       void* v_pages, void* idx_k_pages, msa_stream_t stream) {
   msa_status st = check_config(cfg);
   if (st != MSA_OK) return st;
+  if (cfg->kv_dtype == MSA_KV_NVFP4) return MSA_ERR_UNSUPPORTED;   // no quantise-on-write form
   if (!ws || !k || !v || !k_pages || !v_pages || (idx_k != nullptr && idx_k_pages == nullptr))
     return MSA_ERR_INVALID_ARG;
   if (!aligned16(k) || !aligned16(v) || !aligned16(k_pages) || !aligned16(v_pages) ||

@@ -29,10 +29,18 @@
 //  * e4m3 tiles: K feeds an fp16 MMA straight from shared memory (the index
 //    dimension is permuted so a thread's four K values of a k-step are one
 //    32-bit load), V is converted to fp16 rows by its warp; e4m3 is exact in
-//    fp16, k_scale folds into the softmax scale and v_scale into the output.
+//    fp16, k_scale folds into the softmax scale and v_scale into the output;
+//  * NVFP4 slots (vLLM MiniMaxM3SparseMSANvfp4Backend: each KV head's keys and
+//    values are two slots of packed FP4 data plus block scales) arrive as 1-D
+//    bulk copies of 9 KiB per (page, head, K|V) -- 72-byte rows are not a TMA
+//    tile shape -- and are dequantised the same way: a thread's four K values
+//    of a k-step are two bytes of E2M1 codes in one 16-element scale block, so
+//    K = e2m1 x e4m3 is formed in registers (exact in fp16: at most 6
+//    significant bits, magnitudes 2^-10 .. 2688) and V rows likewise.
 // msa_combine then merges the splits in a fixed order (deterministic).
 #include <cuda.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "msa_device.cuh"
@@ -48,6 +56,20 @@ constexpr int kStages = 3;                         // ring depth (tiles)
 constexpr int kTileBytes = kBlock * kHeadDim * 2;  // bf16 tile, 32 KiB
 constexpr int kFp8Stages = 4;                      // fp8 tiles are 16 KiB
 constexpr int kFp8TileBytes = kBlock * kHeadDim;
+constexpr int kFp4Row = kHeadDim / 2 + kHeadDim / 16;   // NVFP4 row: 64 data + 8 scale bytes
+constexpr int kFp4Stages = 7;                      // NVFP4 slots are 9 KiB (two CTAs per SM)
+constexpr int kFp4TileBytes = kBlock * kFp4Row;
+
+// KV forms of the decode kernel.
+enum KvForm { kKvBf16 = 0, kKvFp8 = 1, kKvFp4 = 2 };
+
+template <int KV>
+struct KvTraits {
+  static constexpr int kStagesN = KV == kKvBf16 ? kStages : (KV == kKvFp8 ? kFp8Stages : kFp4Stages);
+  static constexpr int kTile = KV == kKvBf16 ? kTileBytes
+                                             : (KV == kKvFp8 ? kFp8TileBytes : kFp4TileBytes);
+  static constexpr bool kF16 = KV != kKvBf16;      // fp16 MMAs on dequantised operands
+};
 constexpr int kConvBytes = 32 * 256;               // per consumer warp: 32 rows, f16
 constexpr int kItems = 2;                          // work-item records in flight
 
@@ -65,6 +87,8 @@ struct DecodeArgs {
   float v_scale;
   const __nv_bfloat16* q;
   const int32_t* selected;
+  const uint8_t* k_pool;   // NVFP4: the pools, read with bulk copies (no tensor map)
+  const uint8_t* v_pool;
 };
 
 // The blocks of work item (t, h, split s), as a lane-distributed list: lane i
@@ -136,21 +160,68 @@ __device__ __forceinline__ void convert_v_rows(const uint8_t* tile, uint8_t* con
   }
 }
 
+// Two FP4 E2M1 codes (one byte, the even element in the low nibble) -> f16x2.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t h;
+  asm("{\n .reg .b8 b;\n cvt.u8.u32 b, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}"
+      : "=r"(h)
+      : "r"(byte));
+  return h;
+}
+
+// An E4M3 block-scale byte -> f16x2 holding it twice.
+__device__ __forceinline__ uint32_t e4m3_scale_f16x2(uint32_t byte) {
+  return e4m3x2_to_f16x2((uint16_t)(byte | (byte << 8)));
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
+                            *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// NVFP4: the warp converts its 32 rows of a V slot (72-byte rows: 64 bytes of
+// E2M1 codes, 8 E4M3 block scales) to f16 rows in its private staging area
+// (256-byte swizzled rows), zeroing rows past the last visible token.
+__device__ __forceinline__ void convert_v_rows_fp4(const uint8_t* tile, uint8_t* conv, int warp,
+                                                   int ntok, int lane) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int idx = k * 32 + lane;            // 32 rows x 8 blocks of 16 elements
+    const int rl = idx >> 3, c = idx & 7;
+    const int row = warp * 32 + rl;
+    uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (row < ntok) {
+      const uint8_t* rp = tile + row * kFp4Row;
+      const uint2 w = *reinterpret_cast<const uint2*>(rp + 8 * c);
+      const uint32_t sc = e4m3_scale_f16x2(rp[kHeadDim / 2 + c]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        o[e] = hmul2_u32(e2m1x2_to_f16x2((w.x >> (8 * e)) & 0xffu), sc);
+        o[4 + e] = hmul2_u32(e2m1x2_to_f16x2((w.y >> (8 * e)) & 0xffu), sc);
+      }
+    }
+    *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // Persistent split-K decode.  Warp 4 produces: for every block of every work
 // item of this CTA it waits for a free ring slot and issues the K and the V
 // tile as 2-D TMA loads.  Warps 0-3 consume: warp w owns tokens [32w, 32w+32)
 // of every tile, runs S = Q K^T and P V on m16n8k16 tensor-core MMAs with its
 // own online softmax, and the four states merge once per work item.
-template <bool FP8>
+template <int KV>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
               const __grid_constant__ CUtensorMap tmap_v) {
-  constexpr int NST = FP8 ? kFp8Stages : kStages;
-  constexpr int TB = FP8 ? kFp8TileBytes : kTileBytes;
+  constexpr int NST = KvTraits<KV>::kStagesN;
+  constexpr int TB = KvTraits<KV>::kTile;
+  constexpr bool F16 = KvTraits<KV>::kF16;     // fp16 MMAs, V converted per warp
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem;                                      // NST x TB, 1 KiB aligned
   uint8_t* conv = smem + NST * TB;                           // fp8: 4 x 8 KiB
-  uint8_t* qbuf = conv + (FP8 ? kConsumers * kConvBytes : 0);   // kItems x G x 256 B
+  uint8_t* qbuf = conv + (F16 ? kConsumers * kConvBytes : 0);   // kItems x G x 256 B
   float* merge = reinterpret_cast<float*>(qbuf + kItems * a.G * 256);
   __shared__ __align__(8) uint64_t full_bar[NST], empty_bar[NST];
   __shared__ __align__(8) uint64_t item_full[kItems], item_empty[kItems];
@@ -243,10 +314,16 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
           for (int kind = 0; kind < 2; ++kind) {
             mbar_wait(&empty_bar[stage], phase ^ 1u, ws.hdr);
             mbar_arrive_expect_tx(&full_bar[stage], TB);
-            const void* tm = kind == 0 ? (const void*)&tmap_k : (const void*)&tmap_v;
             uint8_t* dst = ring + stage * TB;
-            tma_load_2d(dst, tm, 0, y, &full_bar[stage]);
-            if (!FP8) tma_load_2d(dst + TB / 2, tm, 64, y, &full_bar[stage]);
+            if (KV == kKvFp4) {
+              // slot 2h (keys) or 2h + 1 (values) of the page
+              const int64_t slot = ((int64_t)meta[islot].page[bi] * a.Hkv + h) * 2 + kind;
+              bulk_load(dst, (kind == 0 ? a.k_pool : a.v_pool) + slot * TB, TB, &full_bar[stage]);
+            } else {
+              const void* tm = kind == 0 ? (const void*)&tmap_k : (const void*)&tmap_v;
+              tma_load_2d(dst, tm, 0, y, &full_bar[stage]);
+              if (KV == kKvBf16) tma_load_2d(dst + TB / 2, tm, 64, y, &full_bar[stage]);
+            }
             if (++stage == NST) { stage = 0; phase ^= 1u; }
           }
         }
@@ -288,7 +365,7 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
           const __nv_bfloat16* qr = qb + row * kHeadDim;
           if (row >= a.G) {
             qa[ks][hr] = qa[ks][hr + 2] = 0u;
-          } else if (FP8) {
+          } else if (F16) {
             const uint2 w = *reinterpret_cast<const uint2*>(qr + ks * 16 + 4 * tq);
             qa[ks][hr] = bf16x2_to_f16x2(w.x);
             qa[ks][hr + 2] = bf16x2_to_f16x2(w.y);
@@ -317,7 +394,18 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-        if (FP8) {
+        if (KV == kKvFp4) {
+          // d = 16 ks + 4 tq + {0,1 | 2,3}: two bytes of codes in scale block ks
+          const uint8_t* rp = kt + (warp * 32 + nt * 8 + g) * kFp4Row;
+          const uint2 sb = *reinterpret_cast<const uint2*>(rp + kHeadDim / 2);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t w = *reinterpret_cast<const uint16_t*>(rp + 8 * ks + 2 * tq);
+            const uint32_t sc2 = e4m3_scale_f16x2(((ks < 4 ? sb.x : sb.y) >> (8 * (ks & 3))) & 0xffu);
+            mma_f16(sc[nt], qa[ks], hmul2_u32(e2m1x2_to_f16x2(w & 0xffu), sc2),
+                    hmul2_u32(e2m1x2_to_f16x2(w >> 8), sc2));
+          }
+        } else if (F16) {
           const int row = warp * 32 + nt * 8 + g;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
@@ -375,7 +463,7 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
       for (int nt = 0; nt < 4; ++nt) {
         const float p0 = exp2f(sc[nt][0] - mref[0]), p1 = exp2f(sc[nt][1] - mref[0]);
         const float p2 = exp2f(sc[nt][2] - mref[1]), p3 = exp2f(sc[nt][3] - mref[1]);
-        if (FP8) {
+        if (F16) {
           const __half2 h01 = __floats2half2_rn(p0, p1), h23 = __floats2half2_rn(p2, p3);
           const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
           l_r[0] += f01.x + f01.y;
@@ -395,8 +483,11 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
       uint8_t* vt = ring + stage * TB;
       uint32_t vbase;
       int vrow0;
-      if (FP8) {
-        convert_v_rows(vt, my_conv, warp, ntok, lane);
+      if (F16) {
+        if (KV == kKvFp4)
+          convert_v_rows_fp4(vt, my_conv, warp, ntok, lane);
+        else
+          convert_v_rows(vt, my_conv, warp, ntok, lane);
         __syncwarp();
         vbase = smem_u32(my_conv);
         vrow0 = 0;
@@ -419,7 +510,7 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
 #pragma unroll
         for (int nd = 0; nd < 16; nd += 2) {
           uint32_t b0, b1, b2, b3;
-          if (FP8) {
+          if (F16) {
             ldsm_x4_t(vbase + swz(row, nd + (lane >> 4)), b0, b1, b2, b3);
             mma_f16(acc[nd], pa[kk], b0, b1);
             mma_f16(acc[nd + 1], pa[kk], b2, b3);
@@ -644,15 +735,15 @@ combine_prefill_kernel(WsView ws, int Hq, int Hkv, int S, __nv_bfloat16* __restr
   reinterpret_cast<uint4*>(out + idx * kHeadDim)[c] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
 }
 
-template <bool FP8>
+template <int KV>
 size_t decode_smem(int G) {
-  const size_t ring = FP8 ? (size_t)kFp8Stages * kFp8TileBytes : (size_t)kStages * kTileBytes;
-  const size_t conv = FP8 ? (size_t)kConsumers * kConvBytes : 0;
+  const size_t ring = (size_t)KvTraits<KV>::kStagesN * KvTraits<KV>::kTile;
+  const size_t conv = KvTraits<KV>::kF16 ? (size_t)kConsumers * kConvBytes : 0;
   return ring + conv + (size_t)kItems * G * kHeadDim * 2 +
          (size_t)(kConsumers - 1) * G * kHeadDim * 4;
 }
 
-template <bool FP8>
+template <int KV>
 msa_status launch_decode(const WsView& v, const DecodeArgs& a, const CUtensorMap& tk,
                          const CUtensorMap& tv, cudaStream_t s) {
   static std::mutex mu;
@@ -660,12 +751,12 @@ msa_status launch_decode(const WsView& v, const DecodeArgs& a, const CUtensorMap
   static size_t smem_set[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return MSA_ERR_CUDA;
-  const size_t smem = decode_smem<FP8>(a.G);
+  const size_t smem = decode_smem<KV>(a.G);
   int grid;
   {
     std::lock_guard<std::mutex> lk(mu);
     if (smem_set[dev] < smem) {
-      if (cudaFuncSetAttribute(decode_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(decode_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem) != cudaSuccess)
         return MSA_ERR_CUDA;
       smem_set[dev] = smem;
@@ -673,7 +764,7 @@ msa_status launch_decode(const WsView& v, const DecodeArgs& a, const CUtensorMap
     }
     if (grid_per_dev[dev] == 0) {
       int per_sm = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<FP8>, kThreads,
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<KV>, kThreads,
                                                         smem) != cudaSuccess)
         return MSA_ERR_CUDA;
       grid_per_dev[dev] = sm_count() * (per_sm > 0 ? per_sm : 1);
@@ -682,7 +773,7 @@ msa_status launch_decode(const WsView& v, const DecodeArgs& a, const CUtensorMap
   }
   if (grid > a.n_items) grid = a.n_items;
   if (grid <= 0) return MSA_OK;
-  return launch_pdl(decode_kernel<FP8>, dim3(grid), dim3(kThreads), smem, s, v, a, tk, tv);
+  return launch_pdl(decode_kernel<KV>, dim3(grid), dim3(kThreads), smem, s, v, a, tk, tv);
 }
 
 }  // namespace
@@ -711,19 +802,27 @@ extern "C" msa_status msa_sparse_decode(const msa_config* cfg, void* ws, const v
   if (items <= 0) return MSA_OK;
   if (items > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
   a.n_items = (int)items;
-  const bool fp8 = cfg->kv_dtype == MSA_KV_FP8_E4M3;
-  a.scale_log2 = cfg->softmax_scale * (fp8 ? cfg->k_scale : 1.f) * kLog2e;
-  a.v_scale = fp8 ? cfg->v_scale : 1.f;
+  const bool scaled = cfg->kv_dtype != MSA_KV_BF16;
+  a.scale_log2 = cfg->softmax_scale * (scaled ? cfg->k_scale : 1.f) * kLog2e;
+  a.v_scale = scaled ? cfg->v_scale : 1.f;
   a.q = (const __nv_bfloat16*)q;
   a.selected = selected;
-  const int64_t rows = (int64_t)cfg->num_pages * a.Hkv * kBlock;
-  if (rows > 0x7fffffff) return MSA_ERR_UNSUPPORTED;   // TMA row coordinates are int32
-  CUtensorMap tk, tv;
-  if (!make_pool_map(&tk, k_pages, rows, fp8) || !make_pool_map(&tv, v_pages, rows, fp8))
-    return MSA_ERR_CUDA;
+  a.k_pool = (const uint8_t*)k_pages;
+  a.v_pool = (const uint8_t*)v_pages;
   const WsView v = view_of(*cfg, ws);
   cudaStream_t s = (cudaStream_t)stream;
-  return fp8 ? launch_decode<true>(v, a, tk, tv, s) : launch_decode<false>(v, a, tk, tv, s);
+  CUtensorMap tk, tv;
+  if (cfg->kv_dtype == MSA_KV_NVFP4) {
+    memset(&tk, 0, sizeof(tk));      // bulk copies from the pool pointers instead
+    memset(&tv, 0, sizeof(tv));
+    return launch_decode<kKvFp4>(v, a, tk, tv, s);
+  }
+  const bool fp8 = cfg->kv_dtype == MSA_KV_FP8_E4M3;
+  const int64_t rows = (int64_t)cfg->num_pages * a.Hkv * kBlock;
+  if (rows > 0x7fffffff) return MSA_ERR_UNSUPPORTED;   // TMA row coordinates are int32
+  if (!make_pool_map(&tk, k_pages, rows, fp8) || !make_pool_map(&tv, v_pages, rows, fp8))
+    return MSA_ERR_CUDA;
+  return fp8 ? launch_decode<kKvFp8>(v, a, tk, tv, s) : launch_decode<kKvBf16>(v, a, tk, tv, s);
 }
 
 namespace msa {

@@ -43,8 +43,10 @@ msa_status check_config(const msa_config* c) {
       c->blocks_per_split < 0 || !(c->softmax_scale > 0.f))
     return MSA_ERR_INVALID_ARG;
   if (c->num_q_heads % c->num_kv_heads != 0) return MSA_ERR_INVALID_ARG;
-  if (c->kv_dtype != MSA_KV_BF16 && c->kv_dtype != MSA_KV_FP8_E4M3) return MSA_ERR_INVALID_ARG;
-  if (c->kv_dtype == MSA_KV_FP8_E4M3 && !(c->k_scale > 0.f && c->v_scale > 0.f))
+  if (c->kv_dtype != MSA_KV_BF16 && c->kv_dtype != MSA_KV_FP8_E4M3 &&
+      c->kv_dtype != MSA_KV_NVFP4)
+    return MSA_ERR_INVALID_ARG;
+  if (c->kv_dtype != MSA_KV_BF16 && !(c->k_scale > 0.f && c->v_scale > 0.f))
     return MSA_ERR_INVALID_ARG;
   if (c->head_dim != kHeadDim || c->block_size != kBlock) return MSA_ERR_UNSUPPORTED;
   if (c->index_dim != 64 && c->index_dim != 128) return MSA_ERR_UNSUPPORTED;

@@ -17,7 +17,8 @@ import torch
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsa.so")
 _lib = None
 
-MSA_KV_BF16, MSA_KV_FP8_E4M3 = 0, 1
+MSA_KV_BF16, MSA_KV_FP8_E4M3, MSA_KV_NVFP4 = 0, 1, 2
+KV_DTYPES = {"bf16": MSA_KV_BF16, "fp8_e4m3": MSA_KV_FP8_E4M3, "nvfp4": MSA_KV_NVFP4}
 MSA_MODE_DECODE, MSA_MODE_PREFILL = 0, 1
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED",
           3: "MSA_ERR_CUDA", 4: "MSA_ERR_DEVICE_FLAG"}
@@ -135,7 +136,11 @@ def _need(t: torch.Tensor, name: str, dtype=None, dim=None, rows=None, tail=None
 
 
 def _kv_dtypes(cfg):
-    return (torch.bfloat16,) if cfg.kv_dtype == MSA_KV_BF16 else (torch.float8_e4m3fn, torch.uint8)
+    if cfg.kv_dtype == MSA_KV_BF16:
+        return (torch.bfloat16,)
+    if cfg.kv_dtype == MSA_KV_FP8_E4M3:
+        return (torch.float8_e4m3fn, torch.uint8)
+    return (torch.uint8,)
 
 
 def max_tokens(cfg) -> int:
@@ -147,6 +152,8 @@ def _need_pools(cfg, k_pages=None, v_pages=None, idx_k_pages=None):
     """The pools must hold cfg.num_pages pages of [H_kv, 128, D | d]: the
     kernels' TMA maps and page checks are built from cfg.num_pages."""
     shape = (cfg.num_kv_heads, cfg.block_size, cfg.head_dim)
+    if cfg.kv_dtype == MSA_KV_NVFP4:    # K and V slots per head, 72-byte rows
+        shape = (2 * cfg.num_kv_heads, cfg.block_size, cfg.head_dim // 2 + cfg.head_dim // 16)
     if k_pages is not None:
         _need(k_pages, "k_pages", _kv_dtypes(cfg), 4, cfg.num_pages, shape)
     if v_pages is not None:
@@ -197,7 +204,7 @@ def make_config(*, num_q_heads, num_kv_heads, init_blocks, local_blocks, topk_bl
     c.head_dim, c.block_size = head_dim, block_size
     c.init_blocks, c.local_blocks, c.topk_blocks = init_blocks, local_blocks, topk_blocks
     c.index_dim, c.q_len = index_dim, q_len
-    c.kv_dtype = {"bf16": MSA_KV_BF16, "fp8_e4m3": MSA_KV_FP8_E4M3}[kv_dtype]
+    c.kv_dtype = KV_DTYPES[kv_dtype]
     c.softmax_scale = 1.0 / math.sqrt(head_dim) if softmax_scale is None else softmax_scale
     c.k_scale, c.v_scale = k_scale, v_scale
     c.max_batch, c.max_q_tokens = max_batch, max_q_tokens

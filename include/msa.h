@@ -24,7 +24,8 @@
  *  - Layouts (row-major, contiguous):
  *      q            [T, H_q, D]            bf16
  *      idx_q        [T, H_kv, d]           bf16
- *      k_pages      [num_pages, H_kv, P, D] bf16, or fp8 e4m3 codes (kv_dtype)
+ *      k_pages      [num_pages, H_kv, P, D] bf16, or fp8 e4m3 codes (kv_dtype),
+ *                   or NVFP4 slots [num_pages, 2 H_kv, P, 72] (MSA_KV_NVFP4)
  *      v_pages      [num_pages, H_kv, P, D] same type as k_pages
  *      idx_k_pages  [num_pages, H_kv, P, d] bf16
  *      block_table  [batch, >= max_blocks_per_req] int32 (row stride given);
@@ -70,7 +71,17 @@ typedef enum msa_status {
 
 typedef enum msa_kv_dtype {
   MSA_KV_BF16 = 0,
-  MSA_KV_FP8_E4M3 = 1        /* e4m3 "fn" codes; value = decode(code) * scale */
+  MSA_KV_FP8_E4M3 = 1,       /* e4m3 "fn" codes; value = decode(code) * scale */
+  MSA_KV_NVFP4 = 2           /* NVFP4 slots (vLLM MiniMaxM3SparseMSANvfp4Backend):
+                                each pool is [num_pages, 2 * H_kv, P, 72] bytes,
+                                slot 2h = keys, slot 2h + 1 = values of KV head
+                                h; a 72-byte token row is 64 bytes of FP4 E2M1
+                                codes (element 2i in the low nibble of byte i)
+                                then 8 E4M3 scales, one per 16 elements; value
+                                = e2m1(code) * e4m3(block scale) * k_scale or
+                                v_scale.  Keys are read from k_pages, values
+                                from v_pages (the same combined pool is passed
+                                twice).  Decode / verify only.                */
 } msa_kv_dtype;
 
 typedef enum msa_mode {
@@ -112,8 +123,8 @@ typedef struct msa_config {
                                  2..4 = speculative verify                       */
   int32_t kv_dtype;           /* msa_kv_dtype                                    */
   float softmax_scale;        /* applied to q.k before the softmax               */
-  float k_scale;              /* fp8 only: dequantised k = e4m3(code) * k_scale  */
-  float v_scale;              /* fp8 only: dequantised v = e4m3(code) * v_scale  */
+  float k_scale;              /* fp8 / nvfp4: dequantised k = code value * k_scale */
+  float v_scale;              /* fp8 / nvfp4: dequantised v = code value * v_scale */
   int32_t max_batch;          /* largest batch a plan may describe               */
   int32_t max_q_tokens;       /* largest T; 0 = max_batch * q_len                */
   int32_t max_blocks_per_req; /* block-table width used; seq_len <= this * P     */
@@ -207,6 +218,7 @@ msa_status msa_plan_from_req_to_token(const msa_config* cfg, int32_t batch,
  * division), ties to even, magnitudes beyond 448 saturated to +-448, NaN kept.
  * Tokens of idle requests are skipped.  A slot outside [0, num_pages * P) is
  * skipped and sets MSA_DEVERR_PAGE_RANGE.  All pointers 16-byte aligned.
+ * NVFP4 pools have no write form here (MSA_ERR_UNSUPPORTED).
  */
 msa_status msa_cache_write(const msa_config* cfg, void* ws, const int64_t* out_cache_loc,
                            const void* k, const void* v, const void* idx_k, void* k_pages,
@@ -245,7 +257,8 @@ msa_status msa_topk_select(const msa_config* cfg, const void* ws,
  * msa_sparse_decode -- split-K flash decoding over the selected blocks only
  * (vLLM sparse_attention_msa.py module docstring and
  * MiniMaxM3SparseMSAImpl.forward: split-K decode over the top-k blocks with
- * block_table, seq_lens and decode_query_len; fp8 KV is dequantised on load).
+ * block_table, seq_lens and decode_query_len; fp8 and NVFP4 KV are dequantised
+ * on load, the NVFP4 pages read directly in their packed form).
  * For each token t, KV head h and split s, every query head of h's group runs
  * an online softmax over the tokens of the split's selected blocks that are at
  * or before t's position, and the normalised partial output and its
@@ -298,7 +311,7 @@ msa_status msa_build_k2q_csr(const msa_config* cfg, const void* ws, const int32_
  * G + g, so that a tile's rows are contiguous; msa_combine merges each token's
  * slots into out / lse.  selected is not read (the CSR build recorded what it
  * needs).  q, k_pages and v_pages must be 16-byte aligned.  Prefill mode, bf16
- * KV only (fp8 -> MSA_ERR_UNSUPPORTED).
+ * KV only (fp8 or nvfp4 -> MSA_ERR_UNSUPPORTED).
  */
 msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const void* q,
                               const void* k_pages, const void* v_pages,

@@ -77,6 +77,11 @@ def test_validate_config(lib):
     assert ops.validate_config(_cfg(local_blocks=0)) == 1
     assert ops.validate_config(_cfg(q_len=0)) == 1
     assert ops.validate_config(_cfg(kv_dtype="fp8_e4m3", k_scale=0.0)) == 1
+    assert ops.validate_config(_cfg(kv_dtype="nvfp4", k_scale=0.5, v_scale=0.5)) == 0
+    assert ops.validate_config(_cfg(kv_dtype="nvfp4", v_scale=0.0)) == 1
+    bad = _cfg()
+    bad.kv_dtype = 3
+    assert ops.validate_config(bad) == 1
     assert ops.validate_config(_cfg(softmax_scale=-1.0)) == 1
 
 

@@ -27,8 +27,8 @@ def _full_case(spec):
     return compare(w, sa, run_oracle(w.to("cpu")))
 
 
-@pytest.mark.parametrize("name", ["tiny_decode", "medium_decode", "fp8_decode", "long_decode",
-                                  "verify"])
+@pytest.mark.parametrize("name", ["tiny_decode", "medium_decode", "fp8_decode", "nvfp4_decode",
+                                  "long_decode", "verify"])
 def test_small_workloads_every_element(name):
     spec = wl.WORKLOADS[name] if name == "tiny_decode" else wl.small(name)
     print(name, _full_case(spec))
@@ -99,6 +99,7 @@ def test_verify_full_size_sampled():
 @pytest.mark.parametrize("name,samples", [
     ("long_decode", [(0, 0), (127, 7), (37, 3), (64, 5), (100, 1), (5, 6)]),
     ("fp8_decode", [(0, 0), (31, 7), (9, 3), (17, 5), (25, 1), (4, 6)]),
+    ("nvfp4_decode", [(0, 0), (31, 7), (9, 3), (17, 5), (25, 1), (4, 6)]),
 ])
 def test_full_size_sampled(name, samples):
     spec = wl.WORKLOADS[name]
@@ -150,3 +151,13 @@ def test_verify_bad_page_flagged_and_scored_minus_inf():
     # the other requests are exact
     ref = run_oracle(w.to("cpu"), tokens=list(range(0, 8)) + list(range(12, 16)))
     compare(w, sa, ref, tokens=list(range(0, 8)) + list(range(12, 16)))
+
+
+@pytest.mark.parametrize("q_len", [1, 4])
+def test_nvfp4_group_16_index_64_and_verify_every_element(q_len):
+    """NVFP4 slots with 16 query heads per KV head, index dim 64, and four
+    speculative tokens per request (ragged, straddling a block boundary)."""
+    spec = wl.small("nvfp4_decode", num_q_heads=32, num_kv_heads=2, index_dim=64, q_len=q_len,
+                    seq_lens=(700, 127 + q_len, 2900), seq_len_range=None, batch=3,
+                    num_pages=64, seed=1300 + q_len)
+    _full_case(spec)

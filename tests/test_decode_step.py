@@ -20,7 +20,8 @@ def _separate(cfg, w):
 
 
 @pytest.mark.parametrize("name,kw", [("medium_decode", {}), ("verify", {}),
-                                     ("fp8_decode", {}), ("long_decode", {}),
+                                     ("fp8_decode", {}), ("nvfp4_decode", {}),
+                                     ("long_decode", {}),
                                      ("medium_decode", dict(index_dim=64, topk_blocks=0)),
                                      ("medium_decode", dict(seq_lens=(1, 128, 129, 3000, 0),
                                                             seq_len_range=None, batch=5))])

@@ -109,7 +109,7 @@ def test_page_permutation_invariance_on_gpu():
     assert torch.equal(a.out, b.out) and torch.equal(a.lse, b.lse)
 
 
-@pytest.mark.parametrize("name", ["medium_decode", "fp8_decode", "verify"])
+@pytest.mark.parametrize("name", ["medium_decode", "fp8_decode", "nvfp4_decode", "verify"])
 def test_graph_replay_equals_eager(name):
     """The pages report the prior SM100 MSA decode returning wrong results under
     CUDA-graph capture/replay (sglang MiniMaxSparseAttnBackend.__init__); here the

@@ -36,7 +36,8 @@ def _close(a_out, a_lse, b_out, b_lse):
     assert torch.equal(a_lse, b_lse)
 
 
-@pytest.mark.parametrize("first,second", [("medium_decode", "fp8_decode")])
+@pytest.mark.parametrize("first,second", [("medium_decode", "fp8_decode"),
+                                          ("nvfp4_decode", "medium_decode")])
 def test_noalloc_matches_workspace_path_two_calls(first, second):
     for name in (first, second):
         spec = wl.small(name, batch=4)
