@@ -33,10 +33,11 @@
 //  * NVFP4 slots (vLLM MiniMaxM3SparseMSANvfp4Backend: each KV head's keys and
 //    values are two slots of packed FP4 data plus block scales) arrive as 1-D
 //    bulk copies of 9 KiB per (page, head, K|V) -- 72-byte rows are not a TMA
-//    tile shape -- and are dequantised the same way: a thread's four K values
-//    of a k-step are two bytes of E2M1 codes in one 16-element scale block, so
-//    K = e2m1 x e4m3 is formed in registers (exact in fp16: at most 6
-//    significant bits, magnitudes 2^-10 .. 2688) and V rows likewise.
+//    tile shape -- and are dequantised the same way, with another permutation
+//    of the head dimension: a thread's eight K values of a pair of k-steps are
+//    one 32-bit word of E2M1 codes inside one 16-element scale block, so K =
+//    e2m1 x e4m3 is formed in registers (exact in fp16: at most 6 significant
+//    bits, magnitudes 2^-10 .. 2688) and V rows likewise.
 // msa_combine then merges the splits in a fixed order (deterministic).
 #include <cuda.h>
 
@@ -160,13 +161,14 @@ __device__ __forceinline__ void convert_v_rows(const uint8_t* tile, uint8_t* con
   }
 }
 
-// Two FP4 E2M1 codes (one byte, the even element in the low nibble) -> f16x2.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t h;
-  asm("{\n .reg .b8 b;\n cvt.u8.u32 b, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}"
-      : "=r"(h)
-      : "r"(byte));
-  return h;
+// Eight FP4 E2M1 codes (four bytes, the even element in each low nibble) ->
+// four f16x2, byte i -> h[i].
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
 }
 
 // An E4M3 block-scale byte -> f16x2 holding it twice.
@@ -195,10 +197,13 @@ __device__ __forceinline__ void convert_v_rows_fp4(const uint8_t* tile, uint8_t*
       const uint8_t* rp = tile + row * kFp4Row;
       const uint2 w = *reinterpret_cast<const uint2*>(rp + 8 * c);
       const uint32_t sc = e4m3_scale_f16x2(rp[kHeadDim / 2 + c]);
+      uint32_t lo[4], hi[4];
+      e2m1x8_to_f16x2(w.x, lo);
+      e2m1x8_to_f16x2(w.y, hi);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        o[e] = hmul2_u32(e2m1x2_to_f16x2((w.x >> (8 * e)) & 0xffu), sc);
-        o[4 + e] = hmul2_u32(e2m1x2_to_f16x2((w.y >> (8 * e)) & 0xffu), sc);
+        o[e] = hmul2_u32(lo[e], sc);
+        o[4 + e] = hmul2_u32(hi[e], sc);
       }
     }
     *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -252,6 +257,8 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
     // header), so CTAs that drew cheap items take more of them.
     int islot = 0;
     uint32_t iphase = 0;
+    int nph[kItems] = {0, 0};       // phases armed on item_full[s]
+    int qlast[kItems] = {-1, -1};   // phase of the last Q copy on item_full[s]
     auto grab = [&]() {
       int i = 0;
       if (lane == 0) i = atomicAdd(&ws.hdr->work_next, 1);
@@ -281,6 +288,7 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
         bulk_load(qbuf + islot * qbytes,
                   a.q + ((int64_t)it.t * a.Hq + (int64_t)it.h * a.G) * kHeadDim, qbytes,
                   &item_full[islot]);
+        qlast[islot] = nph[islot]++;
       }
       if (++islot == kItems) { islot = 0; iphase ^= 1u; }
     }
@@ -288,6 +296,12 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
       mbar_wait(&item_empty[islot], iphase ^ 1u, ws.hdr);
       meta[islot].t = -1;
       mbar_arrive(&item_full[islot]);
+      ++nph[islot];
+      if (*reinterpret_cast<volatile int*>(&ws.hdr->err) & MSA_DEVERR_TIMEOUT) {
+        // a wait gave up: let this warp's Q copies land before the CTA retires
+        for (int s2 = 0; s2 < kItems; ++s2)
+          if (qlast[s2] >= 0) mbar_drain(&item_full[s2], (uint32_t)(qlast[s2] & 1));
+      }
       // the last CTA to stop taking items resets the counters for the next
       // launch on this workspace
       if (atomicAdd(&ws.hdr->work_done, 1) == (int)gridDim.x - 1) {
@@ -304,6 +318,7 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
     if (lane == 0) {
       int stage = 0, islot = 0;
       uint32_t phase = 0, iphase = 0;
+      int nload = 0;                 // stage arms (one K or V tile each)
       for (;;) {
         mbar_wait(&item_full[islot], iphase, ws.hdr);
         if (meta[islot].t < 0) break;
@@ -324,15 +339,20 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
               tma_load_2d(dst, tm, 0, y, &full_bar[stage]);
               if (KV == kKvBf16) tma_load_2d(dst + TB / 2, tm, 64, y, &full_bar[stage]);
             }
+            ++nload;
             if (++stage == NST) { stage = 0; phase ^= 1u; }
           }
         }
         mbar_arrive(&item_empty[islot]);
         if (++islot == kItems) { islot = 0; iphase ^= 1u; }
       }
+      // Normally the consumers wait for every tile issued here, so no copy is
+      // in flight when the CTA retires.  After a wait gave up they may not
+      // have: wait (bounded) for the last phase armed on each stage.
+      if (*reinterpret_cast<volatile int*>(&ws.hdr->err) & MSA_DEVERR_TIMEOUT)
+        for (int s2 = 0; s2 < NST && s2 < nload; ++s2)
+          mbar_drain(&full_bar[s2], (uint32_t)(((nload - 1 - s2) / NST) & 1));
     }
-    // No drain needed: the consumers wait for every tile issued here before
-    // they finish, so no copy is in flight when the CTA retires.
     return;
   }
 
@@ -354,6 +374,7 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
     // thread's four K values of a k-step are one 32-bit shared load
     // (d = 16ks + 4tq + {0,1 | 2,3}).
     uint32_t qa[8][4];
+    bool q_ovf = false;             // a query beyond the fp16 range (fp16 operands)
     {
       const __nv_bfloat16* qb =
           reinterpret_cast<const __nv_bfloat16*>(qbuf + islot * a.G * kHeadDim * 2);
@@ -365,10 +386,18 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
           const __nv_bfloat16* qr = qb + row * kHeadDim;
           if (row >= a.G) {
             qa[ks][hr] = qa[ks][hr + 2] = 0u;
+          } else if (KV == kKvFp4) {
+            // k-steps 2m, 2m + 1: d = 32 m + 8 tq + 4 (ks & 1) + {0,1 | 2,3}
+            const uint2 w =
+                *reinterpret_cast<const uint2*>(qr + 32 * (ks >> 1) + 8 * tq + 4 * (ks & 1));
+            qa[ks][hr] = bf16x2_to_f16x2(w.x);
+            qa[ks][hr + 2] = bf16x2_to_f16x2(w.y);
+            q_ovf |= f16x2_has_inf(qa[ks][hr]) | f16x2_has_inf(qa[ks][hr + 2]);
           } else if (F16) {
             const uint2 w = *reinterpret_cast<const uint2*>(qr + ks * 16 + 4 * tq);
             qa[ks][hr] = bf16x2_to_f16x2(w.x);
             qa[ks][hr + 2] = bf16x2_to_f16x2(w.y);
+            q_ovf |= f16x2_has_inf(qa[ks][hr]) | f16x2_has_inf(qa[ks][hr + 2]);
           } else {
             qa[ks][hr] = *reinterpret_cast<const uint32_t*>(qr + ks * 16 + 2 * tq);
             qa[ks][hr + 2] = *reinterpret_cast<const uint32_t*>(qr + ks * 16 + 8 + 2 * tq);
@@ -376,6 +405,7 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
         }
       }
     }
+    if (F16 && __any_sync(0xffffffffu, q_ovf) && lane == 0) set_error(ws.hdr, MSA_DEVERR_FP16_RANGE);
     __syncwarp();
     if (lane == 0) mbar_arrive(&item_empty[islot]);       // Q and metadata are in registers
     if (++islot == kItems) { islot = 0; iphase ^= 1u; }
@@ -395,15 +425,24 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
       for (int nt = 0; nt < 4; ++nt) {
         sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
         if (KV == kKvFp4) {
-          // d = 16 ks + 4 tq + {0,1 | 2,3}: two bytes of codes in scale block ks
+          // k-steps 2m, 2m + 1 of this thread: d = 32 m + 8 tq + 0..7, one word
+          // of codes inside scale block 2m + tq / 2
           const uint8_t* rp = kt + (warp * 32 + nt * 8 + g) * kFp4Row;
           const uint2 sb = *reinterpret_cast<const uint2*>(rp + kHeadDim / 2);
+          const uint32_t s01 = e4m3x2_to_f16x2((uint16_t)(sb.x & 0xffffu));
+          const uint32_t s23 = e4m3x2_to_f16x2((uint16_t)(sb.x >> 16));
+          const uint32_t s45 = e4m3x2_to_f16x2((uint16_t)(sb.y & 0xffffu));
+          const uint32_t s67 = e4m3x2_to_f16x2((uint16_t)(sb.y >> 16));
+          const uint32_t sel = (tq >> 1) ? 0x3232u : 0x1010u;   // this thread's half, twice
+          const uint32_t spair[4] = {s01, s23, s45, s67};
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t w = *reinterpret_cast<const uint16_t*>(rp + 8 * ks + 2 * tq);
-            const uint32_t sc2 = e4m3_scale_f16x2(((ks < 4 ? sb.x : sb.y) >> (8 * (ks & 3))) & 0xffu);
-            mma_f16(sc[nt], qa[ks], hmul2_u32(e2m1x2_to_f16x2(w & 0xffu), sc2),
-                    hmul2_u32(e2m1x2_to_f16x2(w >> 8), sc2));
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(rp + 16 * m + 4 * tq);
+            const uint32_t sc2 = __byte_perm(spair[m], 0u, sel);
+            uint32_t h[4];
+            e2m1x8_to_f16x2(w, h);
+            mma_f16(sc[nt], qa[2 * m], hmul2_u32(h[0], sc2), hmul2_u32(h[1], sc2));
+            mma_f16(sc[nt], qa[2 * m + 1], hmul2_u32(h[2], sc2), hmul2_u32(h[3], sc2));
           }
         } else if (F16) {
           const int row = warp * 32 + nt * 8 + g;

@@ -49,8 +49,10 @@ __device__ __forceinline__ float dot8(const float (&q)[8], const uint4& w) {
   return s;
 }
 
-// DIDX: index dim (64 | 128).  QL: query tokens per request scored together
-// (1 = decode, up to 4 = speculative verify); they share every key load.
+// DIDX: index dim (64 | 128).  QL: query tokens per request scored together,
+// sharing every key load (instantiated for decode, QL = 1; speculative verify
+// runs on the tensor-core kernel, whose tile stream does not depend on the
+// q_len x d / 8 registers the queries take here).
 template <int DIDX, int QL>
 __global__ void __launch_bounds__(kThreads, QL == 1 ? 5 : 2)
 index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
@@ -186,20 +188,12 @@ msa_status launch(const msa_config& c, const WsView& v, const void* idx_q, const
                     (const uint4*)idx_q, (const uint4*)idx_k, scores);
 }
 
+// One new token per request (decode); several (verify) go to the tensor-core
+// kernel of index_score_tc.cu.
 msa_status dispatch(const msa_config& c, const WsView& v, const void* idx_q, const void* idx_k,
                     float* scores, cudaStream_t s) {
-  const bool d128 = c.index_dim == 128;
-  switch (c.q_len) {
-    case 1: return d128 ? launch<128, 1>(c, v, idx_q, idx_k, scores, s)
-                        : launch<64, 1>(c, v, idx_q, idx_k, scores, s);
-    case 2: return d128 ? launch<128, 2>(c, v, idx_q, idx_k, scores, s)
-                        : launch<64, 2>(c, v, idx_q, idx_k, scores, s);
-    case 3: return d128 ? launch<128, 3>(c, v, idx_q, idx_k, scores, s)
-                        : launch<64, 3>(c, v, idx_q, idx_k, scores, s);
-    case 4: return d128 ? launch<128, 4>(c, v, idx_q, idx_k, scores, s)
-                        : launch<64, 4>(c, v, idx_q, idx_k, scores, s);
-    default: return MSA_ERR_UNSUPPORTED;
-  }
+  return c.index_dim == 128 ? launch<128, 1>(c, v, idx_q, idx_k, scores, s)
+                            : launch<64, 1>(c, v, idx_q, idx_k, scores, s);
 }
 
 }  // namespace

@@ -115,6 +115,11 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// True if either half of an f16x2 is infinite (a conversion overflowed).
+__device__ __forceinline__ bool f16x2_has_inf(uint32_t h) {
+  return (h & 0x7fffu) == 0x7c00u || ((h >> 16) & 0x7fffu) == 0x7c00u;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

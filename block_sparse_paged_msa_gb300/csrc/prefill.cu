@@ -271,8 +271,10 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   int kL0 = 0, kL1 = 0;                        // loader: Q tiles loaded per warpgroup
   int kW = 0;                                  // warpgroup: tiles done
   int cur_row = -1;
+  int n_kload = 0, n_vload = 0;                // issuer: K / V loads issued (drain on exit)
   // K / V tiles of CSR row rw: K into the K tile, V into V buffer `buf`
   auto load_k = [&](int rw) {
+    ++n_kload;
     const int jj = rw % a.NB, rr = (rw / a.NB) % a.B, hh = rw / (a.NB * a.B);
     const int pg = ws.block_table[(int64_t)rr * a.NB + jj];
     const int y = ((pg < 0 ? 0 : pg) * a.Hkv + hh) * kBlock;
@@ -282,6 +284,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     tma_load_2d_hint(Kt + kTileBytes / 2, &tmap_k, 64, y, &k_full, pol);
   };
   auto load_v = [&](int rw, int buf) {
+    ++n_vload;
     uint8_t* Vst = Vb(buf);
     const int jj = rw % a.NB, rr = (rw / a.NB) % a.B, hh = rw / (a.NB * a.B);
     const int pg = ws.block_table[(int64_t)rr * a.NB + jj];
@@ -331,6 +334,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
         // row, 128 bytes per row and 64-column half); keys past the last
         // visible token become 0, whatever the page holds there
         uint8_t* vb = Vb(vsel);
+        bool ovf = false;          // a value beyond the fp16 range
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int off = (tid + 256 * i) * 16;
@@ -343,9 +347,12 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
             x.y = bf16x2_to_f16x2(x.y);
             x.z = bf16x2_to_f16x2(x.z);
             x.w = bf16x2_to_f16x2(x.w);
+            ovf |= f16x2_has_inf(x.x) | f16x2_has_inf(x.y) | f16x2_has_inf(x.z) |
+                   f16x2_has_inf(x.w);
           }
           *reinterpret_cast<uint4*>(vb + off) = x;
         }
+        if (__any_sync(0xffffffffu, ovf) && lane == 0) set_error(ws.hdr, MSA_DEVERR_FP16_RANGE);
         fence_proxy_async_smem();
       }
       // V (fp16) is ready for the PV MMAs; the issuer has meanwhile started
@@ -677,16 +684,23 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   }
   if (warp < 8) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   // Every MMA and copy has been waited for on the normal path.  After a wait
-  // timed out some may still run: the issuer waits for its MMAs (bounded, no
-  // early exit), and every thread gives in-flight TMA loads ~100 us to land,
-  // before the TMEM is freed and the shared memory released.
+  // timed out some may still run: the issuer waits for its MMAs, and the
+  // threads that issued TMA loads wait for the last phase they armed on each
+  // barrier of those loads (bounded, no early exit), before the TMEM is freed
+  // and the shared memory released.
   if (issuer && lane == 0) {
     umma_commit(&k_free);
-    for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&k_free, kf_phase); ++i) {
-    }
+    mbar_drain(&k_free, kf_phase);
   }
   if (*reinterpret_cast<volatile int*>(&ws.hdr->err) & MSA_DEVERR_TIMEOUT) {
-    for (int i = 0; i < 1000; ++i) __nanosleep(100);
+    if (issuer && lane == 0) {
+      if (n_kload > 0) mbar_drain(&k_full, (uint32_t)((n_kload - 1) & 1));
+      if (n_vload > 0) mbar_drain(&v_full, (uint32_t)((n_vload - 1) & 1));
+    }
+    if (loader && lw == 0 && lane == 0 && G >= 8) {   // the Q boxes (G < 8 copies completed)
+      if (kL0 > 0) mbar_drain(&q_full[0], (uint32_t)((kL0 - 1) & 1));
+      if (kL1 > 0) mbar_drain(&q_full[1], (uint32_t)((kL1 - 1) & 1));
+    }
   }
   tc_fence_before();
   __syncthreads();

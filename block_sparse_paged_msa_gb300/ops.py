@@ -22,7 +22,7 @@ KV_DTYPES = {"bf16": MSA_KV_BF16, "fp8_e4m3": MSA_KV_FP8_E4M3, "nvfp4": MSA_KV_N
 MSA_MODE_DECODE, MSA_MODE_PREFILL = 0, 1
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED",
           3: "MSA_ERR_CUDA", 4: "MSA_ERR_DEVICE_FLAG"}
-DEVERR_BITS = {1: "PAGE_RANGE", 2: "SEQ_LEN", 4: "SLOT_ALIGN", 8: "TIMEOUT"}
+DEVERR_BITS = {1: "PAGE_RANGE", 2: "SEQ_LEN", 4: "SLOT_ALIGN", 8: "TIMEOUT", 16: "FP16_RANGE"}
 
 
 class MsaError(RuntimeError):

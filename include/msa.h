@@ -98,7 +98,13 @@ enum {
   MSA_DEVERR_SEQ_LEN = 2,      /* seq_len > max_blocks_per_req*P, or < query count,
                                   or the step's tokens exceed max_q_tokens        */
   MSA_DEVERR_SLOT_ALIGN = 4,   /* req_to_token slot of a block not page-aligned   */
-  MSA_DEVERR_TIMEOUT = 8       /* a pipeline wait gave up (results invalid)       */
+  MSA_DEVERR_TIMEOUT = 8,      /* a pipeline wait gave up (results invalid)       */
+  MSA_DEVERR_FP16_RANGE = 16   /* a bf16 value beyond the fp16 range (|x| > 65504,
+                                  or infinite) met an fp16 operand: the queries
+                                  of the fp8 / NVFP4 decode, the values of the
+                                  prefill tiles (results involving it invalid).
+                                  Magnitudes below 2^-14 are not flagged; they
+                                  keep fp16's subnormal precision only.          */
 };
 
 /*

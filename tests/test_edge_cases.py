@@ -193,3 +193,27 @@ def test_binding_rejects_tensors_smaller_than_the_config():
         msa.plan(cfg, w.seq_lens, w.block_table, sa.ws[:256])
     torch.cuda.synchronize()
     assert bool((sa.out == 3).all())
+
+
+@pytest.mark.parametrize("name", ["fp8_decode", "nvfp4_decode", "prefill"])
+def test_fp16_range_is_flagged(name):
+    """The fp8 / NVFP4 decode convert the bf16 queries, and the prefill tiles
+    the bf16 values, to fp16 MMA operands: a value beyond fp16's range is
+    reported as MSA_DEVERR_FP16_RANGE (never a fault), and a clean step after
+    it reports nothing."""
+    spec = wl.small(name, batch=2) if name != "prefill" else wl.small(name)
+    w = wl.make_workload(spec, device="cuda")
+    sa = run_gpu(w)
+    assert msa.check_device_error(sa.ws) == 0
+    if name == "prefill":
+        # a value of a block every token selects (the init block of request 0)
+        w.v_pages[int(w.block_table[0, 0]), 0, 5, 7] = 1e6
+    else:
+        w.q[1, 3, 17] = -2e5
+    sa.run(w.seq_lens, w.block_table, w.idx_q, w.idx_k_pages, w.q, w.k_pages, w.v_pages,
+           cu_seqlens_q=w.cu_seqlens_q if sa.prefill else None)
+    assert msa.check_device_error(sa.ws) & 16
+    w2 = wl.make_workload(spec, device="cuda")
+    sa.run(w2.seq_lens, w2.block_table, w2.idx_q, w2.idx_k_pages, w2.q, w2.k_pages, w2.v_pages,
+           cu_seqlens_q=w2.cu_seqlens_q if sa.prefill else None)
+    assert msa.check_device_error(sa.ws) == 0
