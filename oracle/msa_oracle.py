@@ -41,7 +41,7 @@ __all__ = [
     "query_positions", "gather_sequence", "block_scores", "select_blocks",
     "attention", "combine", "sparse_attention", "build_k2q_csr", "e4m3_encode",
     "cache_slots", "cache_write", "e2m1_to_float", "nvfp4_dequant", "nvfp4_row_bytes",
-    "NVFP4_BLOCK",
+    "NVFP4_BLOCK", "compact_selection", "paged_attention",
 ]
 
 
@@ -342,6 +342,36 @@ def sparse_attention(*, seq_lens, q_lens, block_table, idx_q, idx_k_pages, q,
             out[t, h * G:(h + 1) * G] = o
             lse[t, h * G:(h + 1) * G] = ls
     return {"scores": scores, "selected": selected, "out": out, "lse": lse}
+
+
+# --------------------------------------------------------------------------
+# Dense-sparse decode (sglang MiniMaxSparseAttnBackend._dense_sparse_main_decode
+# and the SGLANG_OPT_USE_MINIMAX_DENSE_SPARSE_DECODE branch of forward_decode):
+# the selected blocks become a compacted page table and a dense paged decode
+# runs over it with real_seq_lens, max_seq_len = topk_blocks * block_size.
+# --------------------------------------------------------------------------
+def compact_selection(selected: Sequence[int], block_table_row: Sequence[int], position: int,
+                      block_size: int) -> Tuple[List[int], int]:
+    """Pages of the selected blocks in ascending block order, and the number of
+    keys of the compacted sequence: each block contributes its tokens at
+    positions <= ``position`` (every selected block is full except the query's
+    own, which is the last)."""
+    pages, n = [], 0
+    for j in sorted(selected):
+        pages.append(int(block_table_row[j]))
+        n += max(0, min(block_size, position + 1 - j * block_size))
+    return pages, n
+
+
+def paged_attention(q_rows: np.ndarray, k_pages: np.ndarray, v_pages: np.ndarray,
+                    pages: Sequence[int], seq_len: int, head: int, scale: float,
+                    block_size: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Dense paged decode: the sequence is the first ``seq_len`` rows of the
+    listed pages, in order (rows of page i at positions i*P .. i*P + P - 1);
+    every query row of ``q_rows`` attends to all of them (KV head ``head``)."""
+    k = gather_sequence(k_pages, pages, seq_len, block_size)[:, head, :]
+    v = gather_sequence(v_pages, pages, seq_len, block_size)[:, head, :]
+    return attention(q_rows, k, v, scale)
 
 
 # --------------------------------------------------------------------------

@@ -469,6 +469,37 @@ def test_nvfp4_path_uses_dequantised_values():
     assert kf.max() <= 6 * 1.0 * 0.75 and np.abs(vf).max() > 0
 
 
+# ---------------------------------------------------------------- dense-sparse decode
+def test_compact_selection_hand_computed():
+    bt = [40, 41, 42, 43, 44, 45, 46, 47]
+    pages, n = oracle.compact_selection([7, 0, 3], bt, 7 * 128 + 5, 128)
+    assert pages == [40, 43, 47] and n == 2 * 128 + 6
+    pages, n = oracle.compact_selection([0, 1], bt, 1 * 128 + 127, 128)
+    assert pages == [40, 41] and n == 256
+    assert oracle.compact_selection([], bt, 5, 128) == ([], 0)
+
+
+def test_dense_sparse_equals_sparse_attention():
+    """The compacted sequence holds exactly the selected blocks' visible keys,
+    in order, so the dense paged decode over it reproduces the sparse result
+    bit for bit (same rows, same order, same arithmetic)."""
+    spec = wl.small("verify", batch=2, seq_lens=(900, 1100), num_pages=24, num_q_heads=16,
+                    num_kv_heads=2)
+    w = wl.make_workload(spec)
+    res = run_oracle(w)
+    bt, q = to_np(w.block_table), to_np(w.q)
+    kp, vp = to_np(w.k_pages), to_np(w.v_pages)
+    toks = oracle.query_positions(to_np(w.seq_lens), to_np(w.q_lens))
+    G = spec.group
+    for t, (r, p) in enumerate(toks):
+        for h in range(spec.num_kv_heads):
+            pages, n = oracle.compact_selection(res["selected"][(t, h)], bt[r], p, 128)
+            o, l = oracle.paged_attention(q[t, h * G:(h + 1) * G], kp, vp, pages, n, h,
+                                          spec.softmax_scale, 128)
+            assert np.array_equal(o, res["out"][t, h * G:(h + 1) * G])
+            assert np.array_equal(l, res["lse"][t, h * G:(h + 1) * G])
+
+
 # ---------------------------------------------------------------- mutations
 def _mutants():
     """Plausible mistakes, each planted in a copy of one oracle function."""
@@ -530,7 +561,14 @@ def _mutants():
         rows[..., :D // 2] = (rows[..., :D // 2] >> 4) | ((rows[..., :D // 2] & 0xF) << 4)
         return real_nvfp4(rows, D)
 
-    return [("e2m1_to_float", e2m1_no_subnormal), ("nvfp4_dequant", nvfp4_nibbles_swapped),
+    real_compact = oracle.compact_selection
+
+    def compact_all_full(selected, bt_row, position, P):   # the partial last block counted full
+        pages, n = real_compact(selected, bt_row, position, P)
+        return pages, P * len(pages)
+
+    return [("compact_selection", compact_all_full),
+            ("e2m1_to_float", e2m1_no_subnormal), ("nvfp4_dequant", nvfp4_nibbles_swapped),
             ("e4m3_encode", encode_ties_away), ("cache_slots", slots_one_late),
             ("block_scores", scores_sum), ("block_scores", scores_no_causal),
             ("select_blocks", select_high_tie), ("select_blocks", select_local_off_by_one),
@@ -554,6 +592,7 @@ _PINS = [
     test_cache_write_places_rows_and_leaves_the_rest,
     test_e2m1_codes_are_the_published_value_set,
     test_nvfp4_row_hand_decoded,
+    test_compact_selection_hand_computed,
 ]
 
 
