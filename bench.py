@@ -341,12 +341,14 @@ def cpu_baseline(w: wl.Workload, budget_s: float = 10.0):
 
 # ----------------------------------------------------------------- our arm
 LAUNCHES_PER_CALL = {"plan": 1, "index_score": 1, "topk_select": 1, "build_k2q_csr": 7,
-                     "sparse_prefill": 1, "sparse_decode": 1, "combine": 1}
+                     "sparse_prefill": 1, "sparse_decode": 1, "combine": 1,
+                     "compact_selected": 1}
 
 
 def _step_calls(msa, sa, w):
-    """The step's calls, as msa_decode_step chains them (decode / verify) or
-    SparseAttention.run does (prefill)."""
+    """The step's calls, as msa_decode_step chains them (decode / verify),
+    SparseAttention.run does (prefill), or the dense-sparse form runs them
+    (compaction + dense paged decode in place of the sparse decode)."""
     c = sa.cfg
     cu = w.cu_seqlens_q if sa.prefill else None
     calls = [
@@ -361,6 +363,13 @@ def _step_calls(msa, sa, w):
                                                             sa.q_indices)),
             ("sparse_prefill", lambda: msa.ops.sparse_prefill(
                 c, sa.ws, w.q, w.k_pages, w.v_pages, sa.selected, sa.row_ptr, sa.q_indices)),
+        ]
+    elif sa.dense_sparse:
+        calls += [
+            ("compact_selected", lambda: msa.compact_selected(c, sa.ws, sa.selected, sa.page_table,
+                                                              sa.dense_len)),
+            ("sparse_decode", lambda: msa.paged_decode(c, sa.ws, w.q, w.k_pages, w.v_pages,
+                                                       sa.page_table, sa.dense_len)),
         ]
     else:
         calls += [("sparse_decode", lambda: msa.sparse_decode(c, sa.ws, w.q, w.k_pages,
@@ -481,14 +490,15 @@ def _cache_write_cost(msa, sa, w, spec, stream, n):
                     f"from a CUDA graph of {n} launches"}
 
 
-def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False):
+def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False, dense_sparse=False):
     """Times `steps` steps of one workload after `warmup` untimed ones, the
     dominant kernel bracketed by CUDA events in the timed region, then a
-    per-kernel breakdown from further steps.  Returns the bench fields."""
+    per-kernel breakdown from further steps.  Returns the bench fields.
+    dense_sparse: the decode runs as compaction + dense paged decode."""
     import block_sparse_paged_msa_gb300 as msa
     w = wl.make_workload(spec, device=dev)
     cfg = msa.config_for(spec)
-    sa = msa.SparseAttention(cfg, device=dev)
+    sa = msa.SparseAttention(cfg, device=dev, dense_sparse=dense_sparse)
     stream = torch.cuda.current_stream()
     calls = _step_calls(msa, sa, w)
     names = [n for n, _ in calls]
@@ -558,7 +568,9 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False):
                    "head_dim": spec.head_dim, "index_dim": spec.index_dim,
                    "block": spec.block_size, "init_local_topk": [spec.init_blocks,
                    cfg.local_blocks, spec.topk_blocks],
-                   "pool_pages": spec.num_pages, "parallelism": f"replicas{world}"},
+                   "pool_pages": spec.num_pages, "parallelism": f"replicas{world}",
+                   "decode_form": ("dense_sparse (compacted pages + dense paged decode)"
+                                   if dense_sparse else "sparse (selected lists)")},
         "kernels_ms": per_kernel,
         "kernels_ms_note": ("dominant kernel timed in the timed region; the others in "
                             f"{Kb} further steps with every call bracketed by events"),
@@ -613,9 +625,12 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False):
 
 # The other configurations the default run measures beside the headline, with
 # their timed / warm-up steps (each a few dozen milliseconds of GPU time; most
-# of their cost is drawing the inputs, 90 GB for the long decode).
+# of their cost is drawing the inputs, 90 GB for the long decode).  A name
+# "<workload>:dense_sparse" runs that workload's decode in the dense-sparse
+# form (the A/B of the two decode formulations).
 OTHER_WORKLOADS = {"prefill": (40, 5), "fp8_decode": (200, 10), "nvfp4_decode": (200, 10),
-                   "verify": (100, 5), "long_decode": (40, 5)}
+                   "verify": (100, 5), "long_decode": (40, 5),
+                   "medium_decode:dense_sparse": (200, 10)}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -636,14 +651,19 @@ def run_ours(args, rank, world, local_rank):
                    "data": "synthetic (seeded; integer-valued bf16 index vectors, N(0,1) bf16 "
                            "q/k/v)"})
     others = [n for n in args.others.split(",") if n and n != "none" and n != spec.name]
+    bad = [n for n in others if n.partition(":")[0] not in wl.WORKLOADS]
+    if bad:
+        raise SystemExit(f"unknown workloads {bad}")
     if others:
         # the headline's inputs are kept (the CPU baseline samples them)
         torch.cuda.empty_cache()
         result["workloads"] = {}
         for name in others:
             K, W = OTHER_WORKLOADS.get(name, (40, 5))
-            o = wl.WORKLOADS[name]
-            r, wo = measure(o.replace(seed=o.seed + rank), K, W, dev, world, clock_gpu)
+            base_name, _, form = name.partition(":")
+            o = wl.WORKLOADS[base_name]
+            r, wo = measure(o.replace(seed=o.seed + rank), K, W, dev, world, clock_gpu,
+                            dense_sparse=form == "dense_sparse")
             keep = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "dtype",
                     "roofline", "kernels_ms", "kernel_gbs", "kernel_tflops", "step_hbm",
                     "clocks", "gpu_launches", "config", "cache_write")

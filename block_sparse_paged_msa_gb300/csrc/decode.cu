@@ -90,12 +90,20 @@ struct DecodeArgs {
   const int32_t* selected;
   const uint8_t* k_pool;   // NVFP4: the pools, read with bulk copies (no tensor map)
   const uint8_t* v_pool;
+  // dense paged decode (msa_paged_decode): per (token, KV head) a list of S
+  // pages and the number of keys laid out over them; null for the sparse form
+  const int32_t* page_table;
+  const int32_t* dense_len;
+  int num_pages;
 };
 
 // The blocks of work item (t, h, split s), as a lane-distributed list: lane i
 // (< bps) holds slot s*bps + i; `mask` has a bit for every usable slot (a valid,
 // visible block whose page passed the plan's check).  Producer and consumers
-// derive it identically.
+// derive it identically.  Sparse form: slot i is selected block j, read through
+// the plan's validated block table, with the keys at or before the token's
+// position.  Dense form: slot i is page_table[t, h, i], holding keys i*P ..
+// of a sequence of dense_len[t, h] keys (pages outside the pool are flagged).
 struct ItemBlocks {
   unsigned mask;
   int page, ntok;     // this lane's slot
@@ -108,13 +116,29 @@ __device__ __forceinline__ ItemBlocks item_blocks(const WsView& ws, const Decode
   const int nslot = min(a.bps, a.S - slot0);
   b.page = -1;
   b.ntok = 0;
+  bool bad = false;
   if (lane < nslot) {
-    const int j = a.selected[((int64_t)t * a.Hkv + h) * a.S + slot0 + lane];
-    if (j >= 0 && j * kBlock <= pos) {
-      b.page = ws.block_table[(int64_t)r * a.max_blocks + j];
-      b.ntok = min(kBlock, pos + 1 - j * kBlock);
+    const int64_t row = (int64_t)t * a.Hkv + h;
+    if (a.page_table != nullptr) {
+      const int n = a.dense_len[row] - (slot0 + lane) * kBlock;
+      if (n > 0) {
+        const int pg = a.page_table[row * a.S + slot0 + lane];
+        if (pg >= 0 && pg < a.num_pages) {
+          b.page = pg;
+          b.ntok = min(kBlock, n);
+        } else {
+          bad = true;
+        }
+      }
+    } else {
+      const int j = a.selected[row * a.S + slot0 + lane];
+      if (j >= 0 && j * kBlock <= pos) {
+        b.page = ws.block_table[(int64_t)r * a.max_blocks + j];
+        b.ntok = min(kBlock, pos + 1 - j * kBlock);
+      }
     }
   }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(ws.hdr, MSA_DEVERR_PAGE_RANGE);
   b.mask = __ballot_sync(0xffffffffu, b.page >= 0);
   return b;
 }
@@ -820,13 +844,19 @@ msa_status launch_decode(const WsView& v, const DecodeArgs& a, const CUtensorMap
 
 using namespace msa;
 
-extern "C" msa_status msa_sparse_decode(const msa_config* cfg, void* ws, const void* q,
-                                        const void* k_pages, const void* v_pages,
-                                        const int32_t* selected, msa_stream_t stream) {
+namespace msa {
+namespace {
+// The decode pipeline for either form: `selected` (sparse) or `page_table` +
+// `dense_len` (dense paged decode over compacted pages).
+msa_status decode_common(const msa_config* cfg, void* ws, const void* q, const void* k_pages,
+                         const void* v_pages, const int32_t* selected,
+                         const int32_t* page_table, const int32_t* dense_len,
+                         cudaStream_t s) {
   msa_status st = check_config(cfg);
   if (st != MSA_OK) return st;
   if (is_prefill(*cfg)) return MSA_ERR_INVALID_ARG;   // prefill uses msa_sparse_prefill
-  if (!ws || !q || !k_pages || !v_pages || !selected) return MSA_ERR_INVALID_ARG;
+  if (!ws || !q || !k_pages || !v_pages || (!selected && !(page_table && dense_len)))
+    return MSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages)) return MSA_ERR_INVALID_ARG;
   DecodeArgs a;
   a.Hkv = cfg->num_kv_heads;
@@ -848,8 +878,10 @@ extern "C" msa_status msa_sparse_decode(const msa_config* cfg, void* ws, const v
   a.selected = selected;
   a.k_pool = (const uint8_t*)k_pages;
   a.v_pool = (const uint8_t*)v_pages;
+  a.page_table = page_table;
+  a.dense_len = dense_len;
+  a.num_pages = cfg->num_pages;
   const WsView v = view_of(*cfg, ws);
-  cudaStream_t s = (cudaStream_t)stream;
   CUtensorMap tk, tv;
   if (cfg->kv_dtype == MSA_KV_NVFP4) {
     memset(&tk, 0, sizeof(tk));      // bulk copies from the pool pointers instead
@@ -862,6 +894,25 @@ extern "C" msa_status msa_sparse_decode(const msa_config* cfg, void* ws, const v
   if (!make_pool_map(&tk, k_pages, rows, fp8) || !make_pool_map(&tv, v_pages, rows, fp8))
     return MSA_ERR_CUDA;
   return fp8 ? launch_decode<kKvFp8>(v, a, tk, tv, s) : launch_decode<kKvBf16>(v, a, tk, tv, s);
+}
+}  // namespace
+}  // namespace msa
+
+extern "C" msa_status msa_sparse_decode(const msa_config* cfg, void* ws, const void* q,
+                                        const void* k_pages, const void* v_pages,
+                                        const int32_t* selected, msa_stream_t stream) {
+  if (selected == nullptr) return MSA_ERR_INVALID_ARG;
+  return decode_common(cfg, ws, q, k_pages, v_pages, selected, nullptr, nullptr,
+                       (cudaStream_t)stream);
+}
+
+extern "C" msa_status msa_paged_decode(const msa_config* cfg, void* ws, const void* q,
+                                       const void* k_pages, const void* v_pages,
+                                       const int32_t* page_table, const int32_t* seq_lens,
+                                       msa_stream_t stream) {
+  if (page_table == nullptr || seq_lens == nullptr) return MSA_ERR_INVALID_ARG;
+  return decode_common(cfg, ws, q, k_pages, v_pages, nullptr, page_table, seq_lens,
+                       (cudaStream_t)stream);
 }
 
 namespace msa {

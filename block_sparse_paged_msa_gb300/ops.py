@@ -69,6 +69,8 @@ _SIGNATURES = {
     "msa_topk_select": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "msa_sparse_decode": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "msa_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
+    "msa_compact_selected": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
+    "msa_paged_decode": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P]),
     "msa_check_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "msa_selftest_wait_timeout": (ctypes.c_int, [_CFG, _P, _P]),
     "msa_sparse_decode_noalloc": (ctypes.c_int, [_CFG, ctypes.c_int32, _P, _P, ctypes.c_int32,
@@ -394,6 +396,34 @@ def sparse_decode(cfg, ws, q, k_pages, v_pages, selected, stream=None):
         _stream(stream)))
 
 
+def compact_selected(cfg, ws, selected, page_table, dense_len, stream=None):
+    """Dense-sparse decode, step 1: the selected blocks of every (token, KV
+    head) as a compacted page list [T, H_kv, S] and its key count [T, H_kv]
+    (msa_compact_selected)."""
+    _need_ws(cfg, ws)
+    T = max_tokens(cfg)
+    _need_tokens(cfg, T, selected=selected)
+    _need(page_table, "page_table", torch.int32, 3, T, (cfg.num_kv_heads, _sizes(cfg)[1]))
+    _need(dense_len, "dense_len", torch.int32, 2, T, (cfg.num_kv_heads,))
+    _check("msa_compact_selected", lib().msa_compact_selected(
+        ctypes.byref(cfg), _ptr(ws), _ptr(selected), _ptr(page_table), _ptr(dense_len),
+        _stream(stream)))
+
+
+def paged_decode(cfg, ws, q, k_pages, v_pages, page_table, dense_len, stream=None):
+    """Dense-sparse decode, step 2: a dense paged decode over per-(token, KV
+    head) page lists and key counts (msa_paged_decode); combine() finishes."""
+    _need_ws(cfg, ws)
+    T = max_tokens(cfg)
+    _need_tokens(cfg, T, q=q)
+    _need_pools(cfg, k_pages, v_pages)
+    _need(page_table, "page_table", torch.int32, 3, T, (cfg.num_kv_heads, _sizes(cfg)[1]))
+    _need(dense_len, "dense_len", torch.int32, 2, T, (cfg.num_kv_heads,))
+    _check("msa_paged_decode", lib().msa_paged_decode(
+        ctypes.byref(cfg), _ptr(ws), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+        _ptr(dense_len), _stream(stream)))
+
+
 def combine(cfg, ws, out, lse, stream=None):
     _need_ws(cfg, ws)
     _need_tokens(cfg, max_tokens(cfg), out=out, lse=lse)
@@ -452,8 +482,12 @@ class SparseAttention:
     """Owns the buffers of one configuration and runs the whole path:
     plan -> index score -> top-k select -> sparse decode -> combine."""
 
-    def __init__(self, cfg: MsaConfig, device="cuda"):
+    def __init__(self, cfg: MsaConfig, device="cuda", dense_sparse: bool = False):
+        """dense_sparse: decode through the compacted page table and the dense
+        paged decode (msa_compact_selected + msa_paged_decode) instead of the
+        sparse decode over the selected lists."""
         self.cfg = cfg
+        self.dense_sparse = dense_sparse
         _check("msa_validate_config", validate_config(cfg))
         T = cfg.max_q_tokens or cfg.max_batch * cfg.q_len
         self.max_tokens = T
@@ -467,6 +501,12 @@ class SparseAttention:
                                device=device)
         self.lse = torch.empty((T, cfg.num_q_heads), dtype=torch.float32, device=device)
         self.prefill = cfg.mode == MSA_MODE_PREFILL
+        if dense_sparse:
+            if self.prefill:
+                raise ValueError("the dense-sparse form is a decode form")
+            self.page_table = torch.empty((T, cfg.num_kv_heads, self.width), dtype=torch.int32,
+                                          device=device)
+            self.dense_len = torch.empty((T, cfg.num_kv_heads), dtype=torch.int32, device=device)
         if self.prefill:
             self.row_ptr = torch.empty(k2q_rows(cfg) + 1, dtype=torch.int32, device=device)
             self.q_indices = torch.empty(k2q_capacity(cfg), dtype=torch.int32, device=device)
@@ -479,7 +519,7 @@ class SparseAttention:
         idx_k) first stores the step's new rows into the pools (cache_write,
         right after the plan; slots from out_cache_loc or from the plan)."""
         c = self.cfg
-        if not self.prefill and cu_seqlens_q is None and new_kv is None:
+        if not self.prefill and cu_seqlens_q is None and new_kv is None and not self.dense_sparse:
             decode_step(c, self.ws, seq_lens, block_table, idx_q, idx_k_pages, q, k_pages,
                         v_pages, self.block_scores, self.selected, self.out, self.lse, stream)
             return self.out, self.lse
@@ -493,6 +533,9 @@ class SparseAttention:
             build_k2q_csr(c, self.ws, self.selected, self.row_ptr, self.q_indices, stream)
             sparse_prefill(c, self.ws, q, k_pages, v_pages, self.selected, self.row_ptr,
                            self.q_indices, stream)
+        elif self.dense_sparse:
+            compact_selected(c, self.ws, self.selected, self.page_table, self.dense_len, stream)
+            paged_decode(c, self.ws, q, k_pages, v_pages, self.page_table, self.dense_len, stream)
         else:
             sparse_decode(c, self.ws, q, k_pages, v_pages, self.selected, stream)
         combine(c, self.ws, self.out, self.lse, stream)

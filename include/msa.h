@@ -275,6 +275,35 @@ msa_status msa_sparse_decode(const msa_config* cfg, void* ws, const void* q,
                              const int32_t* selected, msa_stream_t stream);
 
 /*
+ * Dense-sparse decode (sglang MiniMaxSparseAttnBackend.forward_decode with
+ * use_dense_sparse_decode, _dense_sparse_main_decode: the selected blocks
+ * become a page table and a real sequence length per query, and a dense paged
+ * decode runs over them with max_seq_len = topk_blocks * block_size).  The
+ * pages do it for one KV head; here the lists are per (token, KV head).
+ *
+ * msa_compact_selected -- after msa_topk_select (decode mode): for every token
+ * t and KV head h, page_table[t, h, 0..S) = the pages of selected[t, h, :]'s
+ * blocks in ascending block order (blocks whose page the plan flagged are left
+ * out), -1 after them, and seq_lens[t, h] = the number of keys they hold for
+ * the token (every block full but the token's own, which is last).
+ *   page_table [T, H_kv, S] int32;  seq_lens [T, H_kv] int32
+ *
+ * msa_paged_decode -- a dense paged decode over such lists (from
+ * msa_compact_selected or built by the caller): for each token t and KV head
+ * h, every query head of h's group attends to the first seq_lens[t, h] keys of
+ * the pages page_table[t, h, 0..), page i holding keys i*P .. i*P + P - 1.
+ * Split-K partials go to ws as for msa_sparse_decode; msa_combine finishes.
+ * A listed page outside [0, num_pages) within the length is skipped and sets
+ * MSA_DEVERR_PAGE_RANGE.  Run after msa_plan (it takes the step's tokens from
+ * the plan).  Keys beyond S * P are not read.  All KV dtypes.
+ */
+msa_status msa_compact_selected(const msa_config* cfg, const void* ws, const int32_t* selected,
+                                int32_t* page_table, int32_t* seq_lens, msa_stream_t stream);
+msa_status msa_paged_decode(const msa_config* cfg, void* ws, const void* q, const void* k_pages,
+                            const void* v_pages, const int32_t* page_table,
+                            const int32_t* seq_lens, msa_stream_t stream);
+
+/*
  * msa_combine -- log-sum-exp merge of the split-K partials in ws
  * (FlashMLA decode in sglang flashmla_backend.py returns (o, lse) per split
  * plan): lse = ln sum_s exp(lse_s), out = sum_s exp(lse_s - lse) o_s, out
