@@ -13,7 +13,8 @@
 //
 // Design: byte movement only.  One warp per (token, KV head): lanes 0-15 carry
 // the K row and lanes 16-31 the V row (16 bytes of bf16 each), then the index
-// key row; bf16 pools take the bytes as they are, e4m3 pools store
+// key row and the index-value row; bf16 pools take the bytes as they are, e4m3
+// pools store
 // round-to-nearest-even(x / scale) codes, saturated to +-448 (NaN stays NaN),
 // computed with one IEEE fp32 division and the hardware conversion.  A slot
 // outside the pool is skipped and flagged (MSA_DEVERR_PAGE_RANGE), never
@@ -46,8 +47,9 @@ __global__ void __launch_bounds__(kWarps * 32)
 cache_write_kernel(WsView ws, int Hkv, int max_blocks, int64_t pool_slots, int idx_lanes,
                    bool fp8, float k_scale, float v_scale, const int64_t* __restrict__ loc,
                    const uint4* __restrict__ k, const uint4* __restrict__ v,
-                   const uint4* __restrict__ idx_k, uint8_t* __restrict__ k_pages,
-                   uint8_t* __restrict__ v_pages, uint4* __restrict__ idx_pages) {
+                   const uint4* __restrict__ idx_k, const uint4* __restrict__ idx_v,
+                   uint8_t* __restrict__ k_pages, uint8_t* __restrict__ v_pages,
+                   uint4* __restrict__ idx_pages, uint4* __restrict__ idx_v_pages) {
   const int lane = threadIdx.x & 31;
   const int64_t item = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);   // (token, head)
   griddep_launch_dependents();
@@ -83,6 +85,8 @@ cache_write_kernel(WsView ws, int Hkv, int max_blocks, int64_t pool_slots, int i
   }
   if (idx_k != nullptr && lane < idx_lanes)
     idx_pages[row * idx_lanes + lane] = ld_nc(idx_k + item * idx_lanes + lane);
+  if (idx_v != nullptr && lane < idx_lanes)
+    idx_v_pages[row * idx_lanes + lane] = ld_nc(idx_v + item * idx_lanes + lane);
 }
 
 }  // namespace
@@ -92,15 +96,18 @@ using namespace msa;
 
 extern "C" msa_status msa_cache_write(const msa_config* cfg, void* ws,
                                       const int64_t* out_cache_loc, const void* k,
-                                      const void* v, const void* idx_k, void* k_pages,
-                                      void* v_pages, void* idx_k_pages, msa_stream_t stream) {
+                                      const void* v, const void* idx_k, const void* idx_v,
+                                      void* k_pages, void* v_pages, void* idx_k_pages,
+                                      void* idx_v_pages, msa_stream_t stream) {
   msa_status st = check_config(cfg);
   if (st != MSA_OK) return st;
   if (cfg->kv_dtype == MSA_KV_NVFP4) return MSA_ERR_UNSUPPORTED;   // no quantise-on-write form
-  if (!ws || !k || !v || !k_pages || !v_pages || (idx_k != nullptr && idx_k_pages == nullptr))
+  if (!ws || !k || !v || !k_pages || !v_pages || (idx_k != nullptr && idx_k_pages == nullptr) ||
+      (idx_v != nullptr && idx_v_pages == nullptr))
     return MSA_ERR_INVALID_ARG;
   if (!aligned16(k) || !aligned16(v) || !aligned16(k_pages) || !aligned16(v_pages) ||
-      (idx_k && (!aligned16(idx_k) || !aligned16(idx_k_pages))))
+      (idx_k && (!aligned16(idx_k) || !aligned16(idx_k_pages))) ||
+      (idx_v && (!aligned16(idx_v) || !aligned16(idx_v_pages))))
     return MSA_ERR_INVALID_ARG;
   const int64_t items = (int64_t)max_tokens_of(*cfg) * cfg->num_kv_heads;
   if (items <= 0) return MSA_OK;
@@ -112,6 +119,6 @@ extern "C" msa_status msa_cache_write(const msa_config* cfg, void* ws,
                     cfg->max_blocks_per_req, (int64_t)cfg->num_pages * kBlock,
                     cfg->index_dim / 8, fp8, fp8 ? cfg->k_scale : 1.f,
                     fp8 ? cfg->v_scale : 1.f, out_cache_loc, (const uint4*)k, (const uint4*)v,
-                    (const uint4*)idx_k, (uint8_t*)k_pages, (uint8_t*)v_pages,
-                    (uint4*)idx_k_pages);
+                    (const uint4*)idx_k, (const uint4*)idx_v, (uint8_t*)k_pages,
+                    (uint8_t*)v_pages, (uint4*)idx_k_pages, (uint4*)idx_v_pages);
 }

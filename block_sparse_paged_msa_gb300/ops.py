@@ -65,7 +65,9 @@ _SIGNATURES = {
     "msa_plan_from_req_to_token": (ctypes.c_int, [_CFG, ctypes.c_int32, _P, _P, _P,
                                                   ctypes.c_int32, _P, _P, _P]),
     "msa_index_score": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
-    "msa_cache_write": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "msa_cache_write": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "msa_index_attention_scratch_bytes": (ctypes.c_size_t, [_CFG]),
+    "msa_index_attention": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "msa_topk_select": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "msa_sparse_decode": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "msa_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
@@ -332,11 +334,13 @@ def plan_from_req_to_token(cfg, seq_lens, req_to_token, req_pool_indices, ws,
 
 
 def cache_write(cfg, ws, k, v, idx_k, k_pages, v_pages, idx_k_pages, out_cache_loc=None,
-                stream=None):
-    """Store the step's new K / V / index-K rows ([T, H_kv, D | d] bf16) into
-    the pools, after plan() and before index_score() (msa_cache_write).
-    out_cache_loc: [T] int64 slots (page * 128 + row), or None to take each
-    token's slot from the plan's block table and position.  idx_k may be None."""
+                stream=None, idx_v=None, idx_v_pages=None):
+    """Store the step's new K / V / index-K (and index-V) rows ([T, H_kv, D | d]
+    bf16) into the pools, after plan() and before index_score()
+    (msa_cache_write).  out_cache_loc: [T] int64 slots (page * 128 + row), or
+    None to take each token's slot from the plan's block table and position.
+    idx_k may be None; idx_v (with idx_v_pages) only for layers with the
+    index-value branch."""
     _need_ws(cfg, ws)
     T = max_tokens(cfg)
     kv_shape = (cfg.num_kv_heads, cfg.head_dim)
@@ -347,9 +351,43 @@ def cache_write(cfg, ws, k, v, idx_k, k_pages, v_pages, idx_k_pages, out_cache_l
     _need_pools(cfg, k_pages, v_pages, idx_k_pages)
     if out_cache_loc is not None:
         _need(out_cache_loc, "out_cache_loc", torch.int64, 1, T)
+    if idx_v is not None:
+        _need(idx_v, "idx_v", torch.bfloat16, 3, T, (cfg.num_kv_heads, cfg.index_dim))
+        _need(idx_v_pages, "idx_v_pages", torch.bfloat16, 4, cfg.num_pages,
+              (cfg.num_kv_heads, cfg.block_size, cfg.index_dim))
     _check("msa_cache_write", lib().msa_cache_write(
         ctypes.byref(cfg), _ptr(ws), _ptr(out_cache_loc), _ptr(k), _ptr(v), _ptr(idx_k),
-        _ptr(k_pages), _ptr(v_pages), _ptr(idx_k_pages), _stream(stream)))
+        _ptr(idx_v), _ptr(k_pages), _ptr(v_pages), _ptr(idx_k_pages), _ptr(idx_v_pages),
+        _stream(stream)))
+
+
+def index_attention_scratch_bytes(cfg) -> int:
+    return lib().msa_index_attention_scratch_bytes(ctypes.byref(cfg))
+
+
+def index_attention(cfg, ws, idx_q, idx_k_pages, idx_v_pages, scratch, idx_out, idx_lse=None,
+                    stream=None):
+    """The index-value branch's idx_o (msa_index_attention): dense causal
+    attention of the index head over every visible token (this library's
+    reading; the pages name idx_o without its formula).  idx_out [T, H_kv, d]
+    bf16, idx_lse [T, H_kv] float or None; scratch of
+    index_attention_scratch_bytes(cfg) bytes."""
+    _need_ws(cfg, ws)
+    T = max_tokens(cfg)
+    _need_tokens(cfg, T, idx_q=idx_q)
+    _need_pools(cfg, idx_k_pages=idx_k_pages)
+    _need(idx_v_pages, "idx_v_pages", torch.bfloat16, 4, cfg.num_pages,
+          (cfg.num_kv_heads, cfg.block_size, cfg.index_dim))
+    _need(scratch, "scratch", torch.uint8)
+    n = index_attention_scratch_bytes(cfg)
+    if n == 0 or scratch.numel() < n:
+        raise ValueError(f"scratch has {scratch.numel()} bytes, the config needs {n}")
+    _need(idx_out, "idx_out", torch.bfloat16, 3, T, (cfg.num_kv_heads, cfg.index_dim))
+    if idx_lse is not None:
+        _need(idx_lse, "idx_lse", torch.float32, 2, T, (cfg.num_kv_heads,))
+    _check("msa_index_attention", lib().msa_index_attention(
+        ctypes.byref(cfg), _ptr(ws), _ptr(idx_q), _ptr(idx_k_pages), _ptr(idx_v_pages),
+        _ptr(scratch), _ptr(idx_out), _ptr(idx_lse), _stream(stream)))
 
 
 def index_score(cfg, ws, idx_q, idx_k_pages, block_scores, stream=None):
@@ -525,7 +563,7 @@ class SparseAttention:
             return self.out, self.lse
         plan(c, seq_lens, block_table, self.ws, cu_seqlens_q, stream)
         if new_kv is not None:
-            cache_write(c, self.ws, *new_kv, k_pages, v_pages, idx_k_pages, out_cache_loc,
+            cache_write(c, self.ws, *new_kv[:3], k_pages, v_pages, idx_k_pages, out_cache_loc,
                         stream)
         index_score(c, self.ws, idx_q, idx_k_pages, self.block_scores, stream)
         topk_select(c, self.ws, self.block_scores, self.selected, stream)

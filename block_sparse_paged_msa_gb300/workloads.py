@@ -279,3 +279,19 @@ def new_token_rows(spec: WorkloadSpec, num_tokens: int, seed: int, device="cpu")
     idx_k = _randint_bf16((num_tokens, spec.num_kv_heads, spec.index_dim), spec.index_range,
                           gen, device)
     return k, v, idx_k
+
+
+def index_values(spec: WorkloadSpec, seed: int, device="cpu") -> torch.Tensor:
+    """An index-value pool beside the index keys, [num_pages, H_kv, P, d] bf16
+    N(0, 1), drawn from its own seed (the layers that keep an index-value
+    cache in the pages' backend)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    shape = (spec.num_pages, spec.num_kv_heads, spec.block_size, spec.index_dim)
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    flat = out.view(shape[0], -1)
+    for s in range(0, shape[0], 256):
+        e = min(shape[0], s + 256)
+        flat[s:e] = torch.randn((e - s, flat.shape[1]), generator=gen, device=device,
+                                dtype=torch.float32).to(torch.bfloat16)
+    return out

@@ -217,8 +217,10 @@ msa_status msa_plan_from_req_to_token(const msa_config* cfg, int32_t batch,
  *                  seq_len - n + i) goes to row pos % P of the page the block
  *                  table maps block pos / P to
  *   k, v           [T, H_kv, D] bf16;  idx_k [T, H_kv, d] bf16 or NULL (no
- *                  index-key write)
- *   k_pages, v_pages, idx_k_pages: the pools (layouts above)
+ *                  index-key write);  idx_v [T, H_kv, d] bf16 or NULL (no
+ *                  index-value write: layers without the index-value branch)
+ *   k_pages, v_pages, idx_k_pages: the pools (layouts above); idx_v_pages
+ *                  [num_pages, H_kv, P, d] bf16, the index-value pool
  * bf16 pools store the values as they are.  e4m3 pools store, per value, the
  * e4m3fn code nearest to x / scale (cfg->k_scale or v_scale; one IEEE fp32
  * division), ties to even, magnitudes beyond 448 saturated to +-448, NaN kept.
@@ -227,8 +229,31 @@ msa_status msa_plan_from_req_to_token(const msa_config* cfg, int32_t batch,
  * NVFP4 pools have no write form here (MSA_ERR_UNSUPPORTED).
  */
 msa_status msa_cache_write(const msa_config* cfg, void* ws, const int64_t* out_cache_loc,
-                           const void* k, const void* v, const void* idx_k, void* k_pages,
-                           void* v_pages, void* idx_k_pages, msa_stream_t stream);
+                           const void* k, const void* v, const void* idx_k, const void* idx_v,
+                           void* k_pages, void* v_pages, void* idx_k_pages, void* idx_v_pages,
+                           msa_stream_t stream);
+
+/*
+ * msa_index_attention -- the index-value branch's output (sglang
+ * MiniMaxSparseAttnBackend: layers outside disable_value_layer_ids keep an
+ * index-value cache, get_index_kv_buffer, and the sparse ops return (idx_o, o)
+ * with idx_o of shape [tokens, num_idx_heads * idx_head_dim]).  The pages do
+ * not give idx_o's formula; this library's reading (its parity is unpinned):
+ * the index head is a dense causal attention head,
+ *   idx_o[t, h] = sum_u softmax_u(idx_q[t,h] . idx_k[u,h] / sqrt(d)) idx_v[u,h]
+ * over the request's tokens u at positions <= position(t).  Decode mode, after
+ * msa_plan (and msa_cache_write) of the step.
+ *   idx_v_pages  [num_pages, H_kv, P, d] bf16
+ *   scratch      msa_index_attention_scratch_bytes(cfg) bytes, 256-byte aligned
+ *                (split partials; no initialisation needed)
+ *   idx_out      [T, H_kv, d] bf16;  idx_lse [T, H_kv] float (natural log) or NULL
+ * Idle tokens get idx_out = 0, idx_lse = -inf.  Blocks whose page the plan
+ * flagged are skipped.
+ */
+size_t msa_index_attention_scratch_bytes(const msa_config* cfg);
+msa_status msa_index_attention(const msa_config* cfg, const void* ws, const void* idx_q,
+                               const void* idx_k_pages, const void* idx_v_pages, void* scratch,
+                               void* idx_out, float* idx_lse, msa_stream_t stream);
 
 /*
  * msa_index_score -- block scores from the index query/key

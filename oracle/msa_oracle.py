@@ -27,7 +27,10 @@ sees tokens [0, p]; it has nb = floor(p / P) + 1 visible blocks.
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 against brute force, hand-computed selections, closed forms or an independent
-library routine; no function is "parity unpinned".
+library routine.  One READING is unpinned: ``index_attention`` (the
+index-value branch) computes the textbook attention it states, but the pages
+never say that idx_o is that attention -- its parity with the pages is
+"parity unpinned".
 """
 from __future__ import annotations
 
@@ -41,7 +44,7 @@ __all__ = [
     "query_positions", "gather_sequence", "block_scores", "select_blocks",
     "attention", "combine", "sparse_attention", "build_k2q_csr", "e4m3_encode",
     "cache_slots", "cache_write", "e2m1_to_float", "nvfp4_dequant", "nvfp4_row_bytes",
-    "NVFP4_BLOCK", "compact_selection", "paged_attention",
+    "NVFP4_BLOCK", "compact_selection", "paged_attention", "index_attention",
 ]
 
 
@@ -342,6 +345,26 @@ def sparse_attention(*, seq_lens, q_lens, block_table, idx_q, idx_k_pages, q,
             out[t, h * G:(h + 1) * G] = o
             lse[t, h * G:(h + 1) * G] = ls
     return {"scores": scores, "selected": selected, "out": out, "lse": lse}
+
+
+# --------------------------------------------------------------------------
+# Index-value branch (sglang MiniMaxSparseAttnBackend: layers outside
+# disable_value_layer_ids keep an index-value cache beside the index keys,
+# get_index_kv_buffer, and the sparse ops return (idx_o, o) with idx_o of shape
+# [tokens, num_idx_heads * idx_head_dim]).  The pages do not give idx_o's
+# formula.  PARITY UNPINNED: this reading -- the index head as a dense causal
+# attention head over every visible token, softmax scale 1 / sqrt(d) -- is
+# this build's, not the pages'.  The function itself is the textbook
+# `attention` over the gathered index keys and values.
+# --------------------------------------------------------------------------
+def index_attention(idx_q_vec: np.ndarray, idx_k_seq: np.ndarray, idx_v_seq: np.ndarray,
+                    position: int) -> Tuple[np.ndarray, float]:
+    """idx_o of one query token and index head: softmax(idx_q . idx_k[u] /
+    sqrt(d)) over the tokens u <= position, applied to idx_v[u]."""
+    d = idx_q_vec.shape[-1]
+    o, lse = attention(np.asarray(idx_q_vec, dtype=np.float64)[None],
+                       idx_k_seq[:position + 1], idx_v_seq[:position + 1], 1.0 / math.sqrt(d))
+    return o[0], float(lse[0])
 
 
 # --------------------------------------------------------------------------

@@ -500,6 +500,27 @@ def test_dense_sparse_equals_sparse_attention():
             assert np.array_equal(l, res["lse"][t, h * G:(h + 1) * G])
 
 
+# ---------------------------------------------------------------- index-value branch
+def test_index_attention_is_softmax_over_visible_tokens():
+    """The reading itself is unpinned (the pages give no formula for idx_o);
+    what is pinned is that the function computes what it states: scipy's
+    softmax of idx_q . idx_k / sqrt(d) over tokens <= position, applied to
+    idx_v, and a single visible token returns its own value row."""
+    rng = np.random.default_rng(4)
+    d, n = 64, 300
+    q = rng.integers(-4, 5, d).astype(np.float64)
+    k = rng.integers(-4, 5, (n, d)).astype(np.float64)
+    v = rng.standard_normal((n, d))
+    for pos in (0, 17, 299):
+        o, lse = oracle.index_attention(q, k, v, pos)
+        logits = k[:pos + 1] @ q / math.sqrt(d)
+        w = scipy.special.softmax(logits)
+        assert np.allclose(o, w @ v[:pos + 1], rtol=0, atol=1e-12)
+        assert abs(lse - scipy.special.logsumexp(logits)) < 1e-12
+    o, _ = oracle.index_attention(q, k, v, 0)
+    assert np.allclose(o, v[0], atol=1e-15)
+
+
 # ---------------------------------------------------------------- mutations
 def _mutants():
     """Plausible mistakes, each planted in a copy of one oracle function."""
