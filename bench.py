@@ -490,6 +490,42 @@ def _cache_write_cost(msa, sa, w, spec, stream, n):
                     f"from a CUDA graph of {n} launches"}
 
 
+def _index_attention_cost(msa, sa, w, spec, stream, n):
+    """The index-value branch (msa_index_attention) on the step's plan, timed
+    alone over n calls: a layer that keeps index values runs it beside the
+    step.  Algorithmic bytes: every visible index key and index value once per
+    token and KV head (the verify drafts each read their own), idx_q, idx_o."""
+    c = sa.cfg
+    if sa.prefill:
+        return None
+    idx_v = wl.index_values(spec, seed=spec.seed + 600, device=w.q.device)
+    scratch = torch.empty(msa.index_attention_scratch_bytes(c), dtype=torch.uint8,
+                          device=w.q.device)
+    T, H, d = msa.ops.max_tokens(c), spec.num_kv_heads, spec.index_dim
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=w.q.device)
+    lse = torch.empty((T, H), dtype=torch.float32, device=w.q.device)
+    msa.plan(c, w.seq_lens, w.block_table, sa.ws)
+    call = lambda: msa.index_attention(c, sa.ws, w.idx_q, w.idx_k_pages, idx_v,  # noqa: E731
+                                       scratch, out, lse)
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert msa.check_device_error(sa.ws) == 0
+    ms = e0.elapsed_time(e1) / n
+    q_lens = w.q_lens.long()
+    pos = (w.seq_lens.long().repeat_interleave(q_lens) - q_lens.repeat_interleave(q_lens)
+           + torch.cat([torch.arange(int(k), device=q_lens.device) for k in q_lens.tolist()]))
+    nbytes = int((pos + 1).sum()) * H * d * 2 * 2 + w.num_tokens * H * d * 4
+    return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
+            "note": "msa_index_attention (index-value branch; parity of its reading unpinned), "
+                    "timed alone, not in the timed step"}
+
+
 def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False, dense_sparse=False):
     """Times `steps` steps of one workload after `warmup` untimed ones, the
     dominant kernel bracketed by CUDA events in the timed region, then a
@@ -550,6 +586,7 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False, dense_sparse=
                   for i, n in enumerate(names)}
     e2e_res = _e2e(msa, sa, w, cfg, dev, stream, K, warmup, world) if e2e else None
     cw = _cache_write_cost(msa, sa, w, spec, stream, Kb)
+    ia = _index_attention_cost(msa, sa, w, spec, stream, min(Kb, 50)) if e2e else None
 
     T = w.num_tokens
     times = [ms, dom_ms] + ([e2e_res[1]] if e2e_res else [])
@@ -578,6 +615,8 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False, dense_sparse=
         "clocks": clk.summary(),
         "cache_write": cw,
     }
+    if ia is not None:
+        r["index_attention"] = ia
     if e2e_res is not None:
         Ke, e2e_ms, h2d, d2h = e2e_res
         r["e2e"] = {"value": replica_throughput(T, world, Ke, times[2]), "unit": UNIT,
