@@ -165,23 +165,37 @@ __device__ __forceinline__ Item item_of(const WsView& ws, const DecodeArgs& a, i
 // rows past the last visible token.
 __device__ __forceinline__ void convert_v_rows(const uint8_t* tile, uint8_t* conv, int warp,
                                                int ntok, int lane) {
+  // four inputs at a time ahead of their conversions (the staging stores
+  // could alias them for the compiler, which would otherwise chain each load
+  // behind the last store)
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int idx = k * 32 + lane;            // 32 rows x 8 chunks of 16 e4m3
-    const int rl = idx >> 3, c = idx & 7;
-    const int row = warp * 32 + rl;
-    uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    if (row < ntok) {
-      const uint4 w = *reinterpret_cast<const uint4*>(tile + swz128(row, c));
-      const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  for (int k0 = 0; k0 < 8; k0 += 4) {
+    uint4 win[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        o[2 * e] = e4m3x2_to_f16x2((uint16_t)(in[e] & 0xffffu));
-        o[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(in[e] >> 16));
-      }
+    for (int k = 0; k < 4; ++k) {
+      const int idx = (k0 + k) * 32 + lane;     // 32 rows x 8 chunks of 16 e4m3
+      const int row = warp * 32 + (idx >> 3);
+      win[k] = row < ntok ? *reinterpret_cast<const uint4*>(tile + swz128(row, idx & 7))
+                          : make_uint4(0u, 0u, 0u, 0u);
     }
-    *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = (k0 + k) * 32 + lane;
+      const int rl = idx >> 3, c = idx & 7;
+      const int row = warp * 32 + rl;
+      uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      if (row < ntok) {
+        const uint4 w = win[k];
+        const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          o[2 * e] = e4m3x2_to_f16x2((uint16_t)(in[e] & 0xffffu));
+          o[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(in[e] >> 16));
+        }
+      }
+      *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
   }
 }
 
@@ -211,27 +225,41 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
 // (256-byte swizzled rows), zeroing rows past the last visible token.
 __device__ __forceinline__ void convert_v_rows_fp4(const uint8_t* tile, uint8_t* conv, int warp,
                                                    int ntok, int lane) {
+  // four inputs (codes and scale bytes) at a time ahead of their conversions
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int idx = k * 32 + lane;            // 32 rows x 8 blocks of 16 elements
-    const int rl = idx >> 3, c = idx & 7;
-    const int row = warp * 32 + rl;
-    uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    if (row < ntok) {
+  for (int k0 = 0; k0 < 8; k0 += 4) {
+    uint2 win[4];
+    uint32_t sin[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = (k0 + k) * 32 + lane;     // 32 rows x 8 blocks of 16 elements
+      const int row = warp * 32 + (idx >> 3), c = idx & 7;
       const uint8_t* rp = tile + row * kFp4Row;
-      const uint2 w = *reinterpret_cast<const uint2*>(rp + 8 * c);
-      const uint32_t sc = e4m3_scale_f16x2(rp[kHeadDim / 2 + c]);
-      uint32_t lo[4], hi[4];
-      e2m1x8_to_f16x2(w.x, lo);
-      e2m1x8_to_f16x2(w.y, hi);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        o[e] = hmul2_u32(lo[e], sc);
-        o[4 + e] = hmul2_u32(hi[e], sc);
-      }
+      const bool vis = row < ntok;
+      win[k] = vis ? *reinterpret_cast<const uint2*>(rp + 8 * c) : make_uint2(0u, 0u);
+      sin[k] = vis ? rp[kHeadDim / 2 + c] : 0u;
     }
-    *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = (k0 + k) * 32 + lane;
+      const int rl = idx >> 3, c = idx & 7;
+      const int row = warp * 32 + rl;
+      uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      if (row < ntok) {
+        const uint2 w = win[k];
+        const uint32_t sc = e4m3_scale_f16x2(sin[k]);
+        uint32_t lo[4], hi[4];
+        e2m1x8_to_f16x2(w.x, lo);
+        e2m1x8_to_f16x2(w.y, hi);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          o[e] = hmul2_u32(lo[e], sc);
+          o[4 + e] = hmul2_u32(hi[e], sc);
+        }
+      }
+      *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(conv + swz(rl, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
   }
 }
 

@@ -26,7 +26,8 @@ namespace {
 
 constexpr int kIvWarps = 8;
 constexpr int kIvSplitsMax = 32;
-constexpr int kIvUnroll = 8;       // rows per group per chunk (16-byte loads in flight)
+constexpr int kIvUnroll = 8;       // rows per group per chunk: its key and value rows are
+                                   // requested together (16 16-byte loads in flight per lane)
 
 inline int iv_splits(const msa_config& c) {
   return c.max_blocks_per_req < kIvSplitsMax ? c.max_blocks_per_req : kIvSplitsMax;
@@ -80,12 +81,21 @@ index_attn_partial_kernel(WsView ws, int Hkv, int max_blocks, int NS, int bps, f
       const int64_t base = (((int64_t)page * Hkv + h) * kBlock * DIDX) / 8;
 #pragma unroll 1
       for (int rb = 0; rb < kBlock; rb += RPI * kIvUnroll) {
+        // the chunk's key and value rows in flight together (a value row past
+        // the token's position is read from the page but never used)
+        uint4 kr[kIvUnroll], vr[kIvUnroll];
+#pragma unroll
+        for (int u = 0; u < kIvUnroll; ++u) {
+          const int64_t at = base + (rb + u * RPI + grp) * LPR + sub;
+          kr[u] = ld_stream16(idx_k + at);
+          vr[u] = ld_stream16(idx_v + at);
+        }
         float sc[kIvUnroll];
 #pragma unroll
         for (int u = 0; u < kIvUnroll; ++u) {
           const int row = rb + u * RPI + grp;
           float k8[8];
-          unpack8(ld_stream16(idx_k + base + row * LPR + sub), k8);
+          unpack8(kr[u], k8);
           float x = q[0] * k8[0];
 #pragma unroll
           for (int i = 1; i < 8; ++i) x = fmaf(q[i], k8[i], x);
@@ -104,11 +114,10 @@ index_attn_partial_kernel(WsView ws, int Hkv, int max_blocks, int NS, int bps, f
         m = mn;
 #pragma unroll
         for (int u = 0; u < kIvUnroll; ++u) {
-          if (sc[u] == -INFINITY) continue;   // rows past the position: never read
-          const int row = rb + u * RPI + grp;
+          if (sc[u] == -INFINITY) continue;   // rows past the position: not used
           const float p = exp2f(sc[u] - mn);
           float v8[8];
-          unpack8(ld_stream16(idx_v + base + row * LPR + sub), v8);
+          unpack8(vr[u], v8);
           l += p;
 #pragma unroll
           for (int i = 0; i < 8; ++i) o[i] = fmaf(p, v8[i], o[i]);
