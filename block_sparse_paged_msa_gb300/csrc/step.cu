@@ -1,6 +1,7 @@
 // msa_decode_step: the whole decode / verify step in one call -- plan, index
-// scores, top-k selection, split-K sparse decode, combine -- as five kernels
-// chained with programmatic dependent launch.
+// scores with the top-k selection (one kernel when the scan can select as it
+// finishes each request, else two), split-K sparse decode, combine -- chained
+// with programmatic dependent launch.
 #include "msa_internal.cuh"
 
 extern "C" msa_status msa_decode_step(const msa_config* cfg, void* ws, int32_t batch,
@@ -18,9 +19,9 @@ extern "C" msa_status msa_decode_step(const msa_config* cfg, void* ws, int32_t b
     return MSA_ERR_INVALID_ARG;
   if ((st = msa_plan(cfg, batch, seq_lens, nullptr, block_table, bt_stride, ws, stream)) != MSA_OK)
     return st;
-  if ((st = msa_index_score(cfg, ws, idx_q, idx_k_pages, block_scores, stream)) != MSA_OK)
+  if ((st = msa_index_score_topk(cfg, ws, idx_q, idx_k_pages, block_scores, selected,
+                                 stream)) != MSA_OK)
     return st;
-  if ((st = msa_topk_select(cfg, ws, block_scores, selected, stream)) != MSA_OK) return st;
   if ((st = msa_sparse_decode(cfg, ws, q, k_pages, v_pages, selected, stream)) != MSA_OK)
     return st;
   return msa_combine(cfg, ws, out, lse, stream);

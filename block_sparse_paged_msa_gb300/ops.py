@@ -69,6 +69,8 @@ _SIGNATURES = {
     "msa_index_attention_scratch_bytes": (ctypes.c_size_t, [_CFG]),
     "msa_index_attention": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "msa_topk_select": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
+    "msa_index_score_topk": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
+    "msa_index_topk_fused": (ctypes.c_int32, [_CFG]),
     "msa_sparse_decode": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "msa_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "msa_compact_selected": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
@@ -418,6 +420,22 @@ def decode_step(cfg, ws, seq_lens, block_table, idx_q, idx_k_pages, q, k_pages, 
         _stream(stream)))
 
 
+def index_score_topk(cfg, ws, idx_q, idx_k_pages, block_scores, selected, stream=None):
+    """index_score + topk_select in one call (one kernel for decode with at most
+    256 blocks per request: msa_index_score_topk)."""
+    _need_ws(cfg, ws)
+    T = max_tokens(cfg)
+    _need_tokens(cfg, T, idx_q=idx_q, block_scores=block_scores, selected=selected)
+    _need_pools(cfg, idx_k_pages=idx_k_pages)
+    _check("msa_index_score_topk", lib().msa_index_score_topk(
+        ctypes.byref(cfg), _ptr(ws), _ptr(idx_q), _ptr(idx_k_pages), _ptr(block_scores),
+        _ptr(selected), _stream(stream)))
+
+
+def index_topk_fused(cfg) -> bool:
+    return bool(lib().msa_index_topk_fused(ctypes.byref(cfg)))
+
+
 def topk_select(cfg, ws, block_scores, selected, stream=None):
     _need_ws(cfg, ws)
     _need_tokens(cfg, max_tokens(cfg), block_scores=block_scores, selected=selected)
@@ -565,8 +583,7 @@ class SparseAttention:
         if new_kv is not None:
             cache_write(c, self.ws, *new_kv[:3], k_pages, v_pages, idx_k_pages, out_cache_loc,
                         stream)
-        index_score(c, self.ws, idx_q, idx_k_pages, self.block_scores, stream)
-        topk_select(c, self.ws, self.block_scores, self.selected, stream)
+        index_score_topk(c, self.ws, idx_q, idx_k_pages, self.block_scores, self.selected, stream)
         if self.prefill:
             build_k2q_csr(c, self.ws, self.selected, self.row_ptr, self.q_indices, stream)
             sparse_prefill(c, self.ws, q, k_pages, v_pages, self.selected, self.row_ptr,

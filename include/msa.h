@@ -274,6 +274,20 @@ msa_status msa_index_score(const msa_config* cfg, const void* ws, const void* id
                            msa_stream_t stream);
 
 /*
+ * msa_index_score_topk -- msa_index_score followed by msa_topk_select, with
+ * the same results.  For decode (q_len 1, max_blocks_per_req <= 256) one
+ * kernel does both: the warp that scores a request's last block for a KV head
+ * selects that row's blocks as it finishes (a counter per (request, KV head)
+ * in ws, reset by msa_plan), so the selection costs no launch of its own;
+ * otherwise the two kernels run one after the other.  msa_index_topk_fused
+ * says which (1 = one kernel).  ws is written (the counters).
+ */
+msa_status msa_index_score_topk(const msa_config* cfg, void* ws, const void* idx_q,
+                                const void* idx_k_pages, float* block_scores, int32_t* selected,
+                                msa_stream_t stream);
+int32_t msa_index_topk_fused(const msa_config* cfg);
+
+/*
  * msa_topk_select -- per (token, KV head): blocks [0, init) U [nb - local, nb)
  * U the topk best of the remaining blocks, ranked by score descending and block
  * index ascending on ties; written ascending into selected[t, h, 0..S), the
@@ -422,8 +436,8 @@ msa_status msa_noalloc_check_device_error(int32_t* flags, msa_stream_t stream);
 
 /*
  * msa_decode_step -- one decode / verify step (decode mode): msa_plan (with
- * cu_seqlens_q = NULL), msa_index_score, msa_topk_select, msa_sparse_decode,
- * msa_combine.
+ * cu_seqlens_q = NULL), msa_index_score_topk (msa_index_score +
+ * msa_topk_select), msa_sparse_decode, msa_combine.
  * Arguments as in those calls.  The kernels are chained with programmatic
  * dependent launch, so each one's launch overlaps the previous one's tail.
  */
