@@ -84,7 +84,6 @@ def test_index_score_topk_equals_two_calls(name, kw):
         msa.index_score_topk(cfg, b.ws, w.idx_q, w.idx_k_pages, b.block_scores, b.selected)
         torch.cuda.synchronize()
         assert torch.equal(a.selected[:T], b.selected[:T])
-        fin = torch.isfinite(a.block_scores[:T]) | torch.isinf(a.block_scores[:T])
         for t in range(T):
             pos = int(w.seq_lens[t // spec.q_len]) - spec.q_len + t % spec.q_len
             if pos < 0 or int(w.seq_lens[t // spec.q_len]) == 0:
