@@ -87,6 +87,8 @@ cache_write_kernel(WsView ws, int Hkv, int max_blocks, int64_t pool_slots, int i
     idx_pages[row * idx_lanes + lane] = ld_nc(idx_k + item * idx_lanes + lane);
   if (idx_v != nullptr && lane < idx_lanes)
     idx_v_pages[row * idx_lanes + lane] = ld_nc(idx_v + item * idx_lanes + lane);
+  // the step's later kernels read these rows with TMA (async proxy)
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 }  // namespace

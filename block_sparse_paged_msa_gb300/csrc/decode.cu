@@ -25,7 +25,11 @@
 //    and keeps its own online softmax (exp2 domain); the four states merge once
 //    per item and warp 0 writes the normalised partial and its LSE;
 //  * rows past the last visible token are masked in S and cleared in V before
-//    P V (whatever they hold, 0 * NaN would not vanish);
+//    P V (whatever they hold, 0 * NaN would not vanish): in the V fragments'
+//    registers for bf16 tiles, in the converted rows otherwise.  Nothing but
+//    the copy engine writes a stage: clearing rows there with ordinary stores
+//    gave, now and then, wrong values in another block's V tile of the same
+//    CTA, even with a proxy fence before the stage was released;
 //  * e4m3 tiles: K feeds an fp16 MMA straight from shared memory (the index
 //    dimension is permuted so a thread's four K values of a k-step are one
 //    32-bit load), V is converted to fp16 rows by its warp; e4m3 is exact in
@@ -583,21 +587,20 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
         vbase = smem_u32(my_conv);
         vrow0 = 0;
       } else {
-        if (ntok < warp * 32 + 32) {
-          // rows past the last visible token may hold anything; P is 0 there,
-          // but 0 * NaN is not, so clear this warp's rows of the tile
-          for (int i = lane; i < 32 * 16; i += 32) {
-            const int row = warp * 32 + (i >> 4);
-            if (row >= ntok) *reinterpret_cast<uint4*>(vt + swz_tma(row, i & 15)) = make_uint4(0u, 0u, 0u, 0u);
-          }
-          __syncwarp();
-        }
         vbase = smem_u32(vt);
         vrow0 = warp * 32;
       }
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         const int row = vrow0 + kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+        // bf16: rows past the last visible token may hold anything; P is 0
+        // there, but 0 * NaN is not.  The transposed fragments give this
+        // thread keys r, r + 1 (b0, b2) and r + 8, r + 9 (b1, b3), r = 16 kk +
+        // 2 tq of the warp's 32: mask those halves in registers (the stage
+        // itself is written only by the copy engine).
+        const int r = warp * 32 + kk * 16 + 2 * tq;
+        const uint32_t mlo = (r < ntok ? 0x0000ffffu : 0u) | (r + 1 < ntok ? 0xffff0000u : 0u);
+        const uint32_t mhi = (r + 8 < ntok ? 0x0000ffffu : 0u) | (r + 9 < ntok ? 0xffff0000u : 0u);
 #pragma unroll
         for (int nd = 0; nd < 16; nd += 2) {
           uint32_t b0, b1, b2, b3;
@@ -607,8 +610,8 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
             mma_f16(acc[nd + 1], pa[kk], b2, b3);
           } else {
             ldsm_x4_t(vbase + swz_tma(row, nd + (lane >> 4)), b0, b1, b2, b3);
-            mma_bf16(acc[nd], pa[kk], b0, b1);
-            mma_bf16(acc[nd + 1], pa[kk], b2, b3);
+            mma_bf16(acc[nd], pa[kk], b0 & mlo, b1 & mhi);
+            mma_bf16(acc[nd + 1], pa[kk], b2 & mlo, b3 & mhi);
           }
         }
       }

@@ -322,6 +322,14 @@ __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Order this thread's generic-proxy shared-memory accesses with later
+// async-proxy ones (tensor core operand reads, TMA reads and writes): needed
+// before a TMA copy may overwrite shared memory this thread wrote, and before
+// an MMA or a TMA store reads it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Named barrier over `count` threads (ids 1.. are free; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -38,11 +38,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// Make this thread's generic-proxy shared-memory writes visible to the async
-// proxy (tensor core operand reads, TMA).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 1024-byte
 // stride between 8-row groups; `saddr` is a shared-window byte address.
