@@ -346,23 +346,17 @@ LAUNCHES_PER_CALL = {"plan": 1, "index_score": 1, "topk_select": 1, "build_k2q_c
 
 
 def _step_calls(msa, sa, w):
-    """The step's calls, as msa_decode_step chains them (decode / verify: the
-    index scan selects as it goes when msa_index_topk_fused says so),
+    """The step's calls, as msa_decode_step chains them (decode / verify),
     SparseAttention.run does (prefill), or the dense-sparse form runs them
     (compaction + dense paged decode in place of the sparse decode)."""
     c = sa.cfg
     cu = w.cu_seqlens_q if sa.prefill else None
-    calls = [("plan", lambda: msa.plan(c, w.seq_lens, w.block_table, sa.ws, cu))]
-    if msa.ops.index_topk_fused(c):
-        # one kernel scores and, as each request's last block is scored, selects
-        calls += [("index_score", lambda: msa.index_score_topk(
-            c, sa.ws, w.idx_q, w.idx_k_pages, sa.block_scores, sa.selected))]
-    else:
-        calls += [
-            ("index_score", lambda: msa.index_score(c, sa.ws, w.idx_q, w.idx_k_pages,
-                                                    sa.block_scores)),
-            ("topk_select", lambda: msa.topk_select(c, sa.ws, sa.block_scores, sa.selected)),
-        ]
+    calls = [
+        ("plan", lambda: msa.plan(c, w.seq_lens, w.block_table, sa.ws, cu)),
+        ("index_score", lambda: msa.index_score(c, sa.ws, w.idx_q, w.idx_k_pages,
+                                                sa.block_scores)),
+        ("topk_select", lambda: msa.topk_select(c, sa.ws, sa.block_scores, sa.selected)),
+    ]
     if sa.prefill:
         calls += [
             ("build_k2q_csr", lambda: msa.ops.build_k2q_csr(c, sa.ws, sa.selected, sa.row_ptr,

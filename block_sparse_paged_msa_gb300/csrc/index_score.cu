@@ -21,7 +21,7 @@
 // not by requests.
 #include <mutex>
 
-#include "topk_warp.cuh"
+#include "msa_internal.cuh"
 
 namespace msa {
 namespace {
@@ -49,44 +49,15 @@ __device__ __forceinline__ float dot8(const float (&q)[8], const uint4& w) {
   return s;
 }
 
-// SEL: the warp that scores the last block of a request for a KV head also
-// selects that request's rows (its top-k, topk_warp.cuh), so the selection
-// needs no launch of its own: a counter per (request, KV head), zeroed by the
-// plan, counts the scored blocks; the scores are published with a fence
-// before the count and read back through L2.
-struct SelArgs {
-  int init, local, topk, S;
-  int* selected;
-};
-
-// After a warp scored block (r, ., h): count it, and if it was the request's
-// last one for head h, select the request's rows for h.
-__device__ __forceinline__ void select_if_last(const WsView& ws, int r, int h, int qs, int Hkv,
-                                               int max_blocks, int max_tokens,
-                                               const float* scores, const SelArgs& sel,
-                                               int* hist, int lane) {
-  int last = 0;
-  if (lane == 0) {
-    __threadfence();                    // this warp's scores before its count
-    last = atomicAdd(&ws.req_done[(int64_t)r * Hkv + h], 1) == ws.req_nb[r] - 1;
-  }
-  if (__shfl_sync(0xffffffffu, last, 0)) {
-    __threadfence();                    // every count (and score) before the reads
-    if (qs < max_tokens && ws.tok_req[qs] == r)
-      topk_row<8>(ws, (int64_t)qs * Hkv + h, Hkv, max_blocks, sel.init, sel.local, sel.topk,
-                  sel.S, scores, sel.selected, hist, lane);
-  }
-}
-
 // DIDX: index dim (64 | 128).  QL: query tokens per request scored together,
 // sharing every key load (instantiated for decode, QL = 1; speculative verify
 // runs on the tensor-core kernel, whose tile stream does not depend on the
 // q_len x d / 8 registers the queries take here).
-template <int DIDX, int QL, bool SEL>
+template <int DIDX, int QL>
 __global__ void __launch_bounds__(kThreads, QL == 1 ? 5 : 2)
 index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
                    const uint4* __restrict__ idx_q,
-                   const uint4* __restrict__ idx_k, float* __restrict__ scores, SelArgs sel) {
+                   const uint4* __restrict__ idx_k, float* __restrict__ scores) {
   constexpr int LPR = DIDX / 8;            // lanes per key row
   constexpr int RPI = 32 / LPR;            // rows per warp-wide load
   constexpr int ROWS = kUnroll * RPI;      // rows per batch
@@ -111,15 +82,6 @@ index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
   const int batch = ws.hdr->batch;
   const int total = ws.hdr->total_blocks * Hkv;
   const int warps = gridDim.x * (kThreads / 32);
-  __shared__ int whist[SEL ? kThreads / 32 : 1][SEL ? 256 : 1];
-  if (SEL) {
-    // tokens of no (valid) request have no blocks, hence no last block: their
-    // rows are written here
-    const int T = ws.hdr->num_tokens;
-    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < (int64_t)T * Hkv * sel.S;
-         i += (int64_t)gridDim.x * kThreads)
-      if (ws.tok_req[i / ((int64_t)Hkv * sel.S)] < 0) sel.selected[i] = -1;
-  }
   for (int item = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); item < total;
        item += warps) {
     const int h = item % Hkv;
@@ -139,8 +101,6 @@ index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
         for (int i = 0; i < QL; ++i)
           if (qs + i < max_tokens && ws.tok_req[qs + i] == r)
             out[(int64_t)i * Hkv * max_blocks] = -INFINITY;
-      if (SEL) select_if_last(ws, r, h, qs, Hkv, max_blocks, max_tokens, scores, sel,
-                              whist[SEL ? threadIdx.x >> 5 : 0], lane);
       continue;
     }
     float q[QL][8];
@@ -199,14 +159,12 @@ index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
         best[i] = fmaxf(best[i], __shfl_xor_sync(0xffffffffu, best[i], o));
       if (lane == 0 && lim[i] > 0) out[(int64_t)i * Hkv * max_blocks] = best[i];
     }
-    if (SEL) select_if_last(ws, r, h, qs, Hkv, max_blocks, max_tokens, scores, sel,
-                            whist[SEL ? threadIdx.x >> 5 : 0], lane);
   }
 }
 
-template <int DIDX, int QL, bool SEL>
+template <int DIDX, int QL>
 msa_status launch(const msa_config& c, const WsView& v, const void* idx_q, const void* idx_k,
-                  float* scores, cudaStream_t s, int* selected = nullptr) {
+                  float* scores, cudaStream_t s) {
   static std::mutex mu;
   static int occ[64] = {0};
   int dev = 0;
@@ -216,7 +174,7 @@ msa_status launch(const msa_config& c, const WsView& v, const void* idx_q, const
     std::lock_guard<std::mutex> lk(mu);
     if (occ[dev] == 0) {
       int n = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, index_score_kernel<DIDX, QL, SEL>,
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, index_score_kernel<DIDX, QL>,
                                                         kThreads, 0) != cudaSuccess)
         return MSA_ERR_CUDA;
       occ[dev] = n > 0 ? n : 1;
@@ -225,29 +183,17 @@ msa_status launch(const msa_config& c, const WsView& v, const void* idx_q, const
   }
   const int grid = sm_count() * blocks_per_sm;
   if (grid <= 0) return MSA_ERR_CUDA;
-  SelArgs sel;
-  sel.init = c.init_blocks;
-  sel.local = c.local_blocks;
-  sel.topk = c.topk_blocks;
-  sel.S = width_of(c);
-  sel.selected = selected;
-  return launch_pdl(index_score_kernel<DIDX, QL, SEL>, dim3(grid), dim3(kThreads), 0, s, v,
+  return launch_pdl(index_score_kernel<DIDX, QL>, dim3(grid), dim3(kThreads), 0, s, v,
                     c.num_kv_heads, c.max_blocks_per_req, max_tokens_of(c),
-                    (const uint4*)idx_q, (const uint4*)idx_k, scores, sel);
+                    (const uint4*)idx_q, (const uint4*)idx_k, scores);
 }
 
 // One new token per request (decode); several (verify) go to the tensor-core
 // kernel of index_score_tc.cu.
 msa_status dispatch(const msa_config& c, const WsView& v, const void* idx_q, const void* idx_k,
                     float* scores, cudaStream_t s) {
-  return c.index_dim == 128 ? launch<128, 1, false>(c, v, idx_q, idx_k, scores, s)
-                            : launch<64, 1, false>(c, v, idx_q, idx_k, scores, s);
-}
-
-// The scan selects as it goes for decode (one new token per request) when a
-// row's candidates fit the warp selection's 256-candidate form.
-bool fusable(const msa_config& c) {
-  return !is_prefill(c) && c.q_len == 1 && c.max_blocks_per_req <= 256;
+  return c.index_dim == 128 ? launch<128, 1>(c, v, idx_q, idx_k, scores, s)
+                            : launch<64, 1>(c, v, idx_q, idx_k, scores, s);
 }
 
 }  // namespace
@@ -271,25 +217,10 @@ extern "C" msa_status msa_index_score(const msa_config* cfg, const void* ws, con
   return dispatch(*cfg, v, idx_q, idx_k_pages, block_scores, s);
 }
 
-extern "C" int32_t msa_index_topk_fused(const msa_config* cfg) {
-  return check_config(cfg) == MSA_OK && fusable(*cfg) ? 1 : 0;
-}
-
 extern "C" msa_status msa_index_score_topk(const msa_config* cfg, void* ws, const void* idx_q,
                                            const void* idx_k_pages, float* block_scores,
                                            int32_t* selected, msa_stream_t stream) {
-  msa_status st = check_config(cfg);
-  if (st != MSA_OK) return st;
-  if (!ws || !idx_q || !idx_k_pages || !block_scores || !selected) return MSA_ERR_INVALID_ARG;
-  if (!aligned16(idx_q) || !aligned16(idx_k_pages)) return MSA_ERR_INVALID_ARG;
-  if (!fusable(*cfg)) {
-    if ((st = msa_index_score(cfg, ws, idx_q, idx_k_pages, block_scores, stream)) != MSA_OK)
-      return st;
-    return msa_topk_select(cfg, ws, block_scores, selected, stream);
-  }
-  const WsView v = view_of(*cfg, ws);
-  cudaStream_t s = (cudaStream_t)stream;
-  return cfg->index_dim == 128
-             ? launch<128, 1, true>(*cfg, v, idx_q, idx_k_pages, block_scores, s, selected)
-             : launch<64, 1, true>(*cfg, v, idx_q, idx_k_pages, block_scores, s, selected);
+  if (!selected) return MSA_ERR_INVALID_ARG;
+  const msa_status st = msa_index_score(cfg, ws, idx_q, idx_k_pages, block_scores, stream);
+  return st != MSA_OK ? st : msa_topk_select(cfg, ws, block_scores, selected, stream);
 }

@@ -82,8 +82,7 @@ inline int64_t prefill_items_bound(const msa_config& c) {
 
 // Byte offsets of every workspace region.
 struct WsLayout {
-  size_t plan_err, req_seq_len, req_nb, req_cu_nb, req_qstart, req_done, tok_req, tok_pos,
-      block_table;
+  size_t plan_err, req_seq_len, req_nb, req_cu_nb, req_qstart, tok_req, tok_pos, block_table;
   size_t sched, item_order, slot_entry, csr_bits, csr_wpre, o_part, lse_part, total;
 };
 
@@ -97,7 +96,6 @@ inline WsLayout layout_of(const msa_config& c) {
   L.req_nb = o;      o = align_up(o + 4 * B);
   L.req_cu_nb = o;   o = align_up(o + 4 * (B + 1));
   L.req_qstart = o;  o = align_up(o + 4 * (B + 1));
-  L.req_done = o;    o = align_up(o + 4 * B * (size_t)c.num_kv_heads);
   L.tok_req = o;     o = align_up(o + 4 * T);
   L.tok_pos = o;     o = align_up(o + 4 * T);
   L.block_table = o; o = align_up(o + 4 * B * (size_t)c.max_blocks_per_req);
@@ -120,8 +118,6 @@ struct WsView {
   int32_t* req_nb;
   int32_t* req_cu_nb;
   int32_t* req_qstart;
-  int32_t* req_done;      // [max_batch, H_kv] blocks scored per (request, KV head): the
-                          // index scan that also selects counts them (zeroed by the plan)
   int32_t* tok_req;
   int32_t* tok_pos;
   int32_t* block_table;   // [max_batch, max_blocks_per_req], -1 = invalid
@@ -150,7 +146,6 @@ inline WsView view_of(const msa_config& c, const void* ws) {
   v.req_nb = (int32_t*)(b + L.req_nb);
   v.req_cu_nb = (int32_t*)(b + L.req_cu_nb);
   v.req_qstart = (int32_t*)(b + L.req_qstart);
-  v.req_done = (int32_t*)(b + L.req_done);
   v.tok_req = (int32_t*)(b + L.tok_req);
   v.tok_pos = (int32_t*)(b + L.tok_pos);
   v.block_table = (int32_t*)(b + L.block_table);

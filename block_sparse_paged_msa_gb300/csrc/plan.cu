@@ -191,7 +191,6 @@ plan_kernel(WsView ws, int batch, int max_batch, int Hkv, int q_len, int max_blo
     }
     if (tid == 0 && request_flagged(r, seq_lens, cu_q, q_len, max_blocks, max_tokens))
       bad |= MSA_DEVERR_SEQ_LEN;
-    for (int h = tid; h < Hkv; h += blockDim.x) ws.req_done[(int64_t)r * Hkv + h] = 0;
     __shared__ int bad_s;
     if (tid == 0) bad_s = 0;
     __syncthreads();

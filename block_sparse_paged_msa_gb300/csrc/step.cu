@@ -1,7 +1,6 @@
 // msa_decode_step: the whole decode / verify step in one call -- plan, index
-// scores with the top-k selection (one kernel when the scan can select as it
-// finishes each request, else two), split-K sparse decode, combine -- chained
-// with programmatic dependent launch.
+// scores, top-k selection, split-K sparse decode, combine -- as five kernels
+// chained with programmatic dependent launch.
 #include "msa_internal.cuh"
 
 extern "C" msa_status msa_decode_step(const msa_config* cfg, void* ws, int32_t batch,

@@ -1,6 +1,5 @@
-// The warp-wide top-k selection of one (token, KV head) row, shared by
-// msa_topk_select (topk.cu) and the index scan that selects as it finishes a
-// request (index_score.cu).  Not part of the ABI.
+// The warp-wide top-k selection of one (token, KV head) row: msa_topk_select
+// (topk.cu) runs it for rows of up to 1 024 candidates.  Not part of the ABI.
 #pragma once
 
 #include "msa_internal.cuh"

@@ -70,7 +70,6 @@ _SIGNATURES = {
     "msa_index_attention": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "msa_topk_select": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "msa_index_score_topk": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
-    "msa_index_topk_fused": (ctypes.c_int32, [_CFG]),
     "msa_sparse_decode": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "msa_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "msa_compact_selected": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
@@ -421,8 +420,7 @@ def decode_step(cfg, ws, seq_lens, block_table, idx_q, idx_k_pages, q, k_pages, 
 
 
 def index_score_topk(cfg, ws, idx_q, idx_k_pages, block_scores, selected, stream=None):
-    """index_score + topk_select in one call (one kernel for decode with at most
-    256 blocks per request: msa_index_score_topk)."""
+    """index_score then topk_select in one call (msa_index_score_topk)."""
     _need_ws(cfg, ws)
     T = max_tokens(cfg)
     _need_tokens(cfg, T, idx_q=idx_q, block_scores=block_scores, selected=selected)
@@ -430,10 +428,6 @@ def index_score_topk(cfg, ws, idx_q, idx_k_pages, block_scores, selected, stream
     _check("msa_index_score_topk", lib().msa_index_score_topk(
         ctypes.byref(cfg), _ptr(ws), _ptr(idx_q), _ptr(idx_k_pages), _ptr(block_scores),
         _ptr(selected), _stream(stream)))
-
-
-def index_topk_fused(cfg) -> bool:
-    return bool(lib().msa_index_topk_fused(ctypes.byref(cfg)))
 
 
 def topk_select(cfg, ws, block_scores, selected, stream=None):

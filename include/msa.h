@@ -274,18 +274,17 @@ msa_status msa_index_score(const msa_config* cfg, const void* ws, const void* id
                            msa_stream_t stream);
 
 /*
- * msa_index_score_topk -- msa_index_score followed by msa_topk_select, with
- * the same results.  For decode (q_len 1, max_blocks_per_req <= 256) one
- * kernel does both: the warp that scores a request's last block for a KV head
- * selects that row's blocks as it finishes (a counter per (request, KV head)
- * in ws, reset by msa_plan), so the selection costs no launch of its own;
- * otherwise the two kernels run one after the other.  msa_index_topk_fused
- * says which (1 = one kernel).  ws is written (the counters).
+ * msa_index_score_topk -- msa_index_score then msa_topk_select on the same
+ * stream (the second launch overlaps the first one's tail), in one call.
+ * Arguments, results and errors as in those two calls.  (A scan that selects
+ * each request's rows as it finishes them, counting scored blocks per
+ * (request, KV head), measured slower on GB300 than the separate selection
+ * kernel: the per-block release of the counts and the selection tail at the
+ * end of the scan cost more than the launch they save.)
  */
 msa_status msa_index_score_topk(const msa_config* cfg, void* ws, const void* idx_q,
                                 const void* idx_k_pages, float* block_scores, int32_t* selected,
                                 msa_stream_t stream);
-int32_t msa_index_topk_fused(const msa_config* cfg);
 
 /*
  * msa_topk_select -- per (token, KV head): blocks [0, init) U [nb - local, nb)

@@ -149,6 +149,35 @@ def test_graph_replay_equals_eager(name):
         assert torch.equal(g_out[:T], eager.out[:T]) and torch.equal(g_lse[:T], eager.lse[:T])
 
 
+@pytest.mark.parametrize("name", ["medium_decode", "fp8_decode", "nvfp4_decode", "verify",
+                                  "verify:dense_sparse", "prefill"])
+def test_repeated_runs_bit_identical(name):
+    """The same step on the same inputs, 32 times in a row on one workspace:
+    every output and LSE must equal the first run's bit for bit.  The verify
+    case has several work items per decode CTA, so stage reuse across items
+    (and any write into a stage other than the copy engine's) is exercised;
+    a race there shows up as one split's partial differing now and then."""
+    name, _, form = name.partition(":")
+    base = wl.small(name)
+    w = wl.make_workload(base, device="cuda")
+    cfg = msa.config_for(base)
+    sa = msa.SparseAttention(cfg, dense_sparse=form == "dense_sparse")
+    T = w.num_tokens
+    args = (w.seq_lens, w.block_table, w.idx_q, w.idx_k_pages, w.q, w.k_pages, w.v_pages)
+    kw = {"cu_seqlens_q": w.cu_seqlens_q} if sa.prefill else {}
+    sa.run(*args, **kw)
+    torch.cuda.synchronize()
+    out0, lse0 = sa.out[:T].clone(), sa.lse[:T].clone()
+    differ = 0
+    for _ in range(32):
+        sa.out.zero_()
+        sa.run(*args, **kw)
+        torch.cuda.synchronize()
+        differ += int(not (torch.equal(sa.out[:T], out0) and torch.equal(sa.lse[:T], lse0)))
+    assert msa.check_device_error(sa.ws) == 0
+    assert differ == 0, f"{differ} of 32 repeated runs differ from the first"
+
+
 def test_bounded_wait_times_out_without_fault():
     # A wait on a barrier that nothing completes gives up after its limit and
     # reports MSA_DEVERR_TIMEOUT; the next plan clears the word and the same
