@@ -68,9 +68,10 @@ NCU_TRAFFIC_BYTES = {
     # batch-8 / 2048-page capture of the current kernel: 372.4 MB for 367.7 MB
     # algorithmic, scaled by bytes to a full medium-decode launch (1.2608 GB)
     ("medium_decode", "index_score"): 1.2769e9,
-    # full-size one-pass capture of the prefill tile kernel: 1 513.5 MB read
-    # (Q gathers, K/V tiles) + 2 670.4 MB written (the fp16 partials)
-    ("prefill", "sparse_prefill"): 4.1839e9,
+    # full-size one-pass capture of the prefill tile kernel (work items taken
+    # request by request): 690.4 MB read (Q gathers now mostly L2 hits, K/V
+    # tiles) + 2 667.3 MB written (the fp16 partials)
+    ("prefill", "sparse_prefill"): 3.3577e9,
 }
 
 

@@ -723,17 +723,20 @@ sched_count_kernel(const int32_t* __restrict__ row_ptr, int32_t* __restrict__ sc
   if (blockIdx.x == 0 && threadIdx.x == 0) sched[0] = 0;
 }
 
-// The work items ordered by their tile count, largest first (a counting sort
-// in one CTA), so that the CTAs' round-robin share of the items comes out even.
+// The work items request by request (requests ascending), largest first
+// within a request (a counting sort in one CTA per request in turn).  A
+// request's queries (tokens x H_q rows of 256 bytes, contiguous) are what the
+// tiles re-read once per selected block: taken a request at a time they stay
+// in L2, where all requests' together would not.  Largest first keeps the
+// CTAs' round-robin shares of each request even.
 __global__ void __launch_bounds__(1024)
 item_order_kernel(const int32_t* __restrict__ row_ptr, WsView ws, int64_t rows, int tok_per_item,
-                  int tpt) {
+                  int tpt, int B, int NB) {
   __shared__ int cnt[kTilesPerItem + 1], base[kTilesPerItem + 1];
+  __shared__ int run_s;
   griddep_launch_dependents();
   griddep_wait();
   const int tid = threadIdx.x;
-  if (tid <= kTilesPerItem) cnt[tid] = 0;
-  __syncthreads();
   auto items_of = [&](int64_t row, auto&& fn) {
     const int n = row_ptr[row + 1] - row_ptr[row];
     for (int k = 0; k * tok_per_item < n; ++k) {
@@ -741,23 +744,34 @@ item_order_kernel(const int32_t* __restrict__ row_ptr, WsView ws, int64_t rows, 
       fn(k, (m + tpt - 1) / tpt);
     }
   };
-  for (int64_t row = tid; row < rows; row += 1024)
-    items_of(row, [&](int, int sz) { atomicAdd(&cnt[sz], 1); });
-  __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int sz = kTilesPerItem; sz >= 0; --sz) {
-      base[sz] = run;
-      run += cnt[sz];
+  // rows (h, r, j) = (h * B + r) * NB + j; request r owns H_kv * NB of them
+  const int64_t per_req = rows / B;
+  auto row_of = [&](int r, int64_t i) { return ((i / NB) * B + r) * (int64_t)NB + i % NB; };
+  if (tid == 0) run_s = 0;
+  for (int r = 0; r < B; ++r) {
+    if (tid <= kTilesPerItem) cnt[tid] = 0;
+    __syncthreads();
+    for (int64_t i = tid; i < per_req; i += 1024)
+      items_of(row_of(r, i), [&](int, int sz) { atomicAdd(&cnt[sz], 1); });
+    __syncthreads();
+    if (tid == 0) {
+      int run = run_s;
+      for (int sz = kTilesPerItem; sz >= 0; --sz) {
+        base[sz] = run;
+        run += cnt[sz];
+      }
+      run_s = run;
     }
-  }
-  __syncthreads();
-  for (int64_t row = tid; row < rows; row += 1024) {
-    const int rb = row_ptr[row], re = row_ptr[row + 1];
-    items_of(row, [&](int k, int sz) {
-      const int b = rb + k * tok_per_item;
-      ws.item_order[atomicAdd(&base[sz], 1)] = make_int4((int)row, b, min(re, b + tok_per_item), 0);
-    });
+    __syncthreads();
+    for (int64_t i = tid; i < per_req; i += 1024) {
+      const int64_t row = row_of(r, i);
+      const int rb = row_ptr[row], re = row_ptr[row + 1];
+      items_of(row, [&](int k, int sz) {
+        const int b = rb + k * tok_per_item;
+        ws.item_order[atomicAdd(&base[sz], 1)] = make_int4((int)row, b, min(re, b + tok_per_item), 0);
+      });
+    }
+    __syncthreads();
   }
 }
 
@@ -827,7 +841,7 @@ extern "C" msa_status msa_build_k2q_csr(const msa_config* cfg, const void* ws,
   if ((st = launch_pdl(csr_scan_kernel, dim3(1), dim3(1024), 0, s, v.sched, rows)) != MSA_OK)
     return st;
   return launch_pdl(item_order_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)row_ptr, v, rows,
-                    tok_per_item, kBlock / G);
+                    tok_per_item, kBlock / G, B, NB);
 }
 
 extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const void* q,
