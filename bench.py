@@ -65,9 +65,10 @@ FALLBACK_HBM_GBS = 6800.0
 # kernel, from the ncu captures summarised in profiles/ (None until captured for
 # the current kernel).
 NCU_TRAFFIC_BYTES = {
-    # batch-8 / 2048-page capture of the current kernel: 372.4 MB for 367.7 MB
-    # algorithmic, scaled by bytes to a full medium-decode launch (1.2608 GB)
-    ("medium_decode", "index_score"): 1.2769e9,
+    # batch-8 / 2048-page capture of the current kernel (half-tile units):
+    # 371.6 MB (368.3 read + 3.4 written) for 367.7 MB algorithmic, scaled by
+    # bytes to a full medium-decode launch (1.2608 GB)
+    ("medium_decode", "index_score"): 1.2743e9,
     # full-size one-pass capture of the prefill tile kernel (work items taken
     # request by request): 690.4 MB read (Q gathers now mostly L2 hits, K/V
     # tiles) + 2 667.3 MB written (the fp16 partials)
@@ -346,6 +347,14 @@ LAUNCHES_PER_CALL = {"plan": 1, "index_score": 1, "topk_select": 1, "build_k2q_c
                      "compact_selected": 1}
 
 
+def launches_per_call(name, spec):
+    """Kernels one call launches: the decode index scan (one new token per
+    request) sets the scores to -inf first and then scans half tiles."""
+    if name == "index_score" and spec.q_len == 1:
+        return 2
+    return LAUNCHES_PER_CALL[name]
+
+
 def _step_calls(msa, sa, w):
     """The step's calls, as msa_decode_step chains them (decode / verify),
     SparseAttention.run does (prefill), or the dense-sparse form runs them
@@ -612,7 +621,7 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False, dense_sparse=
         "kernels_ms": per_kernel,
         "kernels_ms_note": ("dominant kernel timed in the timed region; the others in "
                             f"{Kb} further steps with every call bracketed by events"),
-        "gpu_launches": sum(LAUNCHES_PER_CALL[n] for n in names) * K,
+        "gpu_launches": sum(launches_per_call(n, spec) for n in names) * K,
         "clocks": clk.summary(),
         "cache_write": cw,
     }

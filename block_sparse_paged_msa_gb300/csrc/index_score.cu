@@ -10,8 +10,12 @@
 // Design (GB300): a pure HBM scan -- every visible index key is read once per
 // request (one 256-byte row per token and KV head at d = 128) against 128 FMAs,
 // about 0.5 FMA per byte, so CUDA cores are ample and the kernel is sized for
-// bytes in flight.  One warp owns one (block, KV head) tile of 128 rows, which
-// is contiguous in the HND page layout (32 KiB at d = 128).  Lanes own a fixed
+// bytes in flight.  One warp owns one half (64 rows) of a (block, KV head)
+// tile, which is contiguous in the HND page layout (16 KiB at d = 128); the two
+// halves' maxima meet in the score with an order-free atomic max over scores
+// set to -inf by a first small kernel (a whole tile per warp left a tail: a
+// warp took 6 or 7 tiles of ~26 us each, so the last third of them ran ~15 us
+// alone).  Lanes own a fixed
 // 16-byte slice of the index dimension, so the index query stays in registers;
 // each lane keeps 8 16-byte streaming loads in flight, and the partial dot
 // products of 8 rows are reduced across the row's lanes with a
@@ -19,6 +23,7 @@
 // The grid is persistent (SMs x resident CTAs) and walks the flattened
 // (request, block, head) list, so ragged sequence lengths balance by blocks,
 // not by requests.
+#include <algorithm>
 #include <mutex>
 
 #include "msa_internal.cuh"
@@ -28,6 +33,27 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 8;   // 16-byte loads in flight per lane
+constexpr int kParts = 2;    // work units per (block, KV head) tile: row ranges of kBlock / kParts
+
+// Max of a score slot and x, in any order of arrival: a non-negative float
+// orders like its int bits, a negative one reversely like its unsigned bits;
+// -0 is taken as +0.  The slot starts at -inf.  x is never NaN here (the
+// warp's own max ignores NaN rows; a part of only NaN rows is not written).
+__device__ __forceinline__ void atomic_max_score(float* slot, float x) {
+  x = x + 0.0f;
+  if (x >= 0.f) atomicMax(reinterpret_cast<int*>(slot), __float_as_int(x));
+  else atomicMin(reinterpret_cast<unsigned int*>(slot), __float_as_uint(x));
+}
+
+// Every score slot of the step's tokens to -inf (the parts meet by atomic max).
+__global__ void __launch_bounds__(256)
+score_init_kernel(WsView ws, int64_t row_slots, float* __restrict__ scores) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int64_t n = (int64_t)ws.hdr->num_tokens * row_slots;
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256)
+    scores[i] = -INFINITY;
+}
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
@@ -61,7 +87,7 @@ index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
   constexpr int LPR = DIDX / 8;            // lanes per key row
   constexpr int RPI = 32 / LPR;            // rows per warp-wide load
   constexpr int ROWS = kUnroll * RPI;      // rows per batch
-  static_assert(kBlock % ROWS == 0, "block must be a multiple of the batch");
+  static_assert((kBlock / kParts) % ROWS == 0, "a part must be a multiple of the batch");
   const int lane = threadIdx.x & 31;
   const int sub = lane % LPR, rsub = lane / LPR;
   // Row (within a batch) whose full dot product this lane holds after the
@@ -80,12 +106,14 @@ index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
   griddep_launch_dependents();
   griddep_wait();
   const int batch = ws.hdr->batch;
-  const int total = ws.hdr->total_blocks * Hkv;
+  const int total = ws.hdr->total_blocks * Hkv * kParts;
   const int warps = gridDim.x * (kThreads / 32);
   for (int item = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); item < total;
        item += warps) {
     const int h = item % Hkv;
-    const int b = item / Hkv;
+    const int part = (item / Hkv) % kParts;
+    const int b = item / (Hkv * kParts);
+    const int r0 = part * (kBlock / kParts);   // this unit's rows [r0, r0 + kBlock / kParts)
     int lo = 0, hi = batch - 1;  // request of flat block b
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -117,12 +145,16 @@ index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
       q[i][6] = bf16lo(w.w); q[i][7] = bf16hi(w.w);
       lim[i] = mine ? ws.tok_pos[qs + i] - j * kBlock + 1 : 0;  // visible rows
     }
+    bool any = false;                          // a visible row in this part
+#pragma unroll
+    for (int i = 0; i < QL; ++i) any |= lim[i] > r0;
+    if (!any) continue;
     const uint4* tile = idx_k + (((int64_t)page * Hkv + h) * kBlock * DIDX) / 8;
     float best[QL];
 #pragma unroll
     for (int i = 0; i < QL; ++i) best[i] = -INFINITY;
 #pragma unroll 1
-    for (int rb = 0; rb < kBlock; rb += ROWS) {
+    for (int rb = r0; rb < r0 + kBlock / kParts; rb += ROWS) {
       uint4 d[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) d[u] = ld_stream(tile + (rb + u * RPI + rsub) * LPR + sub);
@@ -157,7 +189,8 @@ index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1)
         best[i] = fmaxf(best[i], __shfl_xor_sync(0xffffffffu, best[i], o));
-      if (lane == 0 && lim[i] > 0) out[(int64_t)i * Hkv * max_blocks] = best[i];
+      if (lane == 0 && lim[i] > r0 && !isnan(best[i]))
+        atomic_max_score(out + (int64_t)i * Hkv * max_blocks, best[i]);
     }
   }
 }
@@ -183,6 +216,12 @@ msa_status launch(const msa_config& c, const WsView& v, const void* idx_q, const
   }
   const int grid = sm_count() * blocks_per_sm;
   if (grid <= 0) return MSA_ERR_CUDA;
+  const int64_t row_slots = (int64_t)c.num_kv_heads * c.max_blocks_per_req;
+  const int64_t slots = (int64_t)max_tokens_of(c) * row_slots;
+  const unsigned igrid = (unsigned)std::min<int64_t>((slots + 255) / 256, (int64_t)sm_count() * 8);
+  msa_status st = launch_pdl(score_init_kernel, dim3(igrid > 0 ? igrid : 1), dim3(256), 0, s, v,
+                             row_slots, scores);
+  if (st != MSA_OK) return st;
   return launch_pdl(index_score_kernel<DIDX, QL>, dim3(grid), dim3(kThreads), 0, s, v,
                     c.num_kv_heads, c.max_blocks_per_req, max_tokens_of(c),
                     (const uint4*)idx_q, (const uint4*)idx_k, scores);
