@@ -263,7 +263,10 @@ msa_status msa_index_attention(const msa_config* cfg, const void* ws, const void
  *     block_scores[t, h, j] = max over tokens u of block j with
  *                             position(u) <= position(t) of  idx_q[t,h,:] . idx_k[u,h,:]
  * accumulated in fp32 (exact for the integer-valued index vectors used in
- * tests).  Entries j >= the token's visible block count are not written.
+ * tests).  Entries j >= the token's visible block count are not written,
+ * except in decode mode with one new token per request, where every entry of
+ * the step's tokens is first set to -inf (the scan's two half-block units meet
+ * there by an atomic max).
  * Decode mode: bandwidth-bound, every visible index key read once per request
  * (q_len <= 4 queries share each load).  Prefill mode: tensor-core tiles of
  * 128 query tokens x two 128-key blocks (tcgen05, fp32 accumulators in tensor
