@@ -564,16 +564,17 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False, dense_sparse=
             if timed:
                 evs[i][1].record(stream)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    assert msa.check_device_error(sa.ws) == 0
-
     K = steps
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in names] for _ in range(K)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(clock_gpu) as clk:
+        # the warm-up steps run once the sampler is up, right before the timed
+        # region, so that the GPU does not sit idle between them
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        assert msa.check_device_error(sa.ws) == 0
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
