@@ -678,7 +678,8 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False, dense_sparse=
 # of their cost is drawing the inputs, 90 GB for the long decode).  A name
 # "<workload>:dense_sparse" runs that workload's decode in the dense-sparse
 # form (the A/B of the two decode formulations).
-OTHER_WORKLOADS = {"prefill": (40, 5), "fp8_decode": (200, 10), "nvfp4_decode": (200, 10),
+OTHER_WORKLOADS = {"prefill": (40, 5), "nvfp4_prefill": (40, 5), "fp8_decode": (200, 10),
+                   "nvfp4_decode": (200, 10),
                    "verify": (100, 5), "long_decode": (40, 5),
                    "medium_decode:dense_sparse": (200, 10)}
 

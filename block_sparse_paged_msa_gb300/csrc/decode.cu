@@ -203,27 +203,6 @@ __device__ __forceinline__ void convert_v_rows(const uint8_t* tile, uint8_t* con
   }
 }
 
-// Eight FP4 E2M1 codes (four bytes, the even element in each low nibble) ->
-// four f16x2, byte i -> h[i].
-__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
-      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-      : "r"(w));
-}
-
-// An E4M3 block-scale byte -> f16x2 holding it twice.
-__device__ __forceinline__ uint32_t e4m3_scale_f16x2(uint32_t byte) {
-  return e4m3x2_to_f16x2((uint16_t)(byte | (byte << 8)));
-}
-
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
-  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
-                            *reinterpret_cast<const __half2*>(&b));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
 // NVFP4: the warp converts its 32 rows of a V slot (72-byte rows: 64 bytes of
 // E2M1 codes, 8 E4M3 block scales) to f16 rows in its private staging area
 // (256-byte swizzled rows), zeroing rows past the last visible token.

@@ -322,6 +322,28 @@ __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// NVFP4 (E2M1 codes with E4M3 scales per 16 elements) dequantisation helpers.
+// Eight FP4 E2M1 codes (four bytes, the even element in each low nibble) ->
+// four f16x2, byte i -> h[i].
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// An E4M3 block-scale byte -> f16x2 holding it twice.
+__device__ __forceinline__ uint32_t e4m3_scale_f16x2(uint32_t byte) {
+  return e4m3x2_to_f16x2((uint16_t)(byte | (byte << 8)));
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
+                            *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 // Order this thread's generic-proxy shared-memory accesses with later
 // async-proxy ones (tensor core operand reads, TMA reads and writes): needed
 // before a TMA copy may overwrite shared memory this thread wrote, and before

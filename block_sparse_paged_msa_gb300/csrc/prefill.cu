@@ -26,6 +26,7 @@
 //    tile stores with their LSE beside them.  msa_combine merges each token's
 //    slots.
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "tcgen05.cuh"
@@ -187,11 +188,64 @@ __device__ __forceinline__ uint64_t qstep_desc(uint32_t base, int ks) {
 
 struct PrefillArgs {
   int Hkv, Hq, G, S, B, NB;
-  float scale_log2;
+  float scale_log2;                // softmax_scale * k_scale * log2(e)
+  float v_scale;                   // applied to the normalised partial rows
   const __nv_bfloat16* q;
   const int32_t* row_ptr;
   const int32_t* q_idx;
+  const uint8_t* k_pool;           // NVFP4: the pools, read with bulk copies (no tensor map)
+  const uint8_t* v_pool;
 };
+
+// NVFP4 slots: per (page, KV head) a key slot (2h) and a value slot (2h + 1)
+// of 128 rows x 72 bytes (64 bytes of E2M1 codes, 8 E4M3 block scales).
+constexpr int kFp4Row = kHeadDim / 2 + kHeadDim / 16;
+constexpr int kFp4Slot = kBlock * kFp4Row;
+
+// NVFP4 slot in shared memory -> the 128 x 128 tile as TMA would have landed
+// it (two 64-column halves, 128-byte swizzle): keys as bf16 (the S MMA's
+// operand type, the queries being bf16), values as fp16 (the P V MMA's).
+// e2m1 x e4m3 is exact in both (at most 6 significant bits, 2^-10 .. 2688).
+// Values of rows past the last visible key become 0 (their scale byte may
+// be anything, NaN included).  256 threads, four 16-element blocks each.
+template <bool kValues>
+__device__ __forceinline__ void fp4_slot_to_tile(const uint8_t* slot, uint8_t* tile, int ntok,
+                                                 int tid) {
+#pragma unroll
+  for (int i = tid; i < kBlock * 8; i += 256) {
+    const int key = i >> 3, c16 = i & 7;       // 16-element block c16 of row key
+    const uint8_t* rp = slot + key * kFp4Row;
+    const uint2 w = *reinterpret_cast<const uint2*>(rp + 8 * c16);
+    const uint32_t sc = e4m3_scale_f16x2(rp[kHeadDim / 2 + c16]);
+    uint32_t h[8];
+    {
+      uint32_t lo[4], hi[4];
+      e2m1x8_to_f16x2(w.x, lo);
+      e2m1x8_to_f16x2(w.y, hi);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h[e] = hmul2_u32(lo[e], sc);
+        h[4 + e] = hmul2_u32(hi[e], sc);
+      }
+    }
+    if (kValues) {
+      if (key >= ntok) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h[e] = 0u;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const __nv_bfloat162 b =
+            __float22bfloat162_rn(__half22float2(*reinterpret_cast<const __half2*>(&h[e])));
+        h[e] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+    }
+    // elements 16 c16 .. + 7 and + 8 .. + 15: 16-byte chunks 2 c16, 2 c16 + 1
+    *reinterpret_cast<uint4*>(tile + swz_tma(key, 2 * c16)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(tile + swz_tma(key, 2 * c16 + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
 
 // Persistent: one CTA per SM walks the work items.  Per CSR row (KV head h,
 // request r, key block j) the K tile and the V tile arrive by TMA (the next
@@ -211,6 +265,7 @@ struct PrefillArgs {
 // TMEM: per warpgroup 128 columns of S / P and 128 of O (512 in all).  P
 // never touches shared memory.  The issuer polls both warpgroups and serves
 // whichever is ready; the loaders run ahead across items.
+template <bool FP4>
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
@@ -224,7 +279,9 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
   uint8_t* Kt = smem;                          // K tile, bf16, K-major SW128 [key][d]
   // V of the current row and of the next one, [key][d] as TMA lands it; the
   // current one converted to fp16 in place is the MN-major B operand of P V
-  auto Vb = [&](int i) { return i ? smem + 6 * kTileBytes : smem + kTileBytes; };
+  // (NVFP4: one V buffer; the next row's two slots land in 18 KB of the second)
+  auto Vb = [&](int i) { return i && !FP4 ? smem + 6 * kTileBytes : smem + kTileBytes; };
+  uint8_t* Stg = smem + 6 * kTileBytes;        // NVFP4: key slot, value slot
   uint8_t* Pb = smem + 2 * kTileBytes;         // O staging tiles [2], fp16 [row][d]
   uint8_t* Qb = Pb + 2 * kTileBytes;           // Q[2], bf16 [row][d]
 
@@ -283,7 +340,21 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     tma_load_2d_hint(Kt, &tmap_k, 0, y, &k_full, pol);
     tma_load_2d_hint(Kt + kTileBytes / 2, &tmap_k, 64, y, &k_full, pol);
   };
+  // NVFP4: both slots of CSR row rw into the staging area (on v_full)
+  auto load_kv4 = [&](int rw) {
+    ++n_vload;
+    const int jj = rw % a.NB, rr = (rw / a.NB) % a.B, hh = rw / (a.NB * a.B);
+    const int pg = ws.block_table[(int64_t)rr * a.NB + jj];
+    const int64_t slot = ((int64_t)(pg < 0 ? 0 : pg) * a.Hkv + hh) * 2;
+    mbar_arrive_expect_tx(&v_full, 2 * kFp4Slot);
+    bulk_load(Stg, a.k_pool + slot * kFp4Slot, kFp4Slot, &v_full);
+    bulk_load(Stg + kFp4Slot, a.v_pool + (slot + 1) * kFp4Slot, kFp4Slot, &v_full);
+  };
   auto load_v = [&](int rw, int buf) {
+    if (FP4) {
+      load_kv4(rw);
+      return;
+    }
     ++n_vload;
     uint8_t* Vst = Vb(buf);
     const int jj = rw % a.NB, rr = (rw / a.NB) % a.B, hh = rw / (a.NB * a.B);
@@ -323,10 +394,21 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
     // item did not know) they are requested now.
     if (new_row) vsel ^= 1;
     if (new_row && issuer && lane == 0 && pf_row != row) {
-      load_k(row);
+      if (!FP4) load_k(row);
       load_v(row, vsel);
     }
-    if (new_row && warp < 8) {
+    if (new_row && warp < 8 && FP4) {
+      // NVFP4: the row's key and value slots -> the K tile (bf16) and the V
+      // tile (fp16); the staging area is then free for the next row's slots
+      mbar_wait(&v_full, v_phase, ws.hdr);
+      v_phase ^= 1u;
+      fp4_slot_to_tile<false>(Stg, Kt, ntok, tid);
+      fp4_slot_to_tile<true>(Stg + kFp4Slot, Vb(0), ntok, tid);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&vt_ready);
+    }
+    if (new_row && warp < 8 && !FP4) {
       mbar_wait(&v_full, v_phase, ws.hdr);
       v_phase ^= 1u;
       {
@@ -435,7 +517,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
         const uint32_t vlo = (uint32_t)dv, vhi = (uint32_t)(dv >> 32);
         const uint32_t klo = (uint32_t)dk, khi = (uint32_t)(dk >> 32);
         const int nrow = next_row(k, row);
-        if (new_row) {
+        if (new_row && !FP4) {
           mbar_wait(&k_full, k_phase, ws.hdr);
           k_phase ^= 1u;
         }
@@ -450,7 +532,8 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
           v_done = true;
         }
         pf_row = nrow;
-        bool k_done = nrow < 0;                  // the next row's K is requested
+        bool k_done = nrow < 0 || FP4;           // the next row's K is requested
+                                                 // (NVFP4: with its V, into the staging)
         int nS[2] = {0, 0}, nP[2] = {0, 0};      // this item's S / PV per warpgroup
         const int want[2] = {(ntiles + 1) / 2, ntiles / 2};
         uint32_t spins = 0;
@@ -474,7 +557,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
 #pragma unroll
           for (int w = 0; w < 2; ++w) {
             // S_k overwrites P_{k-1}: only once O_{k-1} = P_{k-1} V completed
-            if (nS[w] < want[w] &&
+            if (nS[w] < want[w] && (!FP4 || vt_ok) &&
                 mbar_test_wait(&q_full[w], (uint32_t)(kS[w] & 1)) &&
                 (kS[w] == 0 || mbar_test_wait(&o_ready[w], (uint32_t)((kS[w] - 1) & 1)))) {
               tc_fence_after();
@@ -634,7 +717,7 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
       // stores them as TMA boxes: 128 rows for a full tile, 8-row boxes for
       // the last one, whose rows past a multiple of 8 (G < 8 only) their own
       // threads write.  tcgen05.ld is warp-collective: every lane loads.
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? a.v_scale / l : 0.f;
       const uint64_t inv2 = f2(inv, inv);
       const int e0 = beg + t * TPT;
       const int nrows = min(TPT, end - e0) * G;     // valid rows of this tile
@@ -851,7 +934,8 @@ extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const 
   msa_status st = check_config(cfg);
   if (st != MSA_OK) return st;
   if (!is_prefill(*cfg)) return MSA_ERR_INVALID_ARG;
-  if (cfg->kv_dtype != MSA_KV_BF16) return MSA_ERR_UNSUPPORTED;
+  const bool fp4 = cfg->kv_dtype == MSA_KV_NVFP4;
+  if (cfg->kv_dtype != MSA_KV_BF16 && !fp4) return MSA_ERR_UNSUPPORTED;   // e4m3: not in prefill
   if (!ws || !q || !k_pages || !v_pages || !selected || !row_ptr || !q_indices)
     return MSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages)) return MSA_ERR_INVALID_ARG;
@@ -864,7 +948,10 @@ extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const 
   a.S = width_of(*cfg);
   a.B = cfg->max_batch;
   a.NB = cfg->max_blocks_per_req;
-  a.scale_log2 = cfg->softmax_scale * kLog2e;
+  a.scale_log2 = cfg->softmax_scale * (fp4 ? cfg->k_scale : 1.f) * kLog2e;
+  a.v_scale = fp4 ? cfg->v_scale : 1.f;
+  a.k_pool = (const uint8_t*)k_pages;
+  a.v_pool = (const uint8_t*)v_pages;
   a.q = (const __nv_bfloat16*)q;
   a.row_ptr = row_ptr;
   a.q_idx = q_indices;
@@ -872,8 +959,13 @@ extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const 
   const int64_t prow = (int64_t)cfg->num_pages * a.Hkv * kBlock;
   if (prow > 0x7fffffff) return MSA_ERR_UNSUPPORTED;
   CUtensorMap tk, tv, tq;
-  if (!make_pool_map(&tk, k_pages, prow, false) || !make_pool_map(&tv, v_pages, prow, false))
+  if (fp4) {
+    memset(&tk, 0, sizeof(tk));      // bulk copies from the pool pointers instead
+    memset(&tv, 0, sizeof(tv));
+  } else if (!make_pool_map(&tk, k_pages, prow, false) ||
+             !make_pool_map(&tv, v_pages, prow, false)) {
     return MSA_ERR_CUDA;
+  }
   // queries as [half (2)][row (tokens * H_q)][64 columns]: a box of 8 rows x
   // both halves is one 2 KB group of the half-interleaved Q tile (G >= 8)
   {
@@ -891,9 +983,10 @@ extern "C" msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const 
   if (!make_pool_map(&to, o_part, orows, false) || !make_pool_map(&to8, o_part, orows, false, 8))
     return MSA_ERR_CUDA;
   const size_t smem = kTcSmemBytes;
-  if ((st = set_smem(prefill_tc_kernel, smem)) != MSA_OK) return st;
   const int grid = sm_count();
   if (grid <= 0) return MSA_ERR_CUDA;
-  return launch_pdl(prefill_tc_kernel, dim3(grid), dim3(kTcThreads), smem, (cudaStream_t)stream,
+  auto kern = fp4 ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+  if ((st = set_smem(kern, smem)) != MSA_OK) return st;
+  return launch_pdl(kern, dim3(grid), dim3(kTcThreads), smem, (cudaStream_t)stream,
                     view_of(*cfg, ws), a, tk, tv, tq, to, to8, rows);
 }

@@ -120,6 +120,12 @@ WORKLOADS = {
         num_q_heads=64, num_kv_heads=8, head_dim=128, index_dim=128,
         init_blocks=1, local_tokens=256, topk_blocks=16, num_pages=1024,
         seed=1005),
+    # the same chunked prefill over an NVFP4 KV cache
+    "nvfp4_prefill": WorkloadSpec(
+        name="nvfp4_prefill", batch=4, seq_lens=(18432,) * 4, q_len=2048,
+        num_q_heads=64, num_kv_heads=8, head_dim=128, index_dim=128,
+        init_blocks=1, local_tokens=256, topk_blocks=16, num_pages=1024,
+        kv_dtype="nvfp4", kv_scale=0.75, seed=1008),
     # speculative verify: 4 draft tokens on a 32768-token context
     "verify": WorkloadSpec(
         name="verify", batch=64, seq_lens=(32768 + 4,) * 64, q_len=4,
@@ -142,6 +148,7 @@ def small(name: str, **kw) -> WorkloadSpec:
         "tiny_decode": dict(),
         "verify": dict(batch=4, seq_lens=(1500, 2000, 2600, 3001), num_pages=128),
         "prefill": dict(batch=2, seq_lens=(1400, 900), q_len=300, num_pages=40),
+        "nvfp4_prefill": dict(batch=2, seq_lens=(1400, 900), q_len=300, num_pages=40),
     }[name]
     defaults.update(kw)
     return base.replace(name=base.name + "_small", **defaults)

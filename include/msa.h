@@ -387,7 +387,11 @@ msa_status msa_build_k2q_csr(const msa_config* cfg, const void* ws, const int32_
  * G + g, so that a tile's rows are contiguous; msa_combine merges each token's
  * slots into out / lse.  selected is not read (the CSR build recorded what it
  * needs).  q, k_pages and v_pages must be 16-byte aligned.  Prefill mode, bf16
- * KV only (fp8 or nvfp4 -> MSA_ERR_UNSUPPORTED).
+ * or NVFP4 KV (fp8 -> MSA_ERR_UNSUPPORTED).  NVFP4 (vLLM
+ * MiniMaxM3SparseMSANvfp4Backend, whose prefill runs sparse_atten_nvfp4_kv_func):
+ * k_pages and v_pages are the slot pools as for decode; each row's key and
+ * value slots are dequantised in shared memory (keys to bf16, values to fp16,
+ * both exact), k_scale scales the scores and v_scale the output.
  */
 msa_status msa_sparse_prefill(const msa_config* cfg, void* ws, const void* q,
                               const void* k_pages, const void* v_pages,

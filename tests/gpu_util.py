@@ -10,8 +10,11 @@ from oracle_io import oracle_local_blocks, run_oracle, selected_array, to_np
 
 # Acceptance bounds: selection bit-exact; out max |err| <= 1e-2 and mean |err|
 # <= 1e-3 against fp64 (bf16 output rounding alone is ~4e-3 relative); LSE
-# within 1e-3.
+# within 1e-3.  NVFP4 KV (values up to 6 x the block scale, outputs up to ~4.5
+# here) adds 2^-8 |o| (at least half a bf16 ulp of the reference) to the max bound:
+# the output is bf16, and at |o| in [4, 8) rounding alone reaches 2^-6.
 OUT_MAX, OUT_MEAN, LSE_MAX = 1e-2, 1e-3, 1e-3
+NVFP4_OUT_REL = 2.0 ** -8
 
 
 def run_gpu(w: wl.Workload, **cfg_overrides):
@@ -35,7 +38,7 @@ def compare(w: wl.Workload, sa, ref, tokens=None, kv_heads=None):
     scores = sa.block_scores[:T].cpu().numpy()
     out = to_np(sa.out[:T])
     lse = sa.lse[:T].cpu().numpy().astype(np.float64)
-    errs, lerrs = [], []
+    errs, maxerrs, lerrs = [], [], []   # raw |err| (mean), |err| less the allowance (max)
     for t in tokens:
         for h in kv_heads:
             want = ref["selected"][(t, h)]
@@ -44,11 +47,16 @@ def compare(w: wl.Workload, sa, ref, tokens=None, kv_heads=None):
             sc = ref["scores"][(t, h)]
             assert np.array_equal(scores[t, h, :len(sc)], sc.astype(np.float32)), (t, h)
             hs = slice(h * G, (h + 1) * G)
-            errs.append(np.abs(out[t, hs] - ref["out"][t, hs]).ravel())
+            d = np.abs(out[t, hs] - ref["out"][t, hs])
+            errs.append(d.ravel())
+            if spec.kv_dtype == "nvfp4":
+                d = np.maximum(d - NVFP4_OUT_REL * np.abs(ref["out"][t, hs]), 0.0)
+            maxerrs.append(d.ravel())
             lerrs.append(np.abs(lse[t, hs] - ref["lse"][t, hs]))
     e = np.concatenate(errs)
     le = np.concatenate(lerrs)
-    stats = dict(out_max=float(e.max()), out_mean=float(e.mean()), lse_max=float(le.max()))
+    stats = dict(out_max=float(np.concatenate(maxerrs).max()), out_mean=float(e.mean()),
+                 lse_max=float(le.max()))
     assert stats["out_max"] <= OUT_MAX and stats["out_mean"] <= OUT_MEAN, stats
     assert stats["lse_max"] <= LSE_MAX, stats
     return stats

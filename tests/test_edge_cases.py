@@ -150,7 +150,7 @@ def test_graph_replay_equals_eager(name):
 
 
 @pytest.mark.parametrize("name", ["medium_decode", "fp8_decode", "nvfp4_decode", "verify",
-                                  "verify:dense_sparse", "prefill"])
+                                  "verify:dense_sparse", "prefill", "nvfp4_prefill"])
 def test_repeated_runs_bit_identical(name):
     """The same step on the same inputs, 32 times in a row on one workspace:
     every output and LSE must equal the first run's bit for bit.  The verify

@@ -45,6 +45,24 @@ def test_small_prefill_every_element(kw):
     _csr_matches_oracle(w, sa)
 
 
+@pytest.mark.parametrize("kw", [dict(), dict(num_q_heads=16, num_kv_heads=4, index_dim=64),
+                                dict(seq_lens=(700, 129), q_len=129, topk_blocks=2)],
+                         ids=["g8", "g4_d64", "chunk129_topk2"])
+def test_small_nvfp4_prefill_every_element(kw):
+    """NVFP4 KV (E2M1 codes with E4M3 block scales, a key and a value slot per
+    KV head) in the prefill tiles: each CSR row's slots are dequantised in
+    shared memory (keys to bf16, values to fp16, both exact) with k_scale in
+    the softmax scale and v_scale on the output; compared on every element
+    with the oracle fed the same dequantised pool."""
+    spec = wl.small("nvfp4_prefill", **kw)
+    w = wl.make_workload(spec, device="cuda")
+    sa = run_gpu(w)
+    assert sa.prefill
+    assert msa.check_device_error(sa.ws) == 0
+    print(compare(w, sa, run_oracle(w.to("cpu"))))
+    _csr_matches_oracle(w, sa)
+
+
 def test_prefill_whole_sequence_is_dense_causal():
     """A chunk that is the whole sequence with top-k covering every block is
     plain causal attention."""
