@@ -111,7 +111,10 @@ def compare_sampled(w: wl.Workload, sa, samples):
         assert np.array_equal(scores[t, h, :len(sc)], sc.astype(np.float32)), (t, h)
         e = np.abs(out[t, h * G:(h + 1) * G] - ref["out"][t - q0])
         le = np.abs(lse[t, h * G:(h + 1) * G] - ref["lse"][t - q0])
-        worst["out_max"] = max(worst["out_max"], float(e.max()))
+        em = e
+        if spec.kv_dtype == "nvfp4":
+            em = np.maximum(e - NVFP4_OUT_REL * np.abs(ref["out"][t - q0]), 0.0)
+        worst["out_max"] = max(worst["out_max"], float(em.max()))
         worst["out_mean"] = max(worst["out_mean"], float(e.mean()))
         worst["lse_max"] = max(worst["lse_max"], float(le.max()))
     assert worst["out_max"] <= OUT_MAX and worst["out_mean"] <= OUT_MEAN, worst

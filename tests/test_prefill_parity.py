@@ -76,8 +76,9 @@ def test_prefill_whole_sequence_is_dense_causal():
         assert s == list(range(t // 128 + 1))
 
 
-def test_prefill_full_size_sampled():
-    spec = wl.WORKLOADS["prefill"]
+@pytest.mark.parametrize("name", ["prefill", "nvfp4_prefill"])
+def test_prefill_full_size_sampled(name):
+    spec = wl.WORKLOADS[name]
     w = wl.make_workload(spec, device="cuda")
     sa = run_gpu(w)
     assert msa.check_device_error(sa.ws) == 0
