@@ -44,7 +44,7 @@ __all__ = [
     "query_positions", "gather_sequence", "block_scores", "select_blocks",
     "attention", "combine", "sparse_attention", "build_k2q_csr", "e4m3_encode",
     "cache_slots", "cache_write", "e2m1_to_float", "nvfp4_dequant", "nvfp4_row_bytes",
-    "NVFP4_BLOCK", "compact_selection", "paged_attention", "index_attention",
+    "NVFP4_BLOCK", "e2m1_encode", "nvfp4_quantize", "cache_write_nvfp4", "compact_selection", "paged_attention", "index_attention",
 ]
 
 
@@ -157,6 +157,52 @@ def nvfp4_dequant(rows: np.ndarray, head_dim: int) -> np.ndarray:
     vals[..., 0::2] = e2m1_to_float(data & 0xF)
     vals[..., 1::2] = e2m1_to_float(data >> 4)
     return vals * np.repeat(e4m3_to_float(scales), NVFP4_BLOCK, axis=-1)
+
+
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def e2m1_encode(x: np.ndarray) -> np.ndarray:
+    """Float values -> 4-bit e2m1 codes (uint8 0..15), from the format's
+    definition: the nearest representable magnitude, ties to the code whose
+    mantissa (last) bit is 0; magnitudes beyond 6 saturate to 6; the sign bit
+    is kept (a negative value that rounds to zero is 0x8)."""
+    x = np.asarray(x, dtype=np.float64)
+    mag = np.abs(x)
+    hi = np.clip(np.searchsorted(_E2M1_MAG, mag), 0, len(_E2M1_MAG) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = mag - _E2M1_MAG[lo]
+    d_hi = _E2M1_MAG[hi] - mag
+    code = np.where(d_lo < d_hi, lo, hi)
+    code = np.where(d_lo == d_hi, np.where(lo % 2 == 0, lo, hi), code)
+    code = np.where(mag >= _E2M1_MAG[-1], len(_E2M1_MAG) - 1, code)
+    return (code | np.where(np.signbit(x), 8, 0)).astype(np.uint8)
+
+
+def nvfp4_quantize(x: np.ndarray, scale: float) -> np.ndarray:
+    """[..., D] values -> [..., D/2 + D/16] uint8 NVFP4 rows, for a pool with
+    tensor scale ``scale``.  (Reading: the pages give the format, not the
+    quantiser.)  Every 16-element block's scale is the E4M3 code of
+    amax / (6 * scale) -- its largest magnitude onto E2M1's largest, 6 -- and
+    each element the E2M1 code of x / (block scale * scale); a block whose
+    scale code is 0 stores zero codes.  The operands are fp32, 6 * scale and
+    block scale * scale fp32 products, each quotient one IEEE fp32 division:
+    the precision in which the kernel takes the same rounding decisions."""
+    x = np.asarray(x, dtype=np.float32)
+    D = x.shape[-1]
+    g = np.float32(scale)
+    blocks = x.reshape(x.shape[:-1] + (D // NVFP4_BLOCK, NVFP4_BLOCK))
+    amax = np.abs(blocks).max(axis=-1)
+    q = (amax / (np.float32(6.0) * g)).astype(np.float32)
+    sc = e4m3_encode(q)
+    div = (e4m3_to_float(sc).astype(np.float32) * g).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        u = (blocks / div[..., None]).astype(np.float32)
+    codes = np.where(div[..., None] == 0, np.uint8(0), e2m1_encode(u)).reshape(x.shape)
+    out = np.empty(x.shape[:-1] + (nvfp4_row_bytes(D),), dtype=np.uint8)
+    out[..., :D // 2] = codes[..., 0::2] | (codes[..., 1::2] << 4)
+    out[..., D // 2:] = sc
+    return out
 
 
 # --------------------------------------------------------------------------
@@ -435,6 +481,24 @@ def cache_write(pool: np.ndarray, slots: Sequence[int], rows: np.ndarray,
         else:
             q = np.asarray(rows[t], dtype=np.float32) / np.float32(e4m3_scale)
             out[page, :, row, :] = e4m3_encode(q)
+    return out
+
+
+def cache_write_nvfp4(pool: np.ndarray, slots: Sequence[int], rows: np.ndarray, scale: float,
+                      kind: int) -> np.ndarray:
+    """A copy of the NVFP4 pool [num_pages, 2 H, P, row bytes] with rows[t, h]
+    ([T, H, D] values) quantised (nvfp4_quantize, tensor scale ``scale``) into
+    slot 2 h + kind (0: keys, 1: values) of page slot // P at row slot % P,
+    for every token whose slot is >= 0."""
+    out = pool.copy()
+    P = pool.shape[2]
+    H = pool.shape[1] // 2
+    for t, slot in enumerate(slots):
+        if slot < 0:
+            continue
+        page, row = slot // P, slot % P
+        for h in range(H):
+            out[page, 2 * h + kind, row, :] = nvfp4_quantize(rows[t, h], scale)
     return out
 
 

@@ -446,6 +446,117 @@ def test_nvfp4_row_hand_decoded():
     assert np.array_equal(got, want)
 
 
+def test_e2m1_encode_hand_values():
+    """E2M1 rounding from the format's definition: nearest of 0, 0.5, 1, 1.5, 2,
+    3, 4, 6; a midpoint goes to the code with mantissa bit 0 (the even code);
+    beyond 6 saturates; the sign bit is kept, also on a value that rounds to 0."""
+    x = [0.0, 0.25, 0.26, 0.5, 0.75, 1.25, 1.74, 1.75, 2.5, 3.5, 5.0, 5.01, 6.0, 7.0, 1e9,
+         -0.1, -0.25, -0.3, -2.5, -100.0, -0.0]
+    want = [0, 0, 1, 1, 2, 2, 3, 4, 4, 6, 6, 7, 7, 7, 7,
+            8, 8, 9, 12, 15, 8]
+    assert oracle.e2m1_encode(np.array(x)).tolist() == want
+
+
+def test_e2m1_encode_is_nearest_code_by_exhaustive_search():
+    """Every multiple of 1/64 in [-8, 8] (every midpoint among them): the code
+    is the one of the 16 whose value is nearest, ties to the even code;
+    magnitudes beyond 6 take +-6."""
+    x = np.arange(-512, 513) / 64.0
+    got = oracle.e2m1_encode(x)
+    vals = oracle.e2m1_to_float(np.arange(16))
+    for xi, c in zip(x, got):
+        target = min(max(xi, -6.0), 6.0)
+        d = np.abs(vals - target)
+        best = [k for k in range(16) if d[k] == d.min() and np.signbit(vals[k]) == np.signbit(xi)]
+        if len(best) > 1:
+            best = [k for k in best if k % 2 == 0]
+        assert c == best[0], (xi, c, best)
+
+
+def test_nvfp4_quantize_round_trips_representable_blocks():
+    """A block whose values are e2m1(code) * e4m3(s) * scale and whose largest
+    magnitude is 6 * e4m3(s) * scale quantises back to exactly those codes and
+    that scale byte (powers of two as tensor scales keep every product exact)."""
+    rng = np.random.default_rng(5)
+    D = 128
+    for scale in (1.0, 0.5, 2.0 ** -6):
+        codes = rng.integers(0, 16, size=(6, D)).astype(np.uint8)
+        codes[:, ::16] = rng.choice([7, 15], size=(6, D // 16))   # a +-6 in every block
+        sc = rng.integers(0x08, 0x60, size=(6, D // 16)).astype(np.uint8)
+        rows = np.zeros((6, oracle.nvfp4_row_bytes(D)), dtype=np.uint8)
+        rows[:, :D // 2] = codes[:, 0::2] | (codes[:, 1::2] << 4)
+        rows[:, D // 2:] = sc
+        x = oracle.nvfp4_dequant(rows, D) * scale
+        assert np.array_equal(oracle.nvfp4_quantize(x.astype(np.float32), scale), rows)
+
+
+def test_nvfp4_quantize_hand_block():
+    """One row worked by hand, tensor scale 0.75 (6 * 0.75 = 4.5).
+    Block 0: amax 3 -> 3 / 4.5 = 0.667 -> nearest e4m3 0.6875 (0x33; 0.625 is
+    farther), divisor 0.6875 * 0.75 = 0.515625; its elements sit at quotients
+    5.818 -> 6, 1.25 -> 1 (tie, even), 2.5 -> 2 (tie), 5 -> 4 (tie), 0.75 -> 1
+    (tie, even code 2), 0.25 -> 0 (tie), -0.25 -> -0 (sign kept), -1.745 -> -1.5.
+    Block 1: all zero -> scale 0, codes 0.  Block 2: amax 3.9 at tensor scale
+    0.75 -> 3.9 / 4.5 = 0.8667 -> e4m3 0.875 (0x36), divisor 0.65625,
+    3.9 / 0.65625 = 5.94 -> 6.  Block 3: amax 1e4 -> the scale saturates at 448
+    (0x7E), divisor 336, 1e4 / 336 = 29.8 -> 6 (saturated).  Block 4: amax 1e-4
+    -> 1e-4 / 4.5 rounds to the e4m3 zero -> scale 0 and zero codes."""
+    D = 128
+    x = np.zeros(D, dtype=np.float32)
+    d = 0.515625
+    x[0:8] = [3.0, 1.25 * d, 2.5 * d, 5.0 * d, 0.75 * d, 0.25 * d, -0.25 * d, -0.9]
+    x[32], x[33] = 3.9, -1.0
+    x[48], x[49] = 1e4, -100.0
+    x[64], x[65] = 1e-4, -5e-5
+    got = oracle.nvfp4_quantize(x, 0.75)
+    want = np.zeros(72, dtype=np.uint8)
+    want[0:4] = [0x7 | (0x2 << 4), 0x4 | (0x6 << 4), 0x2 | (0x0 << 4), 0x8 | (0xB << 4)]
+    want[16] = 0x7 | (0xB << 4)                 # 3.9 -> 6; -1.0 / 0.65625 = -1.52 -> -1.5
+    want[24] = 0x7 | (0x9 << 4)                 # 1e4 -> 6; -100 / 336 = -0.298 -> -0.5
+    want[64:72] = [0x33, 0x00, 0x36, 0x7E, 0x00, 0x00, 0x00, 0x00]
+    assert got.tolist() == want.tolist()
+
+
+def test_nvfp4_quantize_error_bound_random():
+    """Random rows: every element dequantises to within half an E2M1 step (at
+    its quotient) of its value, scaled by the block divisor, unless the block
+    scale rounded down and the element saturated at 6; then within 6.25% of
+    the block's amax (half the relative spacing of normal e4m3 scales, which
+    these magnitudes keep)."""
+    rng = np.random.default_rng(11)
+    D = 128
+    x = (rng.standard_normal((64, D)) * rng.choice([0.2, 1.0, 50.0], size=(64, 1))).astype(
+        np.float32)
+    scale = 0.75
+    q = oracle.nvfp4_quantize(x, scale)
+    xh = oracle.nvfp4_dequant(q, D) * scale
+    div = oracle.e4m3_to_float(q[:, D // 2:]).repeat(16, axis=1) * scale
+    u = np.abs(x) / div
+    step = np.where(u < 2, 0.5, np.where(u < 4, 1.0, 2.0))
+    amax = np.abs(x.reshape(64, 8, 16)).max(-1).repeat(16, axis=1)
+    err = np.abs(xh - x)
+    ok = (err <= 0.5 * step * div * (1 + 1e-5)) | ((u > 6) & (err <= 0.0625 * amax * (1 + 1e-5)))
+    assert (q[:, D // 2:] >= 0x08).all()   # normal scales only
+    assert ok.all()
+
+
+def test_cache_write_nvfp4_places_slots():
+    """Keys go to slot 2h, values to slot 2h + 1 of the token's page row; the
+    other slots and rows keep their bytes."""
+    P, H, D = 4, 2, 32
+    RB = oracle.nvfp4_row_bytes(D)
+    pool = np.full((3, 2 * H, P, RB), 0xAB, dtype=np.uint8)
+    rows = np.arange(2 * H * D, dtype=np.float32).reshape(2, H, D) / 7.0 - 5.0
+    k_out = oracle.cache_write_nvfp4(pool, [1 * P + 2, -1], rows, 0.5, 0)
+    v_out = oracle.cache_write_nvfp4(pool, [1 * P + 2, -1], rows, 0.5, 1)
+    want_k, want_v = pool.copy(), pool.copy()
+    for h in range(H):
+        want_k[1, 2 * h, 2] = oracle.nvfp4_quantize(rows[0, h], 0.5)
+        want_v[1, 2 * h + 1, 2] = oracle.nvfp4_quantize(rows[0, h], 0.5)
+    assert np.array_equal(k_out, want_k) and np.array_equal(v_out, want_v)
+    assert (pool == 0xAB).all()
+
+
 def test_nvfp4_path_uses_dequantised_values():
     """Attention over an NVFP4 pool equals attention over the float pools that
     hold its dequantised values times the tensor scales (K from slot 2h, V from
@@ -588,7 +699,36 @@ def _mutants():
         pages, n = real_compact(selected, bt_row, position, P)
         return pages, P * len(pages)
 
+    real_e2m1_enc, real_quant = oracle.e2m1_encode, oracle.nvfp4_quantize
+
+    def e2m1_ties_away(x):                # round half away from zero
+        x = np.asarray(x, dtype=np.float64)
+        return real_e2m1_enc(np.nextafter(np.abs(x), np.inf) * np.where(np.signbit(x), -1, 1))
+
+    def quant_no_tensor_scale(x, scale):  # the block scale from amax / 6 alone
+        x = np.asarray(x, dtype=np.float32)
+        D = x.shape[-1]
+        out = real_quant(x, 1.0)
+        div = (oracle.e4m3_to_float(out[..., D // 2:]) * scale).repeat(16, axis=-1)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            c = np.where(div == 0, 0, real_e2m1_enc(x / div)).astype(np.uint8)
+        out[..., :D // 2] = c[..., 0::2] | (c[..., 1::2] << 4)
+        return out
+
+    def quant_scale_from_mean(x, scale):  # the block scale from the mean magnitude
+        x = np.asarray(x, dtype=np.float32)
+        b = np.abs(x.reshape(x.shape[:-1] + (-1, 16)))
+        ratio = (b.max(-1) / np.maximum(b.mean(-1), 1e-30)).repeat(16, axis=-1)
+        return real_quant(np.where(b.reshape(x.shape) > 0, x / ratio.reshape(x.shape), x), scale)
+
+    real_cw4 = oracle.cache_write_nvfp4
+
+    def cw4_slot_swapped(pool, slots, rows, scale, kind):   # values in the key slot
+        return real_cw4(pool, slots, rows, scale, 1 - kind)
+
     return [("compact_selection", compact_all_full),
+            ("e2m1_encode", e2m1_ties_away), ("nvfp4_quantize", quant_no_tensor_scale),
+            ("nvfp4_quantize", quant_scale_from_mean), ("cache_write_nvfp4", cw4_slot_swapped),
             ("e2m1_to_float", e2m1_no_subnormal), ("nvfp4_dequant", nvfp4_nibbles_swapped),
             ("e4m3_encode", encode_ties_away), ("cache_slots", slots_one_late),
             ("block_scores", scores_sum), ("block_scores", scores_no_causal),
@@ -613,6 +753,12 @@ _PINS = [
     test_cache_write_places_rows_and_leaves_the_rest,
     test_e2m1_codes_are_the_published_value_set,
     test_nvfp4_row_hand_decoded,
+    test_e2m1_encode_hand_values,
+    test_e2m1_encode_is_nearest_code_by_exhaustive_search,
+    test_nvfp4_quantize_round_trips_representable_blocks,
+    test_nvfp4_quantize_hand_block,
+    test_nvfp4_quantize_error_bound_random,
+    test_cache_write_nvfp4_places_slots,
     test_compact_selection_hand_computed,
 ]
 
