@@ -61,7 +61,6 @@ constexpr int kStages = 3;                         // ring depth (tiles)
 constexpr int kTileBytes = kBlock * kHeadDim * 2;  // bf16 tile, 32 KiB
 constexpr int kFp8Stages = 4;                      // fp8 tiles are 16 KiB
 constexpr int kFp8TileBytes = kBlock * kHeadDim;
-constexpr int kFp4Row = kHeadDim / 2 + kHeadDim / 16;   // NVFP4 row: 64 data + 8 scale bytes
 constexpr int kFp4Stages = 7;                      // NVFP4 slots are 9 KiB (two CTAs per SM)
 constexpr int kFp4TileBytes = kBlock * kFp4Row;
 

@@ -15,6 +15,7 @@ namespace msa {
 
 constexpr int kBlock = 128;      // P: sparse block = KV page
 constexpr int kHeadDim = 128;    // D
+constexpr int kFp4Row = kHeadDim / 2 + kHeadDim / 16;   // NVFP4 row: 64 code + 8 scale bytes
 constexpr int kMaxGroup = 16;    // query heads per KV head (one m16 MMA tile)
 constexpr int kMaxBlocksPerReq = 8192;
 constexpr int kMaxBatch = 65536;

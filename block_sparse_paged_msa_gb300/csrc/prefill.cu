@@ -199,7 +199,6 @@ struct PrefillArgs {
 
 // NVFP4 slots: per (page, KV head) a key slot (2h) and a value slot (2h + 1)
 // of 128 rows x 72 bytes (64 bytes of E2M1 codes, 8 E4M3 block scales).
-constexpr int kFp4Row = kHeadDim / 2 + kHeadDim / 16;
 constexpr int kFp4Slot = kBlock * kFp4Row;
 
 // NVFP4 slot in shared memory -> the 128 x 128 tile as TMA would have landed

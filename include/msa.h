@@ -224,9 +224,16 @@ msa_status msa_plan_from_req_to_token(const msa_config* cfg, int32_t batch,
  * bf16 pools store the values as they are.  e4m3 pools store, per value, the
  * e4m3fn code nearest to x / scale (cfg->k_scale or v_scale; one IEEE fp32
  * division), ties to even, magnitudes beyond 448 saturated to +-448, NaN kept.
+ * NVFP4 pools (k_pages and v_pages may be the same allocation) take the keys
+ * of KV head h in slot 2h of k_pages and the values in slot 2h + 1 of
+ * v_pages.  The pages give the format, not the quantiser; this library's
+ * reading: each 16-element block's scale byte is the e4m3fn code of
+ * amax / (6 * scale), each element the E2M1 code of x / (e4m3(scale byte) *
+ * scale), every division and product one IEEE fp32 operation and every code
+ * round-to-nearest-even, saturating; a block whose scale code is 0 stores zero
+ * codes.
  * Tokens of idle requests are skipped.  A slot outside [0, num_pages * P) is
  * skipped and sets MSA_DEVERR_PAGE_RANGE.  All pointers 16-byte aligned.
- * NVFP4 pools have no write form here (MSA_ERR_UNSUPPORTED).
  */
 msa_status msa_cache_write(const msa_config* cfg, void* ws, const int64_t* out_cache_loc,
                            const void* k, const void* v, const void* idx_k, const void* idx_v,

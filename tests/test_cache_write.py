@@ -6,9 +6,12 @@ set_fused_kv_index_buffer) is byte work: the pools after the write must equal,
 byte for byte, the oracle's pools -- rows placed by the plan's block table and
 positions, or by explicit out_cache_loc slots; e4m3 pools hold the codes of
 x / scale, rounded to nearest even and saturated (planted values beyond +-448
-and in the subnormal range).  Bad slots are flagged and skipped.  Written and
-then attended over in one captured CUDA graph, the step equals eager execution
-bit for bit and the oracle within the parity bounds."""
+and in the subnormal range); NVFP4 pools hold E2M1 codes under E4M3 block
+scales of amax / (6 * scale), keys in slot 2h and values in slot 2h + 1 (a
+planted block of exact rounding ties and signed zeros).  Bad slots are flagged
+and skipped.  Written and then attended over in one captured CUDA graph, the
+step equals eager execution bit for bit and the oracle within the parity
+bounds."""
 import numpy as np
 import pytest
 import torch
@@ -29,11 +32,25 @@ def _rows(spec, T, seed, plant=False):
                             device="cuda").to(torch.bfloat16)
         k[0, 0, :8] = vals
         v[-1, -1, -8:] = vals
+        # one 16-element block whose quotients are exact E2M1 ties at tensor
+        # scale 0.75: amax 3 -> block scale 0.6875, divisor 33/64; plus -0 and 0
+        d = 33.0 / 64.0
+        tie = torch.tensor([3.0, 0.25 * d, -0.75 * d, 1.25 * d, -1.75 * d, 2.5 * d, 3.5 * d,
+                            -5.0 * d, -0.0, 0.0, 0.5 * d, -3.0 * d, 6.0 * d, 4.0 * d, 0.0,
+                            -0.0], device="cuda")
+        assert torch.equal(tie.to(torch.bfloat16).float(), tie)
+        k[min(1, T - 1), 0, 16:32] = tie.to(torch.bfloat16)
     return k, v, idx_k
 
 
 def _expected(w, k, v, idx_k, slots):
     s = w.spec
+    if s.kv_dtype == "nvfp4":    # K and V slots of every head in each pool
+        kp = oracle.cache_write_nvfp4(to_np(w.k_pages), slots, to_np(k), s.kv_scale, 0)
+        vp = oracle.cache_write_nvfp4(to_np(w.v_pages), slots, to_np(v), s.kv_scale, 1)
+        if w.k_pages.data_ptr() == w.v_pages.data_ptr():
+            kp = vp = oracle.cache_write_nvfp4(kp, slots, to_np(v), s.kv_scale, 1)
+        return kp, vp, oracle.cache_write(to_np(w.idx_k_pages), slots, to_np(idx_k))
     scale = s.kv_scale if s.kv_dtype == "fp8_e4m3" else None
     return (oracle.cache_write(to_np(w.k_pages), slots, to_np(k), e4m3_scale=scale),
             oracle.cache_write(to_np(w.v_pages), slots, to_np(v), e4m3_scale=scale),
@@ -46,10 +63,11 @@ def _check_pools(w, want):
         assert np.array_equal(got, exp), name
 
 
-@pytest.mark.parametrize("name", ["medium_decode", "fp8_decode", "verify", "prefill"])
+@pytest.mark.parametrize("name", ["medium_decode", "fp8_decode", "nvfp4_decode", "verify",
+                                  "prefill", "nvfp4_prefill"])
 @pytest.mark.parametrize("explicit_slots", [False, True])
 def test_cache_write_bytes_match_oracle(name, explicit_slots):
-    spec = wl.small(name, batch=3) if name in ("medium_decode", "fp8_decode") else wl.small(name)
+    spec = wl.small(name, batch=3) if name.endswith("_decode") else wl.small(name)
     w = wl.make_workload(spec, device="cuda")
     cfg = msa.config_for(spec)
     sa = msa.SparseAttention(cfg)
@@ -104,7 +122,7 @@ def test_idle_request_writes_nothing_and_index_key_is_optional():
     _check_pools(w, want)
 
 
-@pytest.mark.parametrize("name", ["medium_decode", "fp8_decode", "verify"])
+@pytest.mark.parametrize("name", ["medium_decode", "fp8_decode", "nvfp4_decode", "verify"])
 def test_write_then_decode_graph_replay_equals_eager_and_oracle(name):
     """The cache write and the whole decode step captured as one CUDA graph;
     replayed on new inputs written in place, it equals eager execution bit for
@@ -114,6 +132,8 @@ def test_write_then_decode_graph_replay_equals_eager_and_oracle(name):
     cfg = msa.config_for(base)
     T = w.num_tokens
     bufs = {kk: vv.clone() for kk, vv in w.__dict__.items() if isinstance(vv, torch.Tensor)}
+    if w.k_pages.data_ptr() == w.v_pages.data_ptr():   # NVFP4: one pool for K and V
+        bufs["v_pages"] = bufs["k_pages"]
     rows = [t.clone() for t in _rows(base, T, seed=80)]
     sa = msa.SparseAttention(cfg)
 
