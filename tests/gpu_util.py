@@ -10,11 +10,13 @@ from oracle_io import oracle_local_blocks, run_oracle, selected_array, to_np
 
 # Acceptance bounds: selection bit-exact; out max |err| <= 1e-2 and mean |err|
 # <= 1e-3 against fp64 (bf16 output rounding alone is ~4e-3 relative); LSE
-# within 1e-3.  NVFP4 KV (values up to 6 x the block scale, outputs up to ~4.5
-# here) adds 2^-8 |o| (at least half a bf16 ulp of the reference) to the max bound:
-# the output is bf16, and at |o| in [4, 8) rounding alone reaches 2^-6.
+# within 1e-3.  Inputs whose outputs reach |o| > 2.5 -- NVFP4 KV (values up to
+# 6 x the block scale, outputs up to ~4.5 here) and peaked softmaxes that pick
+# out single value rows -- add 2^-8 |o| (at least half a bf16 ulp of the
+# reference) to the max bound: the output is bf16, and at |o| in [4, 8)
+# rounding alone reaches 2^-6.
 OUT_MAX, OUT_MEAN, LSE_MAX = 1e-2, 1e-3, 1e-3
-NVFP4_OUT_REL = 2.0 ** -8
+BF16_OUT_REL = 2.0 ** -8
 
 
 def run_gpu(w: wl.Workload, **cfg_overrides):
@@ -26,10 +28,14 @@ def run_gpu(w: wl.Workload, **cfg_overrides):
     return sa
 
 
-def compare(w: wl.Workload, sa, ref, tokens=None, kv_heads=None):
+def compare(w: wl.Workload, sa, ref, tokens=None, kv_heads=None, out_rel=None):
     """Element-wise comparison of the GPU results with the oracle's over the
-    computed (token, KV head) pairs.  Returns the error statistics."""
+    computed (token, KV head) pairs.  Returns the error statistics.  out_rel:
+    the bf16-rounding allowance (times |o|) on the max bound; by default
+    BF16_OUT_REL for NVFP4 KV, else none."""
     spec = w.spec
+    if out_rel is None:
+        out_rel = BF16_OUT_REL if spec.kv_dtype == "nvfp4" else 0.0
     T = w.num_tokens
     G = spec.group
     tokens = range(T) if tokens is None else tokens
@@ -49,8 +55,8 @@ def compare(w: wl.Workload, sa, ref, tokens=None, kv_heads=None):
             hs = slice(h * G, (h + 1) * G)
             d = np.abs(out[t, hs] - ref["out"][t, hs])
             errs.append(d.ravel())
-            if spec.kv_dtype == "nvfp4":
-                d = np.maximum(d - NVFP4_OUT_REL * np.abs(ref["out"][t, hs]), 0.0)
+            if out_rel:
+                d = np.maximum(d - out_rel * np.abs(ref["out"][t, hs]), 0.0)
             maxerrs.append(d.ravel())
             lerrs.append(np.abs(lse[t, hs] - ref["lse"][t, hs]))
     e = np.concatenate(errs)
@@ -113,7 +119,7 @@ def compare_sampled(w: wl.Workload, sa, samples):
         le = np.abs(lse[t, h * G:(h + 1) * G] - ref["lse"][t - q0])
         em = e
         if spec.kv_dtype == "nvfp4":
-            em = np.maximum(e - NVFP4_OUT_REL * np.abs(ref["out"][t - q0]), 0.0)
+            em = np.maximum(e - BF16_OUT_REL * np.abs(ref["out"][t - q0]), 0.0)
         worst["out_max"] = max(worst["out_max"], float(em.max()))
         worst["out_mean"] = max(worst["out_mean"], float(e.mean()))
         worst["lse_max"] = max(worst["lse_max"], float(le.max()))

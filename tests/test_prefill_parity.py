@@ -12,7 +12,7 @@ import torch
 import block_sparse_paged_msa_gb300 as msa
 import oracle
 from block_sparse_paged_msa_gb300 import workloads as wl
-from gpu_util import compare, compare_sampled, run_gpu
+from gpu_util import BF16_OUT_REL, compare, compare_sampled, run_gpu
 from oracle_io import run_oracle, to_np
 
 pytestmark = pytest.mark.gpu
@@ -61,6 +61,25 @@ def test_small_nvfp4_prefill_every_element(kw):
     assert msa.check_device_error(sa.ws) == 0
     print(compare(w, sa, run_oracle(w.to("cpu"))))
     _csr_matches_oracle(w, sa)
+
+
+@pytest.mark.parametrize("half,mult", [(1, 2.5), (1, 12.0), (0, 12.0)],
+                         ids=["late_x2.5", "late_x12", "early_x12"])
+def test_prefill_score_spread_across_a_block(half, mult):
+    """Keys 64..127 (or 0..63) of every page scaled up: a tile row's later
+    64-key chunk then tops the first chunk's max by far (x12: the softmax
+    reference moves up and the first chunk's P is rescaled), by about the
+    rescale threshold (x2.5: both paths, P values up to 4 against a stale
+    reference), or the first chunk dominates (early).  Compared on every
+    element; the peaked softmax returns near single value rows (|o| up to
+    ~4.5), so the max bound carries the bf16 output rounding allowance."""
+    spec = wl.small("prefill")
+    w = wl.make_workload(spec, device="cuda")
+    sl = slice(64, 128) if half else slice(0, 64)
+    w.k_pages[:, :, sl, :] = (w.k_pages[:, :, sl, :].float() * mult).to(torch.bfloat16)
+    sa = run_gpu(w)
+    assert msa.check_device_error(sa.ws) == 0
+    print(compare(w, sa, run_oracle(w.to("cpu")), out_rel=BF16_OUT_REL))
 
 
 def test_prefill_whole_sequence_is_dense_causal():
