@@ -463,15 +463,14 @@ def _cache_write_cost(msa, sa, w, spec, stream, n):
     """The K / V / index-key cache write that precedes a step (msa_cache_write,
     slots from the plan), timed alone over n calls after the step's plan: it is
     not part of the timed step.  Algorithmic bytes: the new rows read (bf16)
-    and written (bf16 or e4m3 K / V, bf16 index keys)."""
+    and written (bf16, e4m3 or NVFP4 K / V rows, bf16 index keys)."""
     c = sa.cfg
     T = w.num_tokens
-    if spec.kv_dtype == "nvfp4":
-        return None                  # the cache write has no NVFP4 form
     k, v, idx_k = wl.new_token_rows(spec, msa.ops.max_tokens(c), seed=spec.seed + 500,
                                     device=w.q.device)
-    elem = 1 if spec.kv_dtype == "fp8_e4m3" else 2
-    per = spec.num_kv_heads * (2 * spec.head_dim * (2 + elem) + 2 * spec.index_dim * 2)
+    D = spec.head_dim
+    row = {"fp8_e4m3": D, "nvfp4": D // 2 + D // 16}.get(spec.kv_dtype, 2 * D)   # stored K / V row
+    per = spec.num_kv_heads * (2 * D * 2 + 2 * row + 2 * spec.index_dim * 2)
     msa.plan(c, w.seq_lens, w.block_table, sa.ws, w.cu_seqlens_q if sa.prefill else None)
     call = lambda: msa.cache_write(c, sa.ws, k, v, idx_k, w.k_pages, w.v_pages,  # noqa: E731
                                    w.idx_k_pages)
