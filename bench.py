@@ -459,6 +459,34 @@ def _e2e(msa, sa, w, cfg, dev, stream, K, warmup, world):
     return Ke, e2e_ms, h2d, d2h
 
 
+def _device_times(calls, stream, n=20, reps=5):
+    """Device time per launch of each call of the step: the call repeated n
+    times in a CUDA graph (every call of the step is idempotent on its inputs),
+    the median of `reps` replays divided by n.  Without the host launch that
+    a per-call event pair also brackets."""
+    out = {}
+    for name, fn in calls:
+        graph, side = torch.cuda.CUDAGraph(), torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(n):
+                    fn()
+        stream.wait_stream(side)
+        graph.replay()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / n)
+        out[name] = sorted(ts)[reps // 2]
+        del graph
+    return out
+
+
 def _cache_write_cost(msa, sa, w, spec, stream, n):
     """The K / V / index-key cache write that precedes a step (msa_cache_write,
     slots from the plan), timed alone over n calls after the step's plan: it is
@@ -594,6 +622,7 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False, dense_sparse=
     assert msa.check_device_error(sa.ws) == 0
     per_kernel = {n: sum(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(Kb)) / Kb
                   for i, n in enumerate(names)}
+    per_kernel_dev = _device_times(calls, stream)
     e2e_res = _e2e(msa, sa, w, cfg, dev, stream, K, warmup, world) if e2e else None
     cw = _cache_write_cost(msa, sa, w, spec, stream, Kb)
     ia = _index_attention_cost(msa, sa, w, spec, stream, min(Kb, 50)) if e2e else None
@@ -620,7 +649,11 @@ def measure(spec, steps, warmup, dev, world, clock_gpu, e2e=False, dense_sparse=
                                    if dense_sparse else "sparse (selected lists)")},
         "kernels_ms": per_kernel,
         "kernels_ms_note": ("dominant kernel timed in the timed region; the others in "
-                            f"{Kb} further steps with every call bracketed by events"),
+                            f"{Kb} further steps with every call bracketed by events "
+                            "(the host launch of a short call shows in its time)"),
+        "kernels_device_ms": per_kernel_dev,
+        "kernels_device_ms_note": ("each call of the step alone, 20 launches back to back "
+                                   "replayed from a CUDA graph: device time per launch"),
         "gpu_launches": sum(launches_per_call(n, spec) for n in names) * K,
         "clocks": clk.summary(),
         "cache_write": cw,
@@ -715,7 +748,8 @@ def run_ours(args, rank, world, local_rank):
             r, wo = measure(o.replace(seed=o.seed + rank), K, W, dev, world, clock_gpu,
                             dense_sparse=form == "dense_sparse")
             keep = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "dtype",
-                    "roofline", "kernels_ms", "kernel_gbs", "kernel_tflops", "step_hbm",
+                    "roofline", "kernels_ms", "kernels_device_ms", "kernel_gbs",
+                    "kernel_tflops", "step_hbm",
                     "clocks", "gpu_launches", "config", "cache_write")
             result["workloads"][name] = {k: r[k] for k in keep if k in r}
             del wo
