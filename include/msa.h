@@ -231,7 +231,8 @@ msa_status msa_plan_from_req_to_token(const msa_config* cfg, int32_t batch,
  * amax / (6 * scale), each element the E2M1 code of x / (e4m3(scale byte) *
  * scale), every division and product one IEEE fp32 operation and every code
  * round-to-nearest-even, saturating; a block whose scale code is 0 stores zero
- * codes.
+ * codes.  E2M1 has no NaN: a NaN element is stored as +6 (its block's scale
+ * comes from the other elements).
  * Tokens of idle requests are skipped.  A slot outside [0, num_pages * P) is
  * skipped and sets MSA_DEVERR_PAGE_RANGE.  All pointers 16-byte aligned.
  */
