@@ -124,8 +124,9 @@ def test_prefill_full_size_sampled(name):
     assert torch.isfinite(sa.out[:T].float()).all()
 
 
-def test_prefill_graph_replay_equals_eager():
-    base = wl.small("prefill")
+@pytest.mark.parametrize("name", ["prefill", "nvfp4_prefill"])
+def test_prefill_graph_replay_equals_eager(name):
+    base = wl.small(name)
     w = wl.make_workload(base, device="cuda")
     cfg = msa.config_for(base)
     sa = msa.SparseAttention(cfg)
