@@ -112,29 +112,52 @@ struct ItemBlocks {
   int page, ntok;     // this lane's slot
 };
 
-__device__ __forceinline__ ItemBlocks item_blocks(const WsView& ws, const DecodeArgs& a, int t,
-                                                  int h, int s, int r, int pos, int lane) {
-  ItemBlocks b;
+// This lane's raw slot entry, loaded from the item's indices alone (for a
+// token of the step, t < num_tokens) so that the load overlaps the token
+// metadata reads: sparse form, the selected block; dense form, the page and
+// the keys left from the slot on.
+struct SlotRaw {
+  int v0, v1;
+  bool in;            // the lane holds a slot of the item
+};
+
+__device__ __forceinline__ SlotRaw slot_raw(const DecodeArgs& a, bool step_token, int t, int h,
+                                            int s, int lane) {
+  SlotRaw x;
   const int slot0 = s * a.bps;
-  const int nslot = min(a.bps, a.S - slot0);
+  x.in = step_token && lane < min(a.bps, a.S - slot0);
+  x.v0 = -1;
+  x.v1 = 0;
+  if (x.in) {
+    const int64_t row = (int64_t)t * a.Hkv + h;
+    if (a.page_table != nullptr) {
+      x.v0 = a.page_table[row * a.S + slot0 + lane];
+      x.v1 = a.dense_len[row] - (slot0 + lane) * kBlock;
+    } else {
+      x.v0 = a.selected[row * a.S + slot0 + lane];
+    }
+  }
+  return x;
+}
+
+__device__ __forceinline__ ItemBlocks item_blocks(const WsView& ws, const DecodeArgs& a,
+                                                  const SlotRaw& x, int r, int pos, int lane) {
+  ItemBlocks b;
   b.page = -1;
   b.ntok = 0;
   bool bad = false;
-  if (lane < nslot) {
-    const int64_t row = (int64_t)t * a.Hkv + h;
+  if (x.in) {
     if (a.page_table != nullptr) {
-      const int n = a.dense_len[row] - (slot0 + lane) * kBlock;
-      if (n > 0) {
-        const int pg = a.page_table[row * a.S + slot0 + lane];
-        if (pg >= 0 && pg < a.num_pages) {
-          b.page = pg;
-          b.ntok = min(kBlock, n);
+      if (x.v1 > 0) {
+        if (x.v0 >= 0 && x.v0 < a.num_pages) {
+          b.page = x.v0;
+          b.ntok = min(kBlock, x.v1);
         } else {
           bad = true;
         }
       }
     } else {
-      const int j = a.selected[row * a.S + slot0 + lane];
+      const int j = x.v0;
       if (j >= 0 && j * kBlock <= pos) {
         b.page = ws.block_table[(int64_t)r * a.max_blocks + j];
         b.ntok = min(kBlock, pos + 1 - j * kBlock);
@@ -151,15 +174,18 @@ struct Item {
   bool active;
 };
 
-__device__ __forceinline__ Item item_of(const WsView& ws, const DecodeArgs& a, int idx) {
+// Work item idx; num_tokens = the step's tokens (the plan's header, read once).
+// The request and the position are independent loads.
+__device__ __forceinline__ Item item_of(const WsView& ws, const DecodeArgs& a, int idx,
+                                        int num_tokens) {
   Item it;
   it.s = idx % a.nsplit;
   it.h = (idx / a.nsplit) % a.Hkv;
   it.t = idx / (a.nsplit * a.Hkv);
-  it.active = it.t < ws.hdr->num_tokens;
-  it.r = it.active ? ws.tok_req[it.t] : -1;
-  it.active = it.active && it.r >= 0;
-  it.pos = it.active ? ws.tok_pos[it.t] : -1;
+  const bool in = it.t < num_tokens;
+  it.r = in ? ws.tok_req[it.t] : -1;
+  it.pos = in ? ws.tok_pos[it.t] : -1;
+  it.active = it.r >= 0;
   return it;
 }
 
@@ -263,7 +289,9 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
   uint8_t* qbuf = conv + (F16 ? kConsumers * kConvBytes : 0);   // kItems x G x 256 B
   float* merge = reinterpret_cast<float*>(qbuf + kItems * a.G * 256);
   __shared__ __align__(8) uint64_t full_bar[NST], empty_bar[NST];
-  __shared__ __align__(8) uint64_t item_full[kItems], item_empty[kItems];
+  // item_full: a record and its Q rows (consumers); meta_full: the record
+  // alone (the loader, which needs only the pages)
+  __shared__ __align__(8) uint64_t item_full[kItems], item_empty[kItems], meta_full[kItems];
   __shared__ ItemMeta meta[kItems];
   __shared__ float red_m[kConsumers][16], red_l[kConsumers][16];
 
@@ -275,6 +303,7 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
     }
     for (int i = 0; i < kItems; ++i) {
       mbar_init(&item_full[i], 1);
+      mbar_init(&meta_full[i], 1);
       mbar_init(&item_empty[i], kConsumers + 1);   // consumers + loader
     }
     fence_barrier_init();
@@ -293,15 +322,21 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
     uint32_t iphase = 0;
     int nph[kItems] = {0, 0};       // phases armed on item_full[s]
     int qlast[kItems] = {-1, -1};   // phase of the last Q copy on item_full[s]
+    // the first item of every CTA is its own index (no counter round trip at
+    // the start); the rest come from the counter, after the first gridDim.x
     auto grab = [&]() {
       int i = 0;
       if (lane == 0) i = atomicAdd(&ws.hdr->work_next, 1);
-      return __shfl_sync(0xffffffffu, i, 0);
+      return (int)gridDim.x + __shfl_sync(0xffffffffu, i, 0);
     };
-    for (int idx = grab(); idx < a.n_items; idx = grab()) {
-      const Item it = item_of(ws, a, idx);
+    const int num_tokens = ws.hdr->num_tokens;
+    for (int idx = (int)blockIdx.x; idx < a.n_items; idx = grab()) {
+      const int tt = idx / (a.nsplit * a.Hkv);
+      const SlotRaw raw = slot_raw(a, tt < num_tokens, tt, (idx / a.nsplit) % a.Hkv,
+                                   idx % a.nsplit, lane);
+      const Item it = item_of(ws, a, idx, num_tokens);
       if (!it.active) continue;
-      const ItemBlocks bl = item_blocks(ws, a, it.t, it.h, it.s, it.r, it.pos, lane);
+      const ItemBlocks bl = item_blocks(ws, a, raw, it.r, it.pos, lane);
       if (lane == 0) mbar_wait(&item_empty[islot], iphase ^ 1u, ws.hdr);
       __syncwarp();
       if ((bl.mask >> lane) & 1u) {
@@ -317,6 +352,7 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
       }
       __syncwarp();
       if (lane == 0) {
+        mbar_arrive(&meta_full[islot]);              // the loader may start on the pages
         const uint32_t qbytes = (uint32_t)a.G * kHeadDim * 2;
         mbar_arrive_expect_tx(&item_full[islot], qbytes);
         bulk_load(qbuf + islot * qbytes,
@@ -329,6 +365,7 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
     if (lane == 0) {                                      // end-of-work record
       mbar_wait(&item_empty[islot], iphase ^ 1u, ws.hdr);
       meta[islot].t = -1;
+      mbar_arrive(&meta_full[islot]);
       mbar_arrive(&item_full[islot]);
       ++nph[islot];
       if (*reinterpret_cast<volatile int*>(&ws.hdr->err) & MSA_DEVERR_TIMEOUT) {
@@ -354,7 +391,7 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
       uint32_t phase = 0, iphase = 0;
       int nload = 0;                 // stage arms (one K or V tile each)
       for (;;) {
-        mbar_wait(&item_full[islot], iphase, ws.hdr);
+        mbar_wait(&meta_full[islot], iphase, ws.hdr);
         if (meta[islot].t < 0) break;
         const int nblk = meta[islot].nblk, h = meta[islot].h;
         for (int bi = 0; bi < nblk; ++bi) {
