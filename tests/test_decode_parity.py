@@ -60,6 +60,28 @@ def test_split_sizes_agree(bps):
     compare(w, sa, ref)
 
 
+@pytest.mark.parametrize("name", ["medium_decode", "verify"])
+def test_step_batch_below_config_max(name):
+    """A step of 3 requests on a config sized for 8: the work items of the
+    missing tokens are skipped (no selected row of theirs is read); q and idx_q
+    are padded to the config's token count, as the binding requires."""
+    spec = (wl.small(name, batch=3) if name != "verify"
+            else wl.small(name, batch=3, seq_lens=(1500, 2000, 3001)))
+    w = wl.make_workload(spec, device="cuda")
+    ref = run_oracle(w.to("cpu"))
+    cfg = msa.config_for(spec, max_batch=8)
+    sa = msa.SparseAttention(cfg)
+    T, Tmax = w.num_tokens, msa.ops.max_tokens(cfg)
+    q = torch.full((Tmax,) + tuple(w.q.shape[1:]), float("nan"), dtype=w.q.dtype, device="cuda")
+    idx_q = torch.zeros((Tmax,) + tuple(w.idx_q.shape[1:]), dtype=w.idx_q.dtype, device="cuda")
+    q[:T] = w.q
+    idx_q[:T] = w.idx_q
+    sa.run(w.seq_lens, w.block_table, idx_q, w.idx_k_pages, q, w.k_pages, w.v_pages)
+    torch.cuda.synchronize()
+    assert msa.check_device_error(sa.ws) == 0
+    print(compare(w, sa, ref))
+
+
 def test_block_boundaries_and_short_requests():
     # exact multiples of the block, one token, within init+local, one past a block
     spec = wl.small("medium_decode", seq_lens=(128, 1, 384, 129, 1024, 255), seq_len_range=None,
