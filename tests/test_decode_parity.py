@@ -183,3 +183,18 @@ def test_nvfp4_group_16_index_64_and_verify_every_element(q_len):
                     seq_lens=(700, 127 + q_len, 2900), seq_len_range=None, batch=3,
                     num_pages=64, seed=1300 + q_len)
     _full_case(spec)
+
+
+@pytest.mark.parametrize("groups", [(32, 2), (4, 4)], ids=["g16", "g1"])
+@pytest.mark.parametrize("q_len", [1, 4])
+def test_fp8_groups_and_verify_every_element(groups, q_len):
+    """e4m3 K/V with 16 query heads per KV head (index dim 64) or one, alone and
+    with four speculative tokens per request (ragged, straddling a block
+    boundary): K feeds the fp16 MMAs from the tile, V is converted per warp,
+    k_scale / v_scale fold into the softmax scale and the output."""
+    hq, hkv = groups
+    spec = wl.small("fp8_decode", num_q_heads=hq, num_kv_heads=hkv,
+                    index_dim=64 if hq // hkv == 16 else 128, q_len=q_len,
+                    seq_lens=(700, 127 + q_len, 2900), seq_len_range=None, batch=3,
+                    num_pages=64, seed=1400 + 10 * q_len + hq)
+    _full_case(spec)
