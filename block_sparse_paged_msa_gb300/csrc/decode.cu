@@ -10,10 +10,12 @@
 //
 // Work item = (query token t, KV head h, split s); a split is a run of
 // consecutive slots of t's selected list.  Design (GB300):
-//  * a persistent grid (two 192-thread CTAs per SM) strides over the work
-//    items; in each CTA a scheduler warp resolves the next items (pages and
-//    visible rows of their blocks, the item's Q rows) into a small ring of
-//    item records, and a loader warp streams, for every selected block, the
+//  * a persistent grid (two 192-thread CTAs per SM) walks the work items
+//    (each CTA's first one is its own index, the rest come from a counter);
+//    in each CTA a scheduler warp resolves the next items (pages and visible
+//    rows of their blocks, the item's Q rows) into a small ring of item
+//    records, and a loader warp streams, as soon as a record is out, for
+//    every selected block, the
 //    block's K tile and V tile ([128 tokens][128 dims], contiguous per page and
 //    KV head in the HND pool: 32 KiB bf16, 16 KiB e4m3) with 2-D TMA loads
 //    (128-byte swizzle) into a ring of shared-memory stages guarded by
@@ -314,10 +316,10 @@ decode_kernel(WsView ws, DecodeArgs a, const __grid_constant__ CUtensorMap tmap_
 
   if (warp == kScheduler) {
     // -------------------------------------------------------- scheduler
-    // Resolves each work item (token metadata -> selected slots -> pages) and
+    // Resolves each work item (token metadata and selected slots -> pages) and
     // publishes it with the item's Q rows, up to kItems ahead of the others.
-    // Items are handed out dynamically (an atomic counter in the workspace
-    // header), so CTAs that drew cheap items take more of them.
+    // After its first item, a CTA takes items from an atomic counter in the
+    // workspace header, so CTAs that drew cheap items take more of them.
     int islot = 0;
     uint32_t iphase = 0;
     int nph[kItems] = {0, 0};       // phases armed on item_full[s]
