@@ -14,13 +14,12 @@
 //    (each CTA's first one is its own index, the rest come from a counter);
 //    in each CTA a scheduler warp resolves the next items (pages and visible
 //    rows of their blocks, the item's Q rows) into a small ring of item
-//    records, and a loader warp streams, as soon as a record is out, for
-//    every selected block, the
-//    block's K tile and V tile ([128 tokens][128 dims], contiguous per page and
-//    KV head in the HND pool: 32 KiB bf16, 16 KiB e4m3) with 2-D TMA loads
-//    (128-byte swizzle) into a ring of shared-memory stages guarded by
-//    mbarriers -- so the copies of the next items are already in flight while
-//    the current one is being finished;
+//    records, and a loader warp streams, as soon as a record is out, each
+//    selected block's K tile and V tile ([128 tokens][128 dims], contiguous
+//    per page and KV head in the HND pool: 32 KiB bf16, 16 KiB e4m3) with 2-D
+//    TMA loads (128-byte swizzle) into a ring of shared-memory stages guarded
+//    by mbarriers -- so the copies of the next items are already in flight
+//    while the current one is being finished;
 //  * four consumer warps share every tile: warp w owns tokens [32w, 32w+32),
 //    runs S = Q K^T and O += P V on m16n8k16 tensor-core MMAs with the G =
 //    H_q / H_kv query heads of the group as the M side (rows >= G are zero),
