@@ -22,7 +22,9 @@
 // transpose-reduce butterfly (one shuffle per row instead of log2(lanes)).
 // The grid is persistent (SMs x resident CTAs) and walks the flattened
 // (request, block, head) list, so ragged sequence lengths balance by blocks,
-// not by requests.
+// not by requests; a unit finds its request by a binary search over the
+// requests' first blocks, or, for up to 32 requests, by one ballot over them
+// kept in the warp's registers.
 #include <algorithm>
 #include <mutex>
 
@@ -108,19 +110,29 @@ index_score_kernel(WsView ws, int Hkv, int max_blocks, int max_tokens,
   const int batch = ws.hdr->batch;
   const int total = ws.hdr->total_blocks * Hkv * kParts;
   const int warps = gridDim.x * (kThreads / 32);
+  // up to 32 requests: lane i keeps request i's first flat block, and a unit
+  // finds its request with one ballot instead of a search through memory
+  const bool small_batch = batch <= 32;
+  const int cu_lane = small_batch && lane < batch ? ws.req_cu_nb[lane] : 0x7fffffff;
   for (int item = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); item < total;
        item += warps) {
     const int h = item % Hkv;
     const int part = (item / Hkv) % kParts;
     const int b = item / (Hkv * kParts);
     const int r0 = part * (kBlock / kParts);   // this unit's rows [r0, r0 + kBlock / kParts)
-    int lo = 0, hi = batch - 1;  // request of flat block b
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (ws.req_cu_nb[mid] <= b) lo = mid; else hi = mid - 1;
+    int r, j;                    // request of flat block b, and its block
+    if (small_batch) {
+      r = __popc(__ballot_sync(0xffffffffu, cu_lane <= b)) - 1;
+      j = b - __shfl_sync(0xffffffffu, cu_lane, r);
+    } else {
+      int lo = 0, hi = batch - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ws.req_cu_nb[mid] <= b) lo = mid; else hi = mid - 1;
+      }
+      r = lo;
+      j = b - ws.req_cu_nb[r];
     }
-    const int r = lo;
-    const int j = b - ws.req_cu_nb[r];
     const int page = ws.block_table[(int64_t)r * max_blocks + j];
     const int qs = ws.req_qstart[r];
     float* out = scores + ((int64_t)qs * Hkv + h) * max_blocks + j;
