@@ -198,3 +198,28 @@ def test_fp8_groups_and_verify_every_element(groups, q_len):
                     seq_lens=(700, 127 + q_len, 2900), seq_len_range=None, batch=3,
                     num_pages=64, seed=1400 + 10 * q_len + hq)
     _full_case(spec)
+
+
+def _combo(seed):
+    """A seeded draw of one small decode / verify configuration."""
+    rng = np.random.default_rng(seed)
+    kv = ["medium_decode", "fp8_decode", "nvfp4_decode"][int(rng.integers(3))]
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([1, 2, 4, 8, 16]))
+    q_len = int(rng.integers(1, 5))
+    batch = int(rng.integers(1, 5))
+    lens = tuple(int(x) for x in rng.integers(q_len, 2600, size=batch))
+    return dict(name=kv, num_q_heads=g * hkv, num_kv_heads=hkv, q_len=q_len,
+                index_dim=int(rng.choice([64, 128])), topk_blocks=int(rng.choice([0, 3, 16])),
+                seq_lens=lens, seq_len_range=None, batch=batch, num_pages=96, seed=seed)
+
+
+@pytest.mark.parametrize("seed", range(1500, 1512))
+def test_random_configuration_sweep_every_element(seed):
+    """Seeded draws over KV type (bf16, e4m3, NVFP4), query heads per KV head
+    (1..16), KV heads, new tokens per request (1..4, verify from 2), index dim,
+    top-k (0, 3, 16) and ragged lengths: every combination the kernels accept
+    agrees with the oracle on every element."""
+    kw = _combo(seed)
+    spec = wl.small(kw.pop("name"), **kw)
+    _full_case(spec)

@@ -156,3 +156,33 @@ def test_prefill_graph_replay_equals_eager(name):
         T = w2.num_tokens
         assert torch.equal(g_rp, eager.row_ptr)
         assert torch.equal(g_out[:T], eager.out[:T]) and torch.equal(g_lse[:T], eager.lse[:T])
+
+
+def _pcombo(seed):
+    """A seeded draw of one small chunked-prefill configuration."""
+    rng = np.random.default_rng(seed)
+    kv = ["prefill", "nvfp4_prefill"][int(rng.integers(2))]
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([1, 2, 4, 8, 16]))
+    q_len = int(rng.choice([5, 64, 129, 300]))
+    batch = int(rng.integers(1, 4))
+    lens = tuple(int(x) for x in rng.integers(q_len, 1800, size=batch))
+    return dict(name=kv, num_q_heads=g * hkv, num_kv_heads=hkv, q_len=q_len,
+                index_dim=int(rng.choice([64, 128])), topk_blocks=int(rng.choice([0, 2, 16])),
+                seq_lens=lens, batch=batch, num_pages=64, seed=seed)
+
+
+@pytest.mark.parametrize("seed", range(1600, 1608))
+def test_random_prefill_sweep_every_element(seed):
+    """Seeded draws over KV type (bf16, NVFP4), query heads per KV head, KV
+    heads, chunk length (5 .. 300 new tokens per request), index dim, top-k and
+    ragged prefixes: every element agrees with the oracle, and the CSR with the
+    oracle's."""
+    kw = _pcombo(seed)
+    spec = wl.small(kw.pop("name"), **kw)
+    w = wl.make_workload(spec, device="cuda")
+    sa = run_gpu(w)
+    assert sa.prefill
+    assert msa.check_device_error(sa.ws) == 0
+    print(compare(w, sa, run_oracle(w.to("cpu"))))
+    _csr_matches_oracle(w, sa)
