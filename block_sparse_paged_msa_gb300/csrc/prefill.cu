@@ -167,8 +167,15 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(int32_t* __restrict__ ro
 // rows (tokens x GQA heads); msa_build_k2q_csr writes the first item of every
 // row (ws.sched) and the items ordered largest first (ws.item_order: CSR row,
 // first and end entry of each), so the huge rows of the init / local blocks
-// are split and the CTAs' round-robin shares come out even.
-constexpr int kTilesPerItem = 32;
+// are split and the CTAs' round-robin shares come out even.  The item size
+// sets how evenly the round-robin lands: over the sorted items of the
+// 4 x (16 384 + 2 048)-token prefill, the busiest CTA's share of tiles is 1.09
+// x the mean with items of 32 M-tiles and 1.02 x with 20 (simulated from the
+// step's CSR; measured 0.932 -> 0.889 ms per launch with the issue order below).
+constexpr int kTilesPerItem = 20;
+// the workspace bounds the items by one per 128 CSR entries per row (an item
+// holds kTilesPerItem * 128 / G >= 8 kTilesPerItem tokens, G <= 16)
+static_assert(kTilesPerItem * 8 >= 128, "item bound of the workspace layout");
 constexpr int kLoaderWarps = 3;          // Q loaders (TMA issue from one warp is slow)
 constexpr int kTcThreads = (9 + kLoaderWarps) * 32;   // 2 softmax warpgroups, MMA issuer
 constexpr int kTileBytes = kBlock * kHeadDim * 2;
@@ -263,7 +270,8 @@ __device__ __forceinline__ void fp4_slot_to_tile(const uint8_t* slot, uint8_t* t
 //            TMA tile stores into the partials, LSE beside them.
 // TMEM: per warpgroup 128 columns of S / P and 128 of O (512 in all).  P
 // never touches shared memory.  The issuer polls both warpgroups and serves
-// whichever is ready; the loaders run ahead across items.
+// whichever is ready, each O = P V before any S (P V completion gates the
+// warpgroup's epilogue and its next S); the loaders run ahead across items.
 template <bool FP4>
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
@@ -555,6 +563,22 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
           }
 #pragma unroll
           for (int w = 0; w < 2; ++w) {
+            if (vt_ok && nP[w] < nS[w] && mbar_test_wait(&p_ready[w], (uint32_t)(kP[w] & 1))) {
+              tc_fence_after();
+              // K step ks: P columns +8 ks, V rows 16 ks (+2 KB)
+              const uint32_t ta = tbase + 256 * w, dt = ta + 128;
+              umma_ts<false>(dt, ta, vlo, vhi, idesc_o);
+#pragma unroll
+              for (int ks = 1; ks < 8; ++ks)
+                umma_ts<true>(dt, ta + 8 * ks, vlo + 128 * ks, vhi, idesc_o);
+              umma_commit(&o_ready[w]);
+              ++kP[w];
+              ++nP[w];
+              did = true;
+            }
+          }
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {
             // S_k overwrites P_{k-1}: only once O_{k-1} = P_{k-1} V completed
             if (nS[w] < want[w] && (!FP4 || vt_ok) &&
                 mbar_test_wait(&q_full[w], (uint32_t)(kS[w] & 1)) &&
@@ -576,19 +600,6 @@ prefill_tc_kernel(WsView ws, PrefillArgs a, const __grid_constant__ CUtensorMap 
               ++kS[w];
               ++nS[w];
               if (nS[0] == want[0] && nS[1] == want[1]) umma_commit(&k_free);   // last S
-              did = true;
-            }
-            if (vt_ok && nP[w] < nS[w] && mbar_test_wait(&p_ready[w], (uint32_t)(kP[w] & 1))) {
-              tc_fence_after();
-              // K step ks: P columns +8 ks, V rows 16 ks (+2 KB)
-              const uint32_t ta = tbase + 256 * w, dt = ta + 128;
-              umma_ts<false>(dt, ta, vlo, vhi, idesc_o);
-#pragma unroll
-              for (int ks = 1; ks < 8; ++ks)
-                umma_ts<true>(dt, ta + 8 * ks, vlo + 128 * ks, vhi, idesc_o);
-              umma_commit(&o_ready[w]);
-              ++kP[w];
-              ++nP[w];
               did = true;
             }
           }
