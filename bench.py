@@ -69,10 +69,10 @@ NCU_TRAFFIC_BYTES = {
     # 371.6 MB (368.3 read + 3.4 written) for 367.7 MB algorithmic, scaled by
     # bytes to a full medium-decode launch (1.2608 GB)
     ("medium_decode", "index_score"): 1.2743e9,
-    # full-size one-pass capture of the prefill tile kernel (work items taken
-    # request by request): 690.4 MB read (Q gathers now mostly L2 hits, K/V
-    # tiles) + 2 667.3 MB written (the fp16 partials)
-    ("prefill", "sparse_prefill"): 3.3577e9,
+    # full-size one-pass capture of the prefill tile kernel (work items of 20
+    # M-tiles taken request by request): 649.1 MB read (Q gathers mostly L2
+    # hits, K/V tiles) + 2 666.3 MB written (the fp16 partials)
+    ("prefill", "sparse_prefill"): 3.3154e9,
 }
 
 
